@@ -1,0 +1,492 @@
+/*
+ * oracle.cpp -- plain, slow, double-precision CPU oracle for the draft-block
+ * select-and-verify step of DFlash 2 block drafting.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg load this library. The CUDA library never
+ * links, includes or calls it; the two share no header, helper, table or
+ * constant. Its inputs are the caller's raw bf16 (uint16 bit patterns) or
+ * fp32 bytes; every element is widened to double (exact) before any
+ * arithmetic, and every result is computed in double.
+ *
+ * Sources, cited by page title and section / equation / table:
+ *   [Blog]   "DFlash 2: Keep Drafting Parallel" (Chinese translation of the
+ *            Inco AI blog, "DFlash 2：保持并行草案生成")
+ *   [ZhTW]   "DFlash 2 讓 Qwen3.8-27B 快了兩倍：同模型、同輸出、同一張卡，純粹靠更聰明的推理"
+ *   [Digest] "给 Qwen3.8-27B 配个"草稿加速器"：DFlash2 并行投机解码解读"
+ *
+ * What pins each function (tests/test_oracle_*.py):
+ *   orc_logits, orc_topk ..... numpy float64 matmul and lexsort on the same bytes
+ *   orc_gate ................. closed-form special cases (zero weights, one-hot
+ *                              weights, sign flip); the sigmoid form itself is a
+ *                              reading (the pages name a "context gate" only)
+ *   orc_pair_scores .......... one-hot closed forms, linearity, A = 0 gives U
+ *   orc_path_viterbi ......... brute force over all K^(L-1) paths
+ *   orc_path_greedy .......... hand-worked golden lattice; A = 0 gives top-1
+ *   orc_verify_greedy ........ equality with target-argmax decoding
+ *   orc_verify_sampling ...... chi-square of emitted-token marginals against
+ *                              the target softmax; limiting cases
+ *   orc_philox4x64 ........... numpy.random.Philox raw output
+ *   accept length ............ closed form that reproduces the [Blog] Table 1
+ *                              verify lengths 4.27 / 6.79
+ *
+ * Tie rule everywhere: among equal values the lower token id wins.
+ */
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <vector>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+enum { ORC_BF16 = 0, ORC_FP32 = 1 };
+
+const double kInf = std::numeric_limits<double>::infinity();
+
+/* Exact widening of one stored element to double. */
+inline double widen(const void* p, int dtype, int64_t i) {
+  if (dtype == ORC_BF16) {
+    uint32_t bits = static_cast<uint32_t>(static_cast<const uint16_t*>(p)[i]) << 16;
+    float f;
+    std::memcpy(&f, &bits, sizeof f);
+    return static_cast<double>(f);
+  }
+  return static_cast<double>(static_cast<const float*>(p)[i]);
+}
+
+/* (value desc, id asc): true when candidate (va, ia) ranks before (vb, ib). */
+inline bool ranks_before(double va, int64_t ia, double vb, int64_t ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+inline double rel(double margin, double value) {
+  return margin / std::max(1.0, std::fabs(value));
+}
+
+/* ---- Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers:
+ * as easy as 1, 2, 3", SC'11). Ten rounds of the 4x64 Philox S-box keyed by
+ * a Weyl sequence. Written from the published definition. */
+const uint64_t kPhiloxM0 = 0xD2E7470EE14C6C93ULL;
+const uint64_t kPhiloxM1 = 0xCA5A826395121157ULL;
+const uint64_t kPhiloxW0 = 0x9E3779B97F4A7C15ULL;
+const uint64_t kPhiloxW1 = 0xBB67AE8584CAA73BULL;
+
+void philox4x64_10(const uint64_t in[4], const uint64_t key[2], uint64_t out[4]) {
+  uint64_t c0 = in[0], c1 = in[1], c2 = in[2], c3 = in[3];
+  uint64_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += kPhiloxW0;
+      k1 += kPhiloxW1;
+    }
+    unsigned __int128 p0 = static_cast<unsigned __int128>(kPhiloxM0) * c0;
+    unsigned __int128 p1 = static_cast<unsigned __int128>(kPhiloxM1) * c2;
+    uint64_t hi0 = static_cast<uint64_t>(p0 >> 64), lo0 = static_cast<uint64_t>(p0);
+    uint64_t hi1 = static_cast<uint64_t>(p1 >> 64), lo1 = static_cast<uint64_t>(p1);
+    uint64_t n0 = hi1 ^ c1 ^ k0;
+    uint64_t n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Uniform in (0,1) from the top 24 bits of a 64-bit word: exact in fp32 and fp64. */
+inline double u01(uint64_t x) {
+  return (static_cast<double>(x >> 40) + 0.5) * (1.0 / 16777216.0);
+}
+
+/* Counter layout shared by definition (not by code) with the GPU path:
+ *   key     = (seed, 0)
+ *   accept  : counter (0, t, b, 0), word 0           -- position t = 1..L-1
+ *   gumbel  : counter (v >> 2, t, b, 1), word v & 3  -- row t-1 verifies position t;
+ *             the bonus row L-1 uses t = L                                     */
+double uniform_accept(uint64_t seed, int64_t b, int t) {
+  uint64_t ctr[4] = {0ULL, static_cast<uint64_t>(t), static_cast<uint64_t>(b), 0ULL};
+  uint64_t key[2] = {seed, 0ULL};
+  uint64_t o[4];
+  philox4x64_10(ctr, key, o);
+  return u01(o[0]);
+}
+
+double uniform_gumbel(uint64_t seed, int64_t b, int t, int64_t v) {
+  uint64_t ctr[4] = {static_cast<uint64_t>(v) >> 2, static_cast<uint64_t>(t),
+                     static_cast<uint64_t>(b), 1ULL};
+  uint64_t key[2] = {seed, 0ULL};
+  uint64_t o[4];
+  philox4x64_10(ctr, key, o);
+  return u01(o[v & 3]);
+}
+
+/* log-sum-exp of z/T over one row, in double. */
+double row_lse(const void* Z, int zdtype, int64_t off, int64_t V, double T) {
+  double m = -kInf;
+  for (int64_t v = 0; v < V; ++v) m = std::max(m, widen(Z, zdtype, off + v) / T);
+  double s = 0.0;
+  for (int64_t v = 0; v < V; ++v) s += std::exp(widen(Z, zdtype, off + v) / T - m);
+  return m + std::log(s);
+}
+
+/* Gumbel-max draw from softmax(z/T) restricted to v != excl (excl < 0: none):
+ * argmax_v z_v/T + G_v with G_v = -log(-log U_v). The argmax of independent
+ * Gumbel-perturbed logits is an exact sample from the renormalised softmax
+ * (Gumbel 1954; the Gumbel-max trick). Returns the token and the relative
+ * gap between the two largest keys. */
+int64_t gumbel_argmax(const void* Z, int zdtype, int64_t off, int64_t V, double T, uint64_t seed,
+                      int64_t b, int t, int64_t excl, double* rel_gap) {
+  int64_t best = -1;
+  double bk = -kInf, second = -kInf;
+  for (int64_t v = 0; v < V; ++v) {
+    if (v == excl) continue;
+    double g = -std::log(-std::log(uniform_gumbel(seed, b, t, v)));
+    double key = widen(Z, zdtype, off + v) / T + g;
+    if (best < 0 || key > bk) {  // v increases, so strict '>' keeps the lower id on ties
+      second = bk;
+      bk = key;
+      best = v;
+    } else {
+      second = std::max(second, key);
+    }
+  }
+  *rel_gap = (second == -kInf) ? kInf : rel(bk - second, bk);
+  return best;
+}
+
+}  // namespace
+
+extern "C" {
+
+int orc_abi_version() { return 1; }
+
+/* Draft logits, [Blog] §"A lightweight path selector": U_t(b) is the drafter's
+ * own logit for b, i.e. the shared LM head applied to the position's hidden
+ * state. u[i][v] = sum_{k<d} h[rows[i]][k] * W[k][v], W stored [d][V].
+ * Each output is one dot product accumulated in k order; the vocabulary is
+ * split across threads only to use the cores. */
+int orc_logits(int dtype, const void* h, const void* W, int64_t d, int64_t V,
+               const int64_t* rows, int64_t n, double* u, int nthreads) {
+  if (d <= 0 || V <= 0 || n < 0 || (dtype != ORC_BF16 && dtype != ORC_FP32)) return -1;
+  std::vector<double> hd(static_cast<size_t>(n) * d);
+  for (int64_t i = 0; i < n; ++i)
+    for (int64_t k = 0; k < d; ++k) hd[i * d + k] = widen(h, dtype, rows[i] * d + k);
+  const int64_t CH = 512;
+  const int64_t nch = (V + CH - 1) / CH;
+  if (nthreads <= 0) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+  {
+    std::vector<double> wrow(CH);
+    std::vector<double> acc(static_cast<size_t>(n) * CH);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t c = 0; c < nch; ++c) {
+      const int64_t v0 = c * CH;
+      const int64_t w = std::min(CH, V - v0);
+      std::fill(acc.begin(), acc.end(), 0.0);
+      for (int64_t k = 0; k < d; ++k) {
+        for (int64_t j = 0; j < w; ++j) wrow[j] = widen(W, dtype, k * V + v0 + j);
+        for (int64_t i = 0; i < n; ++i) {
+          const double hk = hd[i * d + k];
+          double* a = acc.data() + i * CH;
+          for (int64_t j = 0; j < w; ++j) a[j] += hk * wrow[j];
+        }
+      }
+      for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = 0; j < w; ++j) u[i * V + v0 + j] = acc[i * CH + j];
+    }
+  }
+  return 0;
+}
+
+/* Keep top-K, [Blog] §"The right tokens are already there" and §"A lightweight
+ * path selector" (K = 16): the K largest logits of a row, ordered by
+ * (value desc, id asc). gap[i] = u_K - u_{K+1} (the boundary margin; +inf when
+ * V == K). */
+int orc_topk(const double* u, int64_t n, int64_t V, int K, int32_t* ids, double* U, double* gap) {
+  if (K <= 0 || V < K) return -1;
+  std::vector<int64_t> idx(V);
+  const int64_t keep = std::min<int64_t>(V, K + 1);
+  for (int64_t i = 0; i < n; ++i) {
+    const double* row = u + i * V;
+    for (int64_t v = 0; v < V; ++v) idx[v] = v;
+    std::partial_sort(idx.begin(), idx.begin() + keep, idx.end(), [row](int64_t a, int64_t b) {
+      return ranks_before(row[a], a, row[b], b);
+    });
+    for (int k = 0; k < K; ++k) {
+      ids[i * K + k] = static_cast<int32_t>(idx[k]);
+      U[i * K + k] = row[idx[k]];
+    }
+    gap[i] = (V > K) ? row[idx[K - 1]] - row[idx[K]] : kInf;
+  }
+  return 0;
+}
+
+/* Context gate H(h_t), [Blog] §"A lightweight path selector": the pages name a
+ * gate computed from the position's hidden state that decides which of the
+ * rank dimensions count; its form is not printed. Reading taken:
+ * g[i][j] = sigmoid(sum_k Wg[j][k] * h[rows[i]][k]), Wg stored [r][d]. */
+int orc_gate(int dtype, const void* h, const void* Wg, int64_t d, int64_t r,
+             const int64_t* rows, int64_t n, double* g) {
+  if (d <= 0 || r <= 0 || n < 0) return -1;
+  for (int64_t i = 0; i < n; ++i) {
+    for (int64_t j = 0; j < r; ++j) {
+      double x = 0.0;
+      for (int64_t k = 0; k < d; ++k) x += widen(Wg, dtype, j * d + k) * widen(h, dtype, rows[i] * d + k);
+      g[i * r + j] = 1.0 / (1.0 + std::exp(-x));
+    }
+  }
+  return 0;
+}
+
+/* Bilinear pair scores, [Blog] §"A lightweight path selector", eq.
+ * S_t(a,b) = U_t(b) + < A(a) (.) H(h_t), B(b) >, and [ZhTW] §2 (same eq.).
+ * P = L-1 draft positions, position t = p+1. The predecessor of position 1 is
+ * the last verified token x0 ("start from the last verified token"), so every
+ * a-row of p = 0 holds S_1(x0, .). For p >= 1 the predecessor a ranges over
+ * the candidates of position p. Output S[p][a][b]. */
+int orc_pair_scores(int dtype, const void* A, const void* Bt, int64_t r, int P, int K,
+                    const int32_t* ids, const double* U, const double* g, int32_t x0, double* S) {
+  if (r <= 0 || P < 1 || K < 1) return -1;
+  for (int p = 0; p < P; ++p) {
+    for (int a = 0; a < K; ++a) {
+      const int64_t tok_a = (p == 0) ? x0 : ids[(p - 1) * K + a];
+      for (int bb = 0; bb < K; ++bb) {
+        const int64_t tok_b = ids[p * K + bb];
+        double s = 0.0;
+        for (int64_t j = 0; j < r; ++j)
+          s += widen(A, dtype, tok_a * r + j) * g[p * r + j] * widen(Bt, dtype, tok_b * r + j);
+        S[(static_cast<int64_t>(p) * K + a) * K + bb] = U[p * K + bb] + s;
+      }
+    }
+  }
+  return 0;
+}
+
+/* Greedy traversal, [Blog] §"A lightweight path selector": from the last
+ * verified token, follow the best successor at each step.
+ * x_1 = argmax_b S_1(x0,b); x_t = argmax_b S_t(x_{t-1}, b).
+ * score = sum of the chosen S values (left to right). margin = smallest
+ * relative gap best-vs-second among the decisions taken. */
+int orc_path_greedy(int P, int K, const double* S, const int32_t* ids, int32_t* path,
+                    int32_t* path_idx, double* score, double* margin) {
+  if (P < 1 || K < 1) return -1;
+  int a = 0;
+  double total = 0.0, mm = kInf;
+  for (int p = 0; p < P; ++p) {
+    const double* row = S + (static_cast<int64_t>(p) * K + a) * K;
+    int best = 0;
+    for (int b = 1; b < K; ++b)
+      if (ranks_before(row[b], ids[p * K + b], row[best], ids[p * K + best])) best = b;
+    double second = -kInf;
+    for (int b = 0; b < K; ++b)
+      if (b != best) second = std::max(second, row[b]);
+    if (K > 1) mm = std::min(mm, rel(row[best] - second, row[best]));
+    path[p] = ids[p * K + best];
+    path_idx[p] = best;
+    total += row[best];
+    a = best;
+  }
+  *score = total;
+  *margin = mm;
+  return 0;
+}
+
+/* Viterbi max-sum, [ZhTW] §2 "Lightweight path selector (Path Selector)": one
+ * dynamic-programming sweep finds the best path through the lattice.
+ * delta_1(b) = S_1(x0,b); delta_t(b) = max_a [delta_{t-1}(a) + S_t(a,b)];
+ * backtrack from argmax_b delta_{L-1}(b). Ties: lower token id, also for the
+ * predecessor. margin = smallest relative best-vs-second gap among the
+ * decisions on the returned path (final choice and each predecessor). */
+int orc_path_viterbi(int P, int K, const double* S, const int32_t* ids, int32_t* path,
+                     int32_t* path_idx, double* score, double* margin) {
+  if (P < 1 || K < 1) return -1;
+  std::vector<double> delta(K), next(K);
+  std::vector<int> bp(static_cast<size_t>(P) * K, 0);
+  std::vector<double> bm(static_cast<size_t>(P) * K, kInf);
+  for (int b = 0; b < K; ++b) delta[b] = S[b];  // p = 0, a-row 0 holds S_1(x0, b)
+  for (int p = 1; p < P; ++p) {
+    for (int b = 0; b < K; ++b) {
+      int best = 0;
+      double bv = delta[0] + S[(static_cast<int64_t>(p) * K + 0) * K + b];
+      double second = -kInf;
+      for (int a = 1; a < K; ++a) {
+        const double v = delta[a] + S[(static_cast<int64_t>(p) * K + a) * K + b];
+        if (ranks_before(v, ids[(p - 1) * K + a], bv, ids[(p - 1) * K + best])) {
+          second = std::max(second, bv);
+          bv = v;
+          best = a;
+        } else {
+          second = std::max(second, v);
+        }
+      }
+      next[b] = bv;
+      bp[p * K + b] = best;
+      bm[p * K + b] = (K > 1) ? rel(bv - second, bv) : kInf;
+    }
+    delta.swap(next);
+  }
+  int fin = 0;
+  for (int b = 1; b < K; ++b)
+    if (ranks_before(delta[b], ids[(P - 1) * K + b], delta[fin], ids[(P - 1) * K + fin])) fin = b;
+  double second = -kInf;
+  for (int b = 0; b < K; ++b)
+    if (b != fin) second = std::max(second, delta[b]);
+  double mm = (K > 1) ? rel(delta[fin] - second, delta[fin]) : kInf;
+  int cur = fin;
+  for (int p = P - 1; p >= 0; --p) {
+    path[p] = ids[p * K + cur];
+    path_idx[p] = cur;
+    if (p > 0) {
+      mm = std::min(mm, bm[p * K + cur]);
+      cur = bp[p * K + cur];
+    }
+  }
+  *score = delta[fin];
+  *margin = mm;
+  return 0;
+}
+
+/* Greedy verification (T = 0), [ZhTW] §"The output is exactly the same" and
+ * [Digest] §5: output identical to target-argmax decoding. Row i of Z is the
+ * target's prediction after x_i (x_0 = last verified token), i = 0..L-1;
+ * y_i = argmax_v Z[i][v]. n = largest k <= L-1 with x_t == y_{t-1} for all
+ * t <= k. Emitted: x_1..x_n then y_n; accept_len = n + 1, which counts the
+ * verifier's own next token as [Blog] Table 1's caption does. Unused output
+ * slots are -1. */
+int orc_verify_greedy(int zdtype, const void* Z, int L, int64_t V, const int32_t* path,
+                      int32_t* out, int32_t* accept_len) {
+  if (L < 2 || V < 1) return -1;
+  std::vector<int64_t> y(L);
+  for (int i = 0; i < L; ++i) {
+    int64_t best = 0;
+    double bv = widen(Z, zdtype, static_cast<int64_t>(i) * V);
+    for (int64_t v = 1; v < V; ++v) {
+      const double z = widen(Z, zdtype, static_cast<int64_t>(i) * V + v);
+      if (z > bv) { bv = z; best = v; }
+    }
+    y[i] = best;
+  }
+  int n = 0;
+  while (n < L - 1 && path[n] == y[n]) ++n;
+  for (int i = 0; i < L; ++i) out[i] = -1;
+  for (int i = 0; i < n; ++i) out[i] = path[i];
+  out[n] = static_cast<int32_t>(y[n]);
+  *accept_len = n + 1;
+  return 0;
+}
+
+/* Rejection-sampling verification (T > 0), [Blog] §"A lightweight path
+ * selector" (rejection sampling recovers the exact target distribution) and
+ * [ZhTW] §"The output is exactly the same". The selected path is a
+ * deterministic proposal. p_i = softmax(Z[i]/T). For t = 1..L-1: accept x_t
+ * when U < p_{t-1}(x_t); on the first rejection emit a draw from p_{t-1}
+ * with x_t removed and renormalised and stop (accept_len = t); when all are
+ * accepted emit a bonus draw from p_{L-1} (accept_len = L).
+ * acc_margin = smallest |U - p| / p over the tests made; gum_margin = the
+ * relative top-2 gap of the Gumbel draw. b is the request's batch index (it
+ * is part of the random counter). */
+int orc_verify_sampling(int zdtype, const void* Z, int L, int64_t V, const int32_t* path,
+                        double T, uint64_t seed, int64_t b, int32_t* out, int32_t* accept_len,
+                        double* acc_margin, double* gum_margin) {
+  if (L < 2 || V < 2 || !(T > 0.0)) return -1;
+  for (int i = 0; i < L; ++i) out[i] = -1;
+  double am = kInf;
+  for (int t = 1; t < L; ++t) {
+    const int64_t off = static_cast<int64_t>(t - 1) * V;
+    const int64_t x = path[t - 1];
+    const double p = std::exp(widen(Z, zdtype, off + x) / T - row_lse(Z, zdtype, off, V, T));
+    const double u = uniform_accept(seed, b, t);
+    am = std::min(am, std::fabs(u - p) / p);
+    if (u < p) {
+      out[t - 1] = static_cast<int32_t>(x);
+      continue;
+    }
+    out[t - 1] = static_cast<int32_t>(gumbel_argmax(Z, zdtype, off, V, T, seed, b, t, x, gum_margin));
+    *accept_len = t;
+    *acc_margin = am;
+    return 0;
+  }
+  const int64_t off = static_cast<int64_t>(L - 1) * V;
+  out[L - 1] = static_cast<int32_t>(gumbel_argmax(Z, zdtype, off, V, T, seed, b, L, -1, gum_margin));
+  *accept_len = L;
+  *acc_margin = am;
+  return 0;
+}
+
+/* The sampling verification above run once per seed in [seed0, seed0 + n), for
+ * the distribution tests: out [n][L], accept_len [n]. */
+int orc_verify_sampling_many(int zdtype, const void* Z, int L, int64_t V, const int32_t* path,
+                             double T, uint64_t seed0, int64_t n, int64_t b, int nthreads,
+                             int32_t* out, int32_t* accept_len) {
+  if (L < 2 || V < 2 || !(T > 0.0) || n < 0) return -1;
+  int bad = 0;
+  if (nthreads <= 0) nthreads = 1;
+#pragma omp parallel for schedule(static) num_threads(nthreads) reduction(| : bad)
+  for (int64_t i = 0; i < n; ++i) {
+    double am, gm;
+    bad |= orc_verify_sampling(zdtype, Z, L, V, path, T, seed0 + static_cast<uint64_t>(i), b,
+                               out + i * L, accept_len + i, &am, &gm);
+  }
+  return bad ? -1 : 0;
+}
+
+/* Raw Philox4x64-10 block, exposed for the library pin. */
+void orc_philox4x64(const uint64_t* ctr, const uint64_t* key, uint64_t* out) {
+  philox4x64_10(ctr, key, out);
+}
+
+/* The whole step for the listed requests of a batch, composed from the
+ * stages above in the pages' order: logits -> keep top-K -> gate -> pair
+ * scores -> path -> verify. Inputs: h [B][L][d], W [d][V], Wg [r][d],
+ * A and Bt [V][r], x0 [B], Z [B][L][V]. Outputs are indexed by list position
+ * q = 0..nreq-1. path_mode 0 = greedy traversal, 1 = Viterbi; T <= 0 selects
+ * greedy verification. */
+int orc_select_verify(int dtype, int zdtype, const void* h, const void* W, const void* Wg,
+                      const void* A, const void* Bt, const int32_t* x0, const void* Z,
+                      int64_t B, int L, int64_t V, int64_t d, int64_t r, int K, int path_mode,
+                      double T, uint64_t seed, const int64_t* reqs, int64_t nreq, int nthreads,
+                      int32_t* cand_ids, double* cand_U, double* gate, double* S, int32_t* path,
+                      double* path_score, int32_t* out, int32_t* accept_len, double* topk_gap,
+                      double* path_margin, double* acc_margin, double* gum_margin) {
+  if (L < 2 || K < 1 || V < K || B < 1) return -1;
+  const int P = L - 1;
+  std::vector<int64_t> rows(P);
+  std::vector<double> u(static_cast<size_t>(P) * V);
+  std::vector<int32_t> pidx(P);
+  for (int64_t q = 0; q < nreq; ++q) {
+    const int64_t b = reqs[q];
+    if (b < 0 || b >= B) return -1;
+    for (int p = 0; p < P; ++p) rows[p] = b * L + (p + 1);
+    int32_t* ids = cand_ids + q * P * K;
+    double* U = cand_U + q * P * K;
+    double* g = gate + q * P * r;
+    double* Sq = S + q * P * K * K;
+    int rc = orc_logits(dtype, h, W, d, V, rows.data(), P, u.data(), nthreads);
+    if (rc == 0) rc = orc_topk(u.data(), P, V, K, ids, U, topk_gap + q * P);
+    if (rc == 0) rc = orc_gate(dtype, h, Wg, d, r, rows.data(), P, g);
+    if (rc == 0) rc = orc_pair_scores(dtype, A, Bt, r, P, K, ids, U, g, x0[b], Sq);
+    if (rc == 0)
+      rc = (path_mode == 1)
+               ? orc_path_viterbi(P, K, Sq, ids, path + q * P, pidx.data(), path_score + q, path_margin + q)
+               : orc_path_greedy(P, K, Sq, ids, path + q * P, pidx.data(), path_score + q, path_margin + q);
+    if (rc != 0) return rc;
+    const char* zb = static_cast<const char*>(Z) +
+                     b * static_cast<int64_t>(L) * V * (zdtype == ORC_BF16 ? 2 : 4);
+    acc_margin[q] = kInf;
+    gum_margin[q] = kInf;
+    if (T > 0.0)
+      rc = orc_verify_sampling(zdtype, zb, L, V, path + q * P, T, seed, b, out + q * L,
+                               accept_len + q, acc_margin + q, gum_margin + q);
+    else
+      rc = orc_verify_greedy(zdtype, zb, L, V, path + q * P, out + q * L, accept_len + q);
+    if (rc != 0) return rc;
+  }
+  return 0;
+}
+
+}  // extern "C"
