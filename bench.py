@@ -1,0 +1,371 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused draft-block select-and-verify step (DFlash 2) on GB300.
+
+One step = one dfs_select_verify call over one batch of the throughput workload
+(B=32 requests, block L=8, V=151936, d=5120, r=256, bf16, Zipf-shaped drafter rows):
+LM head + top-16, gate, pair scores, path, verification. Metric: draft blocks/s (one block
+= one request's L-position block), plus the fraction of the HBM roofline set by the bytes
+of W_vocab and the target logits.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 it runs under torch.distributed.run, one process per GPU; every rank is an
+independent replica with its own batch (weak scaling), rank 0 prints one JSON line.
+--impl reference times the fp64 CPU oracle on this host's cores on a bounded sample of
+the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft blocks/s for select+verify at B=32,L=8,V=151936; % of HBM roofline"
+UNIT = "blocks/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="throughput_B32_L8_V151936_d5120_zipf")
+    ap.add_argument("--path-mode", choices=["greedy", "viterbi"], default="greedy")
+    ap.add_argument("--sampling-temperature", type=float, default=0.6)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU time budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def lmhead_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("lmhead_tc.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "draft_speculative_decoding_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per LM-head launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now."""
+    p = os.path.join(ROOT, "profiles", "lmhead_ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    ent = rec.get(workload)
+    if not ent or ent.get("source_hash") != lmhead_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.rows = []
+        self.proc = None
+        self.thread = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if gpu_uuid:
+            cmd += ["-i", gpu_uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        if not self.rows:
+            return None
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------- our implementation
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from draft_speculative_decoding_gb300 import binding, replicas
+    from draft_speculative_decoding_gb300 import build as dfs_build
+    from draft_speculative_decoding_gb300 import workloads as wl
+
+    rank, world, local = replicas.init()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        dfs_build.build()
+    replicas.barrier()
+    binding.load()
+
+    spec = wl.WORKLOADS[args.workload]
+    data = wl.generate(spec.with_(seed=spec.seed + 1000 * rank), dev)
+    nrot = 3  # rotate target-logit / hidden buffers so no step rereads an L2-resident copy
+    Zs = [data["Z"]] + [wl.fresh_targets(data, 100 + i) for i in range(1, nrot)]
+    hs = [data["h"]] + [data["h"].clone() for _ in range(1, nrot)]
+    dims = binding.make_dims(spec.B, spec.L, spec.V, spec.d, spec.r, binding.DFS_BF16,
+                             binding.DFS_BF16)
+    ws = binding.alloc_workspace(dims)
+    P = spec.L - 1
+    outs = (torch.empty(spec.B, P, dtype=torch.int32, device=dev),
+            torch.empty(spec.B, spec.L, dtype=torch.int32, device=dev),
+            torch.empty(spec.B, dtype=torch.int32, device=dev))
+    mode = binding.DFS_PATH_GREEDY if args.path_mode == "greedy" else binding.DFS_PATH_VITERBI
+    stream = torch.cuda.current_stream()
+
+    def step(i, T, h=None, Z=None, x0=None):
+        binding.dfs_select_verify(dims, hs[i % nrot] if h is None else h, data["W"], data["Wg"],
+                                  data["A"], data["Bt"], data["x0"] if x0 is None else x0,
+                                  Zs[i % nrot] if Z is None else Z, mode, T, spec.seed + i, ws,
+                                  outputs=outs, stream=stream)
+
+    def timed(T, K, W, trace=False):
+        for i in range(W):
+            step(i, T)
+        torch.cuda.synchronize()
+        replicas.barrier()
+        torch.cuda.synchronize()
+        tr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)] if trace else None
+        for ev in (tr or []):
+            ev[0].record(stream)
+            ev[1].record(stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(K):
+            if trace:
+                binding.dfs_set_trace_events(*tr[i])
+            step(W + i, T)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        binding.dfs_set_trace_events(None, None)
+        replicas.barrier()
+        ms = e0.elapsed_time(e1) / K
+        lm = statistics.mean(a.elapsed_time(b) for a, b in tr) if trace else None
+        return ms, lm
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    ms_greedy, lm_ms = timed(0.0, args.steps, args.warmup, trace=True)
+    clk = clocks.stop()
+    assert binding.dfs_get_device_error(ws) == binding.DFS_OK
+    accept = outs[2].float().mean().item()
+    ms_samp, _ = timed(args.sampling_temperature, max(10, args.steps // 2), args.warmup)
+    accept_samp = outs[2].float().mean().item()
+
+    # end to end through the public API: inputs from pinned host memory each step, results
+    # read back to the host each step
+    host_h = [h.cpu().pin_memory() for h in hs]
+    host_Z = [Z.cpu().pin_memory() for Z in Zs]
+    host_x0 = data["x0"].cpu().pin_memory()
+    dev_h, dev_Z, dev_x0 = torch.empty_like(hs[0]), torch.empty_like(Zs[0]), torch.empty_like(data["x0"])
+    host_out = torch.empty(outs[1].shape, dtype=torch.int32).pin_memory()
+    host_acc = torch.empty(outs[2].shape, dtype=torch.int32).pin_memory()
+    K_e2e = max(10, args.steps // 2)
+
+    def e2e_step(i):
+        dev_h.copy_(host_h[i % nrot], non_blocking=True)
+        dev_Z.copy_(host_Z[i % nrot], non_blocking=True)
+        dev_x0.copy_(host_x0, non_blocking=True)
+        step(i, 0.0, dev_h, dev_Z, dev_x0)
+        host_out.copy_(outs[1], non_blocking=True)
+        host_acc.copy_(outs[2], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    replicas.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K_e2e):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / K_e2e
+    h2d = hs[0].numel() * 2 + Zs[0].numel() * 2 + data["x0"].numel() * 4
+    d2h = host_out.numel() * 4 + host_acc.numel() * 4
+
+    value = replicas.job_throughput(spec.B * args.steps, ms_greedy * args.steps / 1e3)
+    ms_max = replicas.max_over_ranks(ms_greedy)
+    value_samp = replicas.job_throughput(spec.B, ms_samp / 1e3)
+    value_e2e = replicas.job_throughput(spec.B, ms_e2e / 1e3)
+    lm_max = replicas.max_over_ranks(lm_ms)
+
+    peaks, peak_src = measured_peaks()
+    w_bytes = spec.d * spec.V * 2  # the LM head, read once per launch
+    z_bytes = spec.B * spec.L * spec.V * 2
+    achieved = w_bytes / (lm_max * 1e-3) / 1e9
+    step_achieved = (w_bytes + z_bytes) / (ms_max * 1e-3) / 1e9
+    traffic = ncu_traffic(args.workload)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(data, spec, args.cpu_seconds)
+
+    row_groups = (spec.B * spec.L + 255) // 256
+    launches_greedy = 2 + row_groups
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; shapes and distributions of the pages' block-8 workload)",
+            "config": {"workload": spec.name, "B": spec.B, "L": spec.L, "K": 16, "V": spec.V,
+                       "d": spec.d, "r": spec.r, "path_mode": args.path_mode,
+                       "temperature": 0.0, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: W_vocab 1.56 GB read every step; "
+                             f"{nrot} rotating target-logit buffers"},
+            "hbm_roofline_frac_step": round(step_achieved / peaks["hbm_gbs"], 4),
+            "roofline": {"kernel": "k_lmhead_tc (LM head + fused top-16 + gate tiles)",
+                         "bound": "hbm", "achieved": round(achieved, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "traffic": traffic, "algorithmic_bytes_per_launch": w_bytes,
+                         "ms_per_launch": round(lm_max, 4),
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
+            "e2e": {"value": round(value_e2e, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)},
+            "sampling": {"temperature": args.sampling_temperature, "value": round(value_samp, 1),
+                         "unit": UNIT, "ms_per_step": round(ms_samp, 4),
+                         "mean_accept_len": round(accept_samp, 3)},
+            "mean_accept_len": round(accept, 3),
+            "gpu_launches": launches_greedy * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    replicas.finalize()
+
+
+def cpu_baseline(data, spec, budget_s):
+    """The fp64 oracle as it stands, on this host's cores, over requests of the same batch
+    until the time budget is spent (at least one request)."""
+    import oracle
+    from draft_speculative_decoding_gb300 import workloads as wl
+
+    npd = {k: wl.to_numpy_bits(data[k]) for k in ("h", "W", "Wg", "A", "Bt", "x0", "Z")}
+    threads = oracle.default_threads()
+    oracle.build()
+    n, t0 = 0, time.perf_counter()
+    while n < spec.B and (n == 0 or time.perf_counter() - t0 < budget_s):
+        oracle.select_verify(npd["h"], npd["W"], npd["Wg"], npd["A"], npd["Bt"], npd["x0"],
+                             npd["Z"], path_mode=0, temperature=0.0, seed=spec.seed, reqs=[n],
+                             nthreads=threads)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {spec.B} requests of {spec.name}, greedy path, T=0, "
+                      f"{dt:.1f} s wall"}
+
+
+# ------------------------------------------------------------------- reference arm (oracle)
+def run_reference(args):
+    from draft_speculative_decoding_gb300 import replicas
+
+    rank, world, _ = replicas.rank_info()
+    if rank != 0:
+        return
+    import torch
+
+    import oracle
+    from draft_speculative_decoding_gb300 import workloads as wl
+
+    spec = wl.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    data = wl.generate(spec, dev)
+    npd = {k: wl.to_numpy_bits(data[k]) for k in ("h", "W", "Wg", "A", "Bt", "x0", "Z")}
+    del data
+    oracle.build()
+    threads = oracle.default_threads()
+
+    def step(i):  # one request of the batch per step: a bounded sample
+        oracle.select_verify(npd["h"], npd["W"], npd["Wg"], npd["A"], npd["Bt"], npd["x0"],
+                             npd["Z"], path_mode=0, temperature=0.0, seed=spec.seed,
+                             reqs=[i % spec.B], nthreads=threads)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    sample = f"1 of {spec.B} requests of {spec.name} per step (greedy path, T=0)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "B": spec.B, "L": spec.L, "K": 16, "V": spec.V,
+                   "d": spec.d, "r": spec.r, "path_mode": "greedy", "temperature": 0.0},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

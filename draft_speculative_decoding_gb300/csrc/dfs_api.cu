@@ -1,0 +1,408 @@
+// dfs_api.cu -- the C ABI of libdfs.so (declared in include/dfs.h): argument checks,
+// workspace layout and the order of kernel launches for each entry point. Nothing here
+// allocates, frees or synchronises except dfs_get_device_error.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/dfs.h"
+#include "kernels.h"
+
+namespace {
+
+using dfs::kK;
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// Tile-shape choice for row groups of 129..256 rows: 0 = automatic, 1 = two 128-row MMA
+// tiles x 128 vocabulary columns (double-buffered TMEM), 2 = two tiles x 256 columns
+// (single-buffered). Read from DFS_LMHEAD_VARIANT on each call, for tuning.
+int lmhead_variant_override() {
+  const char* s = std::getenv("DFS_LMHEAD_VARIANT");
+  const int v = s ? std::atoi(s) : 0;
+  return (v < 0 || v > 2) ? 0 : v;
+}
+
+struct Layout {
+  size_t err, counters, rcounters;
+  size_t part_val, part_idx, gate;
+  size_t zmax, zarg, zsum;
+  size_t cand_ids, cand_U, S, path;
+  size_t rinfo, gkey, gidx;
+  size_t logits;
+  size_t total;
+  int G, nchunk;
+};
+
+int check_dims(const dfs_dims* d) {
+  if (d == nullptr) return DFS_ERR_INVALID;
+  if (d->B < 1 || d->L < 2 || d->K < 1 || d->V < 1 || d->d < 1 || d->r < 1) return DFS_ERR_INVALID;
+  if ((d->dtype != DFS_BF16 && d->dtype != DFS_FP32) || (d->zdtype != DFS_BF16 && d->zdtype != DFS_FP32))
+    return DFS_ERR_UNSUPPORTED;
+  if (d->K != kK || d->L > dfs::kMaxL || d->V < kK || d->V % 8 != 0) return DFS_ERR_UNSUPPORTED;
+  if (d->r % 8 != 0 || d->r > dfs::kMaxRank) return DFS_ERR_UNSUPPORTED;
+  if (d->dtype == DFS_BF16 && d->d % 64 != 0) return DFS_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->B) * d->L > (1LL << 30)) return DFS_ERR_UNSUPPORTED;
+  return DFS_OK;
+}
+
+bool make_layout(const dfs_dims& d, Layout* L) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return false;
+  L->G = d.dtype == DFS_BF16 ? (sms < dfs::kMaxLists ? sms : dfs::kMaxLists) : 1;
+  L->nchunk = (d.V + dfs::kZChunk - 1) / dfs::kZChunk;
+  const size_t rows = static_cast<size_t>(d.B) * d.L;
+  const size_t P = static_cast<size_t>(d.L - 1);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  L->err = take(16);
+  L->counters = take(4 * static_cast<size_t>(d.B));
+  L->rcounters = take(4 * static_cast<size_t>(d.B));
+  L->part_val = take(4 * rows * L->G * kK);
+  L->part_idx = take(4 * rows * L->G * kK);
+  L->gate = take(4 * rows * d.r);
+  L->zmax = take(4 * rows * L->nchunk);
+  L->zarg = take(4 * rows * L->nchunk);
+  L->zsum = take(4 * rows * L->nchunk);
+  L->cand_ids = take(4 * d.B * P * kK);
+  L->cand_U = take(4 * d.B * P * kK);
+  L->S = take(4 * d.B * P * kK * kK);
+  L->path = take(4 * d.B * P);
+  L->rinfo = take(16 * static_cast<size_t>(d.B));
+  L->gkey = take(4 * static_cast<size_t>(d.B) * L->nchunk);
+  L->gidx = take(4 * static_cast<size_t>(d.B) * L->nchunk);
+  L->logits = take(d.dtype == DFS_FP32 ? 4 * rows * d.V : 0);
+  L->total = off;
+  return true;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_ptrs(std::initializer_list<const void*> req, std::initializer_list<const void*> opt) {
+  for (const void* p : req)
+    if (p == nullptr || !aligned16(p)) return DFS_ERR_INVALID;
+  for (const void* p : opt)
+    if (p != nullptr && !aligned16(p)) return DFS_ERR_INVALID;
+  return DFS_OK;
+}
+
+int prepare(const dfs_dims* dims, void* ws, size_t ws_bytes, Layout* L) {
+  int rc = check_dims(dims);
+  if (rc != DFS_OK) return rc;
+  if (ws == nullptr || !aligned16(ws)) return DFS_ERR_INVALID;
+  if (!make_layout(*dims, L)) return DFS_ERR_CUDA;
+  if (ws_bytes < L->total) return DFS_ERR_WORKSPACE;
+  return DFS_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? DFS_OK : DFS_ERR_CUDA; }
+
+thread_local cudaEvent_t g_trace_start = nullptr;
+thread_local cudaEvent_t g_trace_stop = nullptr;
+
+dfs::TailLaunch tail_args(const dfs_dims& d, const Layout& L, void* ws) {
+  dfs::TailLaunch t{};
+  t.B = d.B;
+  t.L = d.L;
+  t.V = d.V;
+  t.r = d.r;
+  t.G = L.G;
+  t.dtype = d.dtype;
+  t.zdtype = d.zdtype;
+  t.part_val = at<float>(ws, L.part_val);
+  t.part_idx = at<int>(ws, L.part_idx);
+  t.gate = at<float>(ws, L.gate);
+  t.zmax = at<float>(ws, L.zmax);
+  t.zarg = at<int>(ws, L.zarg);
+  t.zsum = at<float>(ws, L.zsum);
+  t.nchunk = L.nchunk;
+  t.cand_ids = at<int>(ws, L.cand_ids);
+  t.cand_U = at<float>(ws, L.cand_U);
+  t.S = at<float>(ws, L.S);
+  t.path = at<int>(ws, L.path);
+  t.resample_info = at<int>(ws, L.rinfo);
+  t.counters = at<int>(ws, L.counters);
+  t.gumbel_key = at<float>(ws, L.gkey);
+  t.gumbel_idx = at<int>(ws, L.gidx);
+  t.resample_counters = at<int>(ws, L.rcounters);
+  t.err = at<int>(ws, L.err);
+  return t;
+}
+
+cudaError_t run_lmhead_kernels(const dfs_dims& d, const Layout& L, void* ws, const void* hidden,
+                               const void* W, const void* Wg, bool vocab, bool gate, cudaStream_t s,
+                               int rows);
+
+// Step a1 (+ a2 when gate): LM head, partial top-16 lists, gate rows.
+cudaError_t run_lmhead(const dfs_dims& d, const Layout& L, void* ws, const void* hidden,
+                       const void* W, const void* Wg, bool vocab, bool gate, cudaStream_t s) {
+  const int rows = d.B * d.L;
+  if (vocab && g_trace_start != nullptr && cudaEventRecord(g_trace_start, s) != cudaSuccess)
+    return cudaErrorInvalidResourceHandle;
+  cudaError_t e = run_lmhead_kernels(d, L, ws, hidden, W, Wg, vocab, gate, s, rows);
+  if (e == cudaSuccess && vocab && g_trace_stop != nullptr) e = cudaEventRecord(g_trace_stop, s);
+  return e;
+}
+
+cudaError_t run_lmhead_kernels(const dfs_dims& d, const Layout& L, void* ws, const void* hidden,
+                               const void* W, const void* Wg, bool vocab, bool gate, cudaStream_t s,
+                               int rows) {
+  if (d.dtype == DFS_BF16) {
+    dfs::LmheadLaunch a{};
+    a.hidden = hidden;
+    a.W = W;
+    a.Wg = Wg;
+    a.rows_total = rows;
+    a.L = d.L;
+    a.V = d.V;
+    a.d = d.d;
+    a.r = d.r;
+    a.vocab = vocab;
+    a.gate = gate;
+    a.part_val = at<float>(ws, L.part_val);
+    a.part_idx = at<int>(ws, L.part_idx);
+    a.G = L.G;
+    a.gate_out = at<float>(ws, L.gate);
+    a.err = at<int>(ws, L.err);
+    a.lmhead_variant = lmhead_variant_override();
+    return dfs::launch_lmhead_tc(a, s);
+  }
+  dfs::LmheadSimtLaunch a{};
+  a.hidden = static_cast<const float*>(hidden);
+  a.W = static_cast<const float*>(W);
+  a.Wg = static_cast<const float*>(Wg);
+  a.rows_total = rows;
+  a.L = d.L;
+  a.V = d.V;
+  a.d = d.d;
+  a.r = d.r;
+  a.vocab = vocab;
+  a.gate = gate;
+  a.logits_ws = at<float>(ws, L.logits);
+  a.part_val = at<float>(ws, L.part_val);
+  a.part_idx = at<int>(ws, L.part_idx);
+  a.gate_out = at<float>(ws, L.gate);
+  return dfs::launch_lmhead_simt(a, s);
+}
+
+cudaError_t run_zreduce(const dfs_dims& d, const Layout& L, void* ws, const void* Z, float T,
+                        cudaStream_t s) {
+  dfs::ZReduceLaunch z{};
+  z.Z = Z;
+  z.zdtype = d.zdtype;
+  z.rows = d.B * d.L;
+  z.V = d.V;
+  z.nchunk = L.nchunk;
+  z.inv_T = T > 0.f ? 1.0f / T : 0.f;
+  z.zmax = at<float>(ws, L.zmax);
+  z.zarg = at<int>(ws, L.zarg);
+  z.zsum = at<float>(ws, L.zsum);
+  // the counters and the resample counters are adjacent 256-byte aligned regions
+  z.zero_ptr = at<int>(ws, L.counters);
+  z.zero_count = static_cast<int>((L.part_val - L.counters) / 4);
+  return dfs::launch_zreduce(z, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dfs_version(void) { return 1; }
+
+int dfs_set_trace_events(void* start, void* stop) {
+  g_trace_start = static_cast<cudaEvent_t>(start);
+  g_trace_stop = static_cast<cudaEvent_t>(stop);
+  return DFS_OK;
+}
+
+const char* dfs_status_string(int status) {
+  switch (status) {
+    case DFS_OK: return "ok";
+    case DFS_ERR_INVALID: return "invalid argument";
+    case DFS_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case DFS_ERR_WORKSPACE: return "workspace too small";
+    case DFS_ERR_CUDA: return "CUDA error";
+    case DFS_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+size_t dfs_workspace_size(const dfs_dims* dims) {
+  if (check_dims(dims) != DFS_OK) return 0;
+  Layout L;
+  if (!make_layout(*dims, &L)) return 0;
+  return L.total;
+}
+
+int dfs_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < 16) return DFS_ERR_INVALID;
+  return cuda_rc(cudaMemsetAsync(ws, 0, ws_bytes < 4096 ? ws_bytes : 4096,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+int dfs_get_device_error(void* ws, size_t ws_bytes, int* err, void* stream) {
+  if (ws == nullptr || err == nullptr || ws_bytes < 16) return DFS_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaMemcpyAsync(&word, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DFS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DFS_ERR_CUDA;
+  *err = word ? DFS_ERR_TIMEOUT : DFS_OK;
+  if (word) {
+    if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return DFS_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DFS_ERR_CUDA;
+  }
+  return DFS_OK;
+}
+
+int dfs_lmhead_topk(const dfs_dims* dims, const void* hidden, const void* W_vocab,
+                    int32_t* cand_ids, float* cand_U, void* ws, size_t ws_bytes, void* stream) {
+  Layout L;
+  int rc = prepare(dims, ws, ws_bytes, &L);
+  if (rc != DFS_OK) return rc;
+  if ((rc = check_ptrs({hidden, W_vocab, cand_ids, cand_U}, {})) != DFS_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = run_lmhead(*dims, L, ws, hidden, W_vocab, nullptr, true, false, s);
+  if (e != cudaSuccess) return DFS_ERR_CUDA;
+  dfs::TailLaunch t = tail_args(*dims, L, ws);
+  t.cand_ids = cand_ids;
+  t.cand_U = cand_U;
+  return cuda_rc(dfs::launch_merge(t, s));
+}
+
+int dfs_pair_score(const dfs_dims* dims, const void* hidden, const void* W_g, const void* A,
+                   const void* Btab, const int32_t* last_verified, const int32_t* cand_ids,
+                   const float* cand_U, float* S, float* gate_opt, void* ws, size_t ws_bytes,
+                   void* stream) {
+  Layout L;
+  int rc = prepare(dims, ws, ws_bytes, &L);
+  if (rc != DFS_OK) return rc;
+  if ((rc = check_ptrs({hidden, W_g, A, Btab, last_verified, cand_ids, cand_U, S}, {gate_opt})) != DFS_OK)
+    return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = run_lmhead(*dims, L, ws, hidden, nullptr, W_g, false, true, s);
+  if (e != cudaSuccess) return DFS_ERR_CUDA;
+  dfs::TailLaunch t = tail_args(*dims, L, ws);
+  t.A = A;
+  t.Bt = Btab;
+  t.x0 = last_verified;
+  t.cand_ids = const_cast<int*>(cand_ids);
+  t.cand_U = const_cast<float*>(cand_U);
+  t.S = S;
+  if ((e = dfs::launch_pair(t, s)) != cudaSuccess) return DFS_ERR_CUDA;
+  if (gate_opt != nullptr) {
+    const size_t row = static_cast<size_t>(dims->r) * sizeof(float);
+    e = cudaMemcpy2DAsync(gate_opt, (dims->L - 1) * row, at<char>(ws, L.gate) + row, dims->L * row,
+                          (dims->L - 1) * row, dims->B, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return DFS_ERR_CUDA;
+  }
+  return DFS_OK;
+}
+
+int dfs_path_select(const dfs_dims* dims, const float* S, const int32_t* cand_ids, int path_mode,
+                    int32_t* path, float* path_score, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != DFS_OK) return rc;
+  if (path_mode != DFS_PATH_GREEDY && path_mode != DFS_PATH_VITERBI) return DFS_ERR_INVALID;
+  if ((rc = check_ptrs({S, cand_ids, path}, {path_score})) != DFS_OK) return rc;
+  dfs::TailLaunch t{};
+  t.B = dims->B;
+  t.L = dims->L;
+  t.path_mode = path_mode;
+  t.S = const_cast<float*>(S);
+  t.cand_ids = const_cast<int*>(cand_ids);
+  t.path = path;
+  t.path_score = path_score;
+  return cuda_rc(dfs::launch_path(t, static_cast<cudaStream_t>(stream)));
+}
+
+int dfs_verify(const dfs_dims* dims, const int32_t* path, const void* target_logits,
+               float temperature, uint64_t seed, int32_t* out_tokens, int32_t* accept_len,
+               void* ws, size_t ws_bytes, void* stream) {
+  Layout L;
+  int rc = prepare(dims, ws, ws_bytes, &L);
+  if (rc != DFS_OK) return rc;
+  if (!(temperature >= 0.f) || temperature != temperature) return DFS_ERR_INVALID;
+  if ((rc = check_ptrs({path, target_logits, out_tokens, accept_len}, {})) != DFS_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (run_zreduce(*dims, L, ws, target_logits, temperature, s) != cudaSuccess) return DFS_ERR_CUDA;
+  dfs::TailLaunch t = tail_args(*dims, L, ws);
+  t.Z = target_logits;
+  t.T = temperature;
+  t.seed = seed;
+  t.path = const_cast<int*>(path);
+  t.out_tokens = out_tokens;
+  t.accept_len = accept_len;
+  if (dfs::launch_verify(t, s) != cudaSuccess) return DFS_ERR_CUDA;
+  if (temperature > 0.f && dfs::launch_resample(t, s) != cudaSuccess) return DFS_ERR_CUDA;
+  return DFS_OK;
+}
+
+int dfs_select_verify(const dfs_dims* dims, const void* hidden, const void* W_vocab,
+                      const void* W_g, const void* A, const void* Btab,
+                      const int32_t* last_verified, const void* target_logits, int path_mode,
+                      float temperature, uint64_t seed, int32_t* path, int32_t* out_tokens,
+                      int32_t* accept_len, int32_t* cand_ids_opt, float* cand_U_opt,
+                      float* S_opt, float* path_score_opt, void* ws, size_t ws_bytes,
+                      void* stream) {
+  Layout L;
+  int rc = prepare(dims, ws, ws_bytes, &L);
+  if (rc != DFS_OK) return rc;
+  if (path_mode != DFS_PATH_GREEDY && path_mode != DFS_PATH_VITERBI) return DFS_ERR_INVALID;
+  if (!(temperature >= 0.f) || temperature != temperature) return DFS_ERR_INVALID;
+  if ((rc = check_ptrs({hidden, W_vocab, W_g, A, Btab, last_verified, target_logits, path,
+                        out_tokens, accept_len},
+                       {cand_ids_opt, cand_U_opt, S_opt, path_score_opt})) != DFS_OK)
+    return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (run_zreduce(*dims, L, ws, target_logits, temperature, s) != cudaSuccess) return DFS_ERR_CUDA;
+  if (run_lmhead(*dims, L, ws, hidden, W_vocab, W_g, true, true, s) != cudaSuccess)
+    return DFS_ERR_CUDA;
+  dfs::TailLaunch t = tail_args(*dims, L, ws);
+  t.A = A;
+  t.Bt = Btab;
+  t.x0 = last_verified;
+  t.Z = target_logits;
+  t.T = temperature;
+  t.seed = seed;
+  t.path_mode = path_mode;
+  if (cand_ids_opt) t.cand_ids = cand_ids_opt;
+  if (cand_U_opt) t.cand_U = cand_U_opt;
+  if (S_opt) t.S = S_opt;
+  t.path = path;
+  t.path_score = path_score_opt;
+  t.out_tokens = out_tokens;
+  t.accept_len = accept_len;
+  if (dfs::launch_tail_fused(t, s) != cudaSuccess) return DFS_ERR_CUDA;
+  if (temperature > 0.f && dfs::launch_resample(t, s) != cudaSuccess) return DFS_ERR_CUDA;
+  return DFS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+// kernels.h -- internal launchers of libdfs.so (host side). The C ABI in
+// include/dfs.h validates arguments and lays out the workspace, then calls these.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dfs {
+
+constexpr int kK = 16;          // candidates kept per draft position
+constexpr int kMaxL = 16;       // longest block handled
+constexpr int kMaxRank = 512;   // widest selector rank handled
+constexpr int kMaxLists = 256;  // partial top-16 lists merged per row
+constexpr int kZChunk = 8192;   // target-logit elements per reduction block
+
+// ---- a1 (+a2): LM head with fused top-16 (and gate) on the tensor cores ----
+struct LmheadLaunch {
+  const void* hidden;  // [rows_total, d] bf16 (rows_total = B*L)
+  const void* W;       // [d, V] bf16
+  const void* Wg;      // [r, d] bf16 (gate tiles), may be null when !gate
+  int rows_total, L, V, d, r;
+  bool vocab;          // compute the vocabulary tiles (top-16 partial lists)
+  bool gate;           // compute the gate tiles
+  float* part_val;     // [rows_total][G][16]
+  int* part_idx;
+  int G;               // grid of the vocabulary launch = lists per row
+  float* gate_out;     // [rows_total][r]
+  int* err;
+  int lmhead_variant;  // 0 = automatic; 1 = two M-tiles x 128 vocab (double-buffered TMEM);
+                       // 2 = two M-tiles x 256 vocab (single-buffered TMEM)
+};
+cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s);
+
+// ---- a1 (+a2) for fp32 inputs, on CUDA cores ----
+struct LmheadSimtLaunch {
+  const float* hidden;  // [rows_total, d]
+  const float* W;       // [d, V]
+  const float* Wg;      // [r, d]
+  int rows_total, L, V, d, r;
+  bool vocab, gate;
+  float* logits_ws;     // [rows_total, V] scratch
+  float* part_val;      // [rows_total][1][16]
+  int* part_idx;
+  float* gate_out;      // [rows_total][r]
+};
+cudaError_t launch_lmhead_simt(const LmheadSimtLaunch& a, cudaStream_t s);
+
+// ---- target-logit row statistics (a5/a6 preparation) ----
+struct ZReduceLaunch {
+  const void* Z;   // [rows, V]
+  int zdtype;      // 0 bf16, 1 fp32
+  int rows, V, nchunk;
+  float inv_T;     // 0 for greedy (max/argmax only)
+  float* zmax;     // [rows][nchunk]
+  int* zarg;
+  float* zsum;     // [rows][nchunk] sum of exp((z - chunk max) * inv_T)
+  int* zero_ptr;   // counters cleared for the later kernels of this call
+  int zero_count;
+};
+cudaError_t launch_zreduce(const ZReduceLaunch& a, cudaStream_t s);
+
+// ---- everything after the LM head: merge, pair scores, path, verify ----
+struct TailLaunch {
+  int B, L, V, r, G;
+  int dtype;                 // of A/Bt
+  int zdtype;
+  const float* part_val;     // [B*L][G][16]
+  const int* part_idx;
+  const float* gate;         // [B*L][r]
+  const void* A;             // [V, r]
+  const void* Bt;
+  const int* x0;             // [B]
+  const void* Z;             // [B, L, V]
+  const float* zmax;         // [B*L][nchunk]
+  const int* zarg;
+  const float* zsum;
+  int nchunk;
+  float T;                   // 0 = greedy verification
+  uint64_t seed;
+  int path_mode;
+  int* cand_ids;             // [B][L-1][16]
+  float* cand_U;
+  float* S;                  // [B][L-1][16][16]
+  int* path;                 // [B][L-1]
+  float* path_score;         // [B] or null
+  int* out_tokens;           // [B][L]
+  int* accept_len;           // [B]
+  int* resample_info;        // [B][4]: row, excluded token, output slot, active
+  int* counters;             // [B]
+  float* gumbel_key;         // [B][nchunk]
+  int* gumbel_idx;
+  int* resample_counters;    // [B]
+  int* err;
+};
+// Fused tail for dfs_select_verify: (L-1) x B blocks; the last block of each request
+// selects its path and verifies it.
+cudaError_t launch_tail_fused(const TailLaunch& a, cudaStream_t s);
+// Stage launchers for the separate entry points (same device code).
+cudaError_t launch_merge(const TailLaunch& a, cudaStream_t s);    // partial lists -> cand
+cudaError_t launch_pair(const TailLaunch& a, cudaStream_t s);     // cand + gate -> S
+cudaError_t launch_path(const TailLaunch& a, cudaStream_t s);     // S -> path
+cudaError_t launch_verify(const TailLaunch& a, cudaStream_t s);   // path + Z stats -> out
+cudaError_t launch_resample(const TailLaunch& a, cudaStream_t s); // T > 0 draws
+
+}  // namespace dfs

@@ -98,9 +98,10 @@ void philox4x64_10(const uint64_t in[4], const uint64_t key[2], uint64_t out[4])
   out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* Uniform in (0,1) from the top 24 bits of a 64-bit word: exact in fp32 and fp64. */
+/* Uniform in (0,1) from the top 23 bits of a 64-bit word: (2j+1) * 2^-24 with
+ * j < 2^23, an odd 24-bit integer times a power of two, so exact in fp32 and fp64. */
 inline double u01(uint64_t x) {
-  return (static_cast<double>(x >> 40) + 0.5) * (1.0 / 16777216.0);
+  return (static_cast<double>(x >> 41) + 0.5) * (1.0 / 8388608.0);
 }
 
 /* Counter layout shared by definition (not by code) with the GPU path:
