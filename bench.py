@@ -200,8 +200,11 @@ def run_ours(args):
     except Exception:
         uuid = None
     clocks = ClockSampler(uuid)
-    ms_greedy, lm_ms = timed(0.0, args.steps, args.warmup, trace=True)
+    ms_greedy, _ = timed(0.0, args.steps, args.warmup)
     clk = clocks.stop()
+    # the dominant kernel's own duration, from events recorded around it on its stream (a
+    # separate pass: an event between two kernels stops the second launching early)
+    _, lm_ms = timed(0.0, args.steps, 1, trace=True)
     assert binding.dfs_get_device_error(ws) == binding.DFS_OK
     accept = outs[2].float().mean().item()
     ms_samp, _ = timed(args.sampling_temperature, max(10, args.steps // 2), args.warmup)

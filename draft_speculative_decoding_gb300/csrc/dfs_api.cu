@@ -49,7 +49,7 @@ struct Layout {
   size_t rinfo, gkey, gidx;
   size_t logits;
   size_t total;
-  int G, nchunk;
+  int G, nchunk, nrchunk;
 };
 
 int check_dims(const dfs_dims* d) {
@@ -69,6 +69,7 @@ bool make_layout(const dfs_dims& d, Layout* L) {
   if (sms <= 0) return false;
   L->G = d.dtype == DFS_BF16 ? (sms < dfs::kMaxLists ? sms : dfs::kMaxLists) : 1;
   L->nchunk = (d.V + dfs::kZChunk - 1) / dfs::kZChunk;
+  L->nrchunk = (d.V + dfs::kRChunk - 1) / dfs::kRChunk;
   const size_t rows = static_cast<size_t>(d.B) * d.L;
   const size_t P = static_cast<size_t>(d.L - 1);
   size_t off = 0;
@@ -91,8 +92,8 @@ bool make_layout(const dfs_dims& d, Layout* L) {
   L->S = take(4 * d.B * P * kK * kK);
   L->path = take(4 * d.B * P);
   L->rinfo = take(16 * static_cast<size_t>(d.B));
-  L->gkey = take(4 * static_cast<size_t>(d.B) * L->nchunk);
-  L->gidx = take(4 * static_cast<size_t>(d.B) * L->nchunk);
+  L->gkey = take(4 * static_cast<size_t>(d.B) * L->nrchunk);
+  L->gidx = take(4 * static_cast<size_t>(d.B) * L->nrchunk);
   L->logits = take(d.dtype == DFS_FP32 ? 4 * rows * d.V : 0);
   L->total = off;
   return true;
@@ -143,6 +144,7 @@ dfs::TailLaunch tail_args(const dfs_dims& d, const Layout& L, void* ws) {
   t.zarg = at<int>(ws, L.zarg);
   t.zsum = at<float>(ws, L.zsum);
   t.nchunk = L.nchunk;
+  t.nrchunk = L.nrchunk;
   t.cand_ids = at<int>(ws, L.cand_ids);
   t.cand_U = at<float>(ws, L.cand_U);
   t.S = at<float>(ws, L.S);
@@ -158,22 +160,33 @@ dfs::TailLaunch tail_args(const dfs_dims& d, const Layout& L, void* ws) {
 
 cudaError_t run_lmhead_kernels(const dfs_dims& d, const Layout& L, void* ws, const void* hidden,
                                const void* W, const void* Wg, bool vocab, bool gate, cudaStream_t s,
-                               int rows);
+                               int rows, const void* Z, float T);
+cudaError_t run_zreduce(const dfs_dims& d, const Layout& L, void* ws, const void* Z, float T,
+                        cudaStream_t s);
 
 // Step a1 (+ a2 when gate): LM head, partial top-16 lists, gate rows.
+// With Z != nullptr the target-logit row statistics (and the per-call counter reset) are
+// produced alongside: by the tensor-core kernel's spare warps, or by the standalone
+// reduction kernel on the fp32 path.
 cudaError_t run_lmhead(const dfs_dims& d, const Layout& L, void* ws, const void* hidden,
-                       const void* W, const void* Wg, bool vocab, bool gate, cudaStream_t s) {
+                       const void* W, const void* Wg, bool vocab, bool gate, cudaStream_t s,
+                       const void* Z = nullptr, float T = 0.f) {
   const int rows = d.B * d.L;
+  if (Z != nullptr && d.dtype != DFS_BF16) {
+    cudaError_t ez = run_zreduce(d, L, ws, Z, T, s);
+    if (ez != cudaSuccess) return ez;
+  }
   if (vocab && g_trace_start != nullptr && cudaEventRecord(g_trace_start, s) != cudaSuccess)
     return cudaErrorInvalidResourceHandle;
-  cudaError_t e = run_lmhead_kernels(d, L, ws, hidden, W, Wg, vocab, gate, s, rows);
+  cudaError_t e = run_lmhead_kernels(d, L, ws, hidden, W, Wg, vocab, gate, s, rows,
+                                     d.dtype == DFS_BF16 ? Z : nullptr, T);
   if (e == cudaSuccess && vocab && g_trace_stop != nullptr) e = cudaEventRecord(g_trace_stop, s);
   return e;
 }
 
 cudaError_t run_lmhead_kernels(const dfs_dims& d, const Layout& L, void* ws, const void* hidden,
                                const void* W, const void* Wg, bool vocab, bool gate, cudaStream_t s,
-                               int rows) {
+                               int rows, const void* Z, float T) {
   if (d.dtype == DFS_BF16) {
     dfs::LmheadLaunch a{};
     a.hidden = hidden;
@@ -192,6 +205,18 @@ cudaError_t run_lmhead_kernels(const dfs_dims& d, const Layout& L, void* ws, con
     a.gate_out = at<float>(ws, L.gate);
     a.err = at<int>(ws, L.err);
     a.lmhead_variant = lmhead_variant_override();
+    if (Z != nullptr) {
+      a.Z = Z;
+      a.zdtype = d.zdtype;
+      a.z_rows = rows;
+      a.z_nchunk = L.nchunk;
+      a.z_inv_T = T > 0.f ? 1.0f / T : 0.f;
+      a.zmax = at<float>(ws, L.zmax);
+      a.zarg = at<int>(ws, L.zarg);
+      a.zsum = at<float>(ws, L.zsum);
+      a.zero_ptr = at<int>(ws, L.counters);
+      a.zero_count = static_cast<int>((L.part_val - L.counters) / 4);
+    }
     return dfs::launch_lmhead_tc(a, s);
   }
   dfs::LmheadSimtLaunch a{};
@@ -382,8 +407,8 @@ int dfs_select_verify(const dfs_dims* dims, const void* hidden, const void* W_vo
                        {cand_ids_opt, cand_U_opt, S_opt, path_score_opt})) != DFS_OK)
     return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (run_zreduce(*dims, L, ws, target_logits, temperature, s) != cudaSuccess) return DFS_ERR_CUDA;
-  if (run_lmhead(*dims, L, ws, hidden, W_vocab, W_g, true, true, s) != cudaSuccess)
+  if (run_lmhead(*dims, L, ws, hidden, W_vocab, W_g, true, true, s, target_logits, temperature) !=
+      cudaSuccess)
     return DFS_ERR_CUDA;
   dfs::TailLaunch t = tail_args(*dims, L, ws);
   t.A = A;

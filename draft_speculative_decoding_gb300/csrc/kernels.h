@@ -12,7 +12,8 @@ constexpr int kK = 16;          // candidates kept per draft position
 constexpr int kMaxL = 16;       // longest block handled
 constexpr int kMaxRank = 512;   // widest selector rank handled
 constexpr int kMaxLists = 256;  // partial top-16 lists merged per row
-constexpr int kZChunk = 8192;   // target-logit elements per reduction block
+constexpr int kZChunk = 4096;   // target-logit elements per row-statistics unit
+constexpr int kRChunk = 8192;   // target-logit elements per redraw block
 
 // ---- a1 (+a2): LM head with fused top-16 (and gate) on the tensor cores ----
 struct LmheadLaunch {
@@ -29,6 +30,15 @@ struct LmheadLaunch {
   int* err;
   int lmhead_variant;  // 0 = automatic; 1 = two M-tiles x 128 vocab (double-buffered TMEM);
                        // 2 = two M-tiles x 256 vocab (single-buffered TMEM)
+  // Target-logit row statistics computed by the kernel's spare warps (z_rows = 0: none).
+  const void* Z;       // [z_rows, V]
+  int zdtype, z_rows, z_nchunk;
+  float z_inv_T;       // 0: max/argmax only
+  float* zmax;         // [z_rows][z_nchunk]
+  int* zarg;
+  float* zsum;
+  int* zero_ptr;       // counters cleared for the later kernels of the call
+  int zero_count;
 };
 cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s);
 
@@ -75,7 +85,8 @@ struct TailLaunch {
   const float* zmax;         // [B*L][nchunk]
   const int* zarg;
   const float* zsum;
-  int nchunk;
+  int nchunk;                // row-statistics chunks per target row
+  int nrchunk;               // redraw chunks per target row
   float T;                   // 0 = greedy verification
   uint64_t seed;
   int path_mode;
@@ -88,7 +99,7 @@ struct TailLaunch {
   int* accept_len;           // [B]
   int* resample_info;        // [B][4]: row, excluded token, output slot, active
   int* counters;             // [B]
-  float* gumbel_key;         // [B][nchunk]
+  float* gumbel_key;         // [B][nrchunk]
   int* gumbel_idx;
   int* resample_counters;    // [B]
   int* err;

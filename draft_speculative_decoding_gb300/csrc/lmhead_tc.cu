@@ -23,7 +23,10 @@
 //     beats the row's current 16th value; at the end it writes its list as one partial
 //     list of the row (the tail kernel merges the G lists of a row).
 //   * gate tiles use W_g [r, d] (K-major) as the B operand; their epilogue applies the
-//     sigmoid and stores g[m, j] in fp32.
+//     sigmoid and stores g[m, j] in fp32;
+//   * warps 2-3 stream the target logits (16-byte loads, read once) and write per-chunk
+//     row statistics (max, argmax, sum of exp) for verification, so those bytes move
+//     while the tensor pipe works on W instead of in a kernel of their own.
 // Every mbarrier wait is bounded; on expiry the kernel sets the error word, stops all
 // roles, and frees its tensor memory.
 #include <cuda.h>
@@ -33,6 +36,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rowstat.cuh"
 
 namespace dfs {
 
@@ -48,6 +52,14 @@ struct LmheadParams {
   int* part_idx;
   float* gate_out;
   int* err;
+  const void* Z;
+  int zdtype, z_rows, z_nchunk;
+  float z_inv_T;
+  float* zmax;
+  int* zarg;
+  float* zsum;
+  int* zero_ptr;
+  int zero_count;
 };
 
 template <int MT, int NT, int NBUF, int STAGES>
@@ -129,6 +141,9 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, STAGES>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // Every CTA of this persistent grid is resident now: let the dependent tail kernel launch
+  // onto SMs as they free up (it waits for this grid's completion before reading).
+  grid_dependents_launch();
 
   const int n_tiles = p.n_vocab_tiles + p.n_gate_tiles;
   const int KB = p.d / 64;
@@ -219,6 +234,38 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, STAGES>::kThreads, 1)
           acc = 0;
           acc_phase ^= 1;
         }
+      }
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------ target-logit row statistics
+    if (blockIdx.x == 0 && p.zero_ptr != nullptr)
+      for (int i = threadIdx.x - 64; i < p.zero_count; i += 64) p.zero_ptr[i] = 0;
+    const int n_units = p.z_rows * p.z_nchunk;
+    const int is_bf16 = p.zdtype == 0;
+    for (int u = blockIdx.x * 2 + (warp - 2); u < n_units; u += gridDim.x * 2) {
+      const int row = u / p.z_nchunk, chunk = u - row * p.z_nchunk;
+      const size_t rbase = static_cast<size_t>(row) * p.V;
+      RowStat st = rowstat_empty();
+#pragma unroll 1
+      for (int bt = 0; bt < 4; ++bt) {
+        float x[4][8];
+        int v0[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          v0[g] = chunk * kZChunk + (bt * 4 + g) * 256 + lane * 8;
+          if (v0[g] < p.V) load8_stream(p.Z, is_bf16, rbase + v0[g], x[g]);
+        }
+        if (p.z_inv_T > 0.f)
+          rowstat_fold<4, true>(st, x, v0, p.V, p.z_inv_T);
+        else
+          rowstat_fold<4, false>(st, x, v0, p.V, 0.f);
+      }
+      st = warp_combine(st, p.z_inv_T);
+      if (lane == 0) {
+        const size_t o = static_cast<size_t>(row) * p.z_nchunk + chunk;
+        p.zmax[o] = st.m;
+        p.zarg[o] = st.i;
+        if (p.z_inv_T > 0.f) p.zsum[o] = st.s;
       }
     }
   } else if (warp >= 4) {
@@ -373,6 +420,18 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
   prm.err = a.err;
   for (int row0 = 0; row0 < a.rows_total; row0 += 256) {
     prm.row0 = row0;
+    // the target-logit statistics and the counter reset ride on the first launch only
+    const bool first = row0 == 0;
+    prm.Z = a.Z;
+    prm.zdtype = a.zdtype;
+    prm.z_rows = first ? a.z_rows : 0;
+    prm.z_nchunk = a.z_nchunk;
+    prm.z_inv_T = a.z_inv_T;
+    prm.zmax = a.zmax;
+    prm.zarg = a.zarg;
+    prm.zsum = a.zsum;
+    prm.zero_ptr = first ? a.zero_ptr : nullptr;
+    prm.zero_count = first ? a.zero_count : 0;
     prm.rows = a.rows_total - row0 < 256 ? a.rows_total - row0 : 256;
     const bool two = prm.rows > 128;
     const int variant = two ? (a.lmhead_variant == 2 ? 2 : 1) : 0;
@@ -383,7 +442,7 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
     if (!encode_bf16_2d(&prm.tm_g, a.gate ? a.Wg : a.hidden, a.d, a.gate ? a.r : a.rows_total,
                         64, static_cast<uint32_t>(a.gate ? NT : 128)))
       return cudaErrorInvalidValue;
-    const int grid = a.vocab ? a.G : prm.n_gate_tiles;
+    const int grid = a.vocab ? a.G : (prm.n_gate_tiles > 0 ? prm.n_gate_tiles : 1);
     cudaError_t e;
     if (variant == 0)
       e = launch_cfg<1, 256, 2, 4>(prm, grid, s);

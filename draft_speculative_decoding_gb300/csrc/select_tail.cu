@@ -19,6 +19,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "philox.cuh"
+#include "rowstat.cuh"
 
 namespace dfs {
 
@@ -50,41 +51,11 @@ __device__ __forceinline__ float load1(const void* base, int is_bf16, size_t idx
                  : static_cast<const float*>(base)[idx];
 }
 
-// (max, argmax, sum of exp((z - max) * inv_T)) monoid; ties keep the lower index.
-struct RowStat {
-  float m;
-  int i;
-  float s;
-};
-
-__device__ __forceinline__ RowStat combine(RowStat a, RowStat b, float inv_T) {
-  if (b.m == -INFINITY) return a;
-  if (a.m == -INFINITY) return b;
-  RowStat r;
-  const bool take_b = ranks_before(b.m, b.i, a.m, a.i);
-  r.m = take_b ? b.m : a.m;
-  r.i = take_b ? b.i : a.i;
-  r.s = a.s * expf((a.m - r.m) * inv_T) + b.s * expf((b.m - r.m) * inv_T);
-  return r;
-}
-
-__device__ __forceinline__ RowStat warp_combine(RowStat v, float inv_T) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    RowStat o;
-    o.m = __shfl_xor_sync(0xffffffffu, v.m, off);
-    o.i = __shfl_xor_sync(0xffffffffu, v.i, off);
-    o.s = __shfl_xor_sync(0xffffffffu, v.s, off);
-    v = combine(v, o, inv_T);
-  }
-  return v;
-}
-
 // ------------------------------------------------------------------ target rows
-// One block reduces kZChunk elements of one row of Z: each thread holds 4 x 8
-// consecutive elements.
+// One block of 128 threads reduces kZChunk (4096) elements of one row of Z: each thread
+// holds 4 groups of 8 consecutive elements, the groups 1024 elements apart.
 template <bool kSoft>
-__global__ void __launch_bounds__(256) k_zreduce(const void* Z, int is_bf16, int V, int nchunk,
+__global__ void __launch_bounds__(128) k_zreduce(const void* Z, int is_bf16, int V, int nchunk,
                                                  float inv_T, float* zmax, int* zarg, float* zsum,
                                                  int* zero_ptr, int zero_count) {
   if (blockIdx.x == 0 && blockIdx.y == 0 && zero_ptr != nullptr)
@@ -92,38 +63,21 @@ __global__ void __launch_bounds__(256) k_zreduce(const void* Z, int is_bf16, int
   const int row = blockIdx.y, chunk = blockIdx.x;
   const size_t rbase = static_cast<size_t>(row) * V;
   float x[4][8];
-  RowStat st{-INFINITY, kIntMax, 0.f};
+  int v0[4];
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    const int v0 = chunk * kZChunk + g * 2048 + threadIdx.x * 8;
-    if (v0 < V) {
-      load8(Z, is_bf16, rbase + v0, x[g]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[g][j] = -INFINITY;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (x[g][j] > st.m) {
-        st.m = x[g][j];
-        st.i = v0 + j;
-      }
+    v0[g] = chunk * kZChunk + g * 1024 + threadIdx.x * 8;
+    if (v0[g] < V) load8_stream(Z, is_bf16, rbase + v0[g], x[g]);
   }
-  if (kSoft && st.m != -INFINITY) {
-    float s = 0.f;
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) s += expf((x[g][j] - st.m) * inv_T);
-    st.s = s;
-  }
+  RowStat st = rowstat_empty();
+  rowstat_fold<4, kSoft>(st, x, v0, V, inv_T);
   st = warp_combine(st, inv_T);
-  __shared__ RowStat ws[8];
+  __shared__ RowStat ws[4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) ws[warp] = st;
   __syncthreads();
   if (warp == 0) {
-    st = lane < 8 ? ws[lane] : RowStat{-INFINITY, kIntMax, 0.f};
+    st = lane < 4 ? ws[lane] : rowstat_empty();
     st = warp_combine(st, inv_T);
     if (lane == 0) {
       const size_t o = static_cast<size_t>(row) * nchunk + chunk;
@@ -136,7 +90,7 @@ __global__ void __launch_bounds__(256) k_zreduce(const void* Z, int is_bf16, int
 
 // Merged statistics of one target row, computed by one warp.
 __device__ RowStat row_stat_warp(const TailLaunch& a, int row) {
-  RowStat st{-INFINITY, kIntMax, 0.f};
+  RowStat st = rowstat_empty();
   const float inv_T = a.T > 0.f ? 1.0f / a.T : 0.f;
   for (int c = threadIdx.x & 31; c < a.nchunk; c += 32) {
     const size_t o = static_cast<size_t>(row) * a.nchunk + c;
@@ -473,6 +427,8 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
 // 16 x 16 pairs of position t, and the last block of request b runs path + verification.
 __global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_constant__ TailLaunch a) {
   extern __shared__ __align__(16) uint8_t tail_smem[];
+  grid_dependents_launch();  // a following redraw kernel may take free SMs and wait there
+  grid_dependency_wait();    // the LM-head kernel's results (launched as its dependent)
   const int t = blockIdx.x + 1, b = blockIdx.y, L = a.L, P = L - 1;
   TailSmem sm = carve(tail_smem, a.G, a.r, true);
   const int warp = threadIdx.x >> 5;
@@ -564,9 +520,10 @@ __global__ void __launch_bounds__(kTailThreads) k_verify(const __grid_constant__
   verify_block(a, b, path_tok, rm, rl, ry);
 }
 
-// Gumbel-max redraw for T > 0: block (chunk, b) scans kZChunk tokens of the row named in
+// Gumbel-max redraw for T > 0: block (chunk, b) scans kRChunk tokens of the row named in
 // resample_info[b]; the last block of the request merges the per-chunk winners.
 __global__ void __launch_bounds__(256) k_resample(const __grid_constant__ TailLaunch a) {
+  grid_dependency_wait();  // the verification kernel's redraw requests
   const int b = blockIdx.y, chunk = blockIdx.x, L = a.L;
   const int* info = a.resample_info + static_cast<size_t>(b) * 4;
   const int row = __ldcg(info), excl = __ldcg(info + 1), slot = __ldcg(info + 2);
@@ -576,7 +533,7 @@ __global__ void __launch_bounds__(256) k_resample(const __grid_constant__ TailLa
   int bi = kIntMax;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    const int v0 = chunk * kZChunk + g * 2048 + threadIdx.x * 8;
+    const int v0 = chunk * kRChunk + g * 2048 + threadIdx.x * 8;
     if (v0 >= a.V) continue;
     float x[8];
     load8(a.Z, a.zdtype == 0, rbase + v0, x);
@@ -622,19 +579,19 @@ __global__ void __launch_bounds__(256) k_resample(const __grid_constant__ TailLa
         bk = sk[w];
         bi = si[w];
       }
-    a.gumbel_key[static_cast<size_t>(b) * a.nchunk + chunk] = bk;
-    a.gumbel_idx[static_cast<size_t>(b) * a.nchunk + chunk] = bi;
+    a.gumbel_key[static_cast<size_t>(b) * a.nrchunk + chunk] = bk;
+    a.gumbel_idx[static_cast<size_t>(b) * a.nrchunk + chunk] = bi;
     __threadfence();
-    last = (atomicAdd(a.resample_counters + b, 1) == a.nchunk - 1);
+    last = (atomicAdd(a.resample_counters + b, 1) == a.nrchunk - 1);
   }
   __syncthreads();
   if (!last || threadIdx.x != 0) return;
   __threadfence();
   float fk = -INFINITY;
   int fi = kIntMax;
-  for (int c = 0; c < a.nchunk; ++c) {
-    const float k = __ldcg(a.gumbel_key + static_cast<size_t>(b) * a.nchunk + c);
-    const int i = __ldcg(a.gumbel_idx + static_cast<size_t>(b) * a.nchunk + c);
+  for (int c = 0; c < a.nrchunk; ++c) {
+    const float k = __ldcg(a.gumbel_key + static_cast<size_t>(b) * a.nrchunk + c);
+    const int i = __ldcg(a.gumbel_idx + static_cast<size_t>(b) * a.nrchunk + c);
     if (ranks_before(k, i, fk, fi)) {
       fk = k;
       fi = i;
@@ -642,6 +599,25 @@ __global__ void __launch_bounds__(256) k_resample(const __grid_constant__ TailLa
   }
   a.out_tokens[static_cast<size_t>(b) * L + slot] = fi;
   a.resample_counters[b] = 0;
+}
+
+// Launch as a programmatic dependent of the previous kernel on the stream: the launch is
+// processed while that kernel drains; the kernel waits (griddepcontrol.wait) before it
+// reads what its predecessor wrote.
+template <typename K>
+cudaError_t launch_dependent(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             const TailLaunch& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <typename K>
@@ -655,10 +631,10 @@ cudaError_t set_smem(K kern, size_t bytes) {
 cudaError_t launch_zreduce(const ZReduceLaunch& a, cudaStream_t s) {
   dim3 grid(a.nchunk, a.rows);
   if (a.inv_T > 0.f)
-    k_zreduce<true><<<grid, 256, 0, s>>>(a.Z, a.zdtype == 0, a.V, a.nchunk, a.inv_T, a.zmax,
+    k_zreduce<true><<<grid, 128, 0, s>>>(a.Z, a.zdtype == 0, a.V, a.nchunk, a.inv_T, a.zmax,
                                          a.zarg, a.zsum, a.zero_ptr, a.zero_count);
   else
-    k_zreduce<false><<<grid, 256, 0, s>>>(a.Z, a.zdtype == 0, a.V, a.nchunk, 0.f, a.zmax,
+    k_zreduce<false><<<grid, 128, 0, s>>>(a.Z, a.zdtype == 0, a.V, a.nchunk, 0.f, a.zmax,
                                           a.zarg, a.zsum, a.zero_ptr, a.zero_count);
   return cudaGetLastError();
 }
@@ -667,8 +643,7 @@ cudaError_t launch_tail_fused(const TailLaunch& a, cudaStream_t s) {
   const size_t bytes = tail_smem_bytes(a.G, a.r, true);
   cudaError_t e = set_smem(k_tail_fused, bytes);
   if (e != cudaSuccess) return e;
-  k_tail_fused<<<dim3(a.L - 1, a.B), kTailThreads, bytes, s>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(k_tail_fused, dim3(a.L - 1, a.B), dim3(kTailThreads), bytes, s, a);
 }
 
 cudaError_t launch_merge(const TailLaunch& a, cudaStream_t s) {
@@ -698,8 +673,7 @@ cudaError_t launch_verify(const TailLaunch& a, cudaStream_t s) {
 }
 
 cudaError_t launch_resample(const TailLaunch& a, cudaStream_t s) {
-  k_resample<<<dim3(a.nchunk, a.B), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(k_resample, dim3(a.nrchunk, a.B), dim3(256), 0, s, a);
 }
 
 }  // namespace dfs

@@ -45,27 +45,38 @@ def _run(data, spec, mode, T, seed):
 
 
 def _compare(g, o, spec, reqs, T):
-    """Exact ids/paths/accept lengths on requests without near-ties; returns excluded count."""
-    excluded = 0
+    """Exact ids, paths and accept lengths. A request may differ only where the oracle shows
+    a near-tie for the decision that differs; such requests are counted and skipped
+    downstream. Returns the number of requests that diverged on a near-tie."""
+    diverged = 0
     P = spec.L - 1
     for q, b in enumerate(reqs):
-        near = (np.any(o["topk_gap"][q] < TOPK_GAP * np.abs(o["cand_U"][q][:, -1]))
-                or o["path_margin"][q] < PATH_MARGIN
-                or (T > 0 and (o["acc_margin"][q] < ACC_MARGIN or o["gumbel_margin"][q] < GUMBEL_MARGIN)))
-        if near:
-            excluded += 1
+        sets_equal = True
+        for p in range(P):
+            if sorted(g["cand_ids"][b, p].tolist()) != sorted(o["cand_ids"][q, p].tolist()):
+                assert o["topk_gap"][q, p] < TOPK_GAP * abs(o["cand_U"][q, p, -1]), \
+                    f"request {b} position {p + 1}: top-16 differs without a near-tie"
+                sets_equal = False
+        if not sets_equal:
+            diverged += 1
             continue
         for p in range(P):
-            assert sorted(g["cand_ids"][b, p].tolist()) == sorted(o["cand_ids"][q, p].tolist())
             Sg = reorder_S_to(o["cand_ids"][q, p - 1] if p else None, o["cand_ids"][q, p],
                               g["cand_ids"][b, p - 1] if p else None, g["cand_ids"][b, p],
                               g["S"][b, p], p == 0)
             assert np.all(close(Sg, o["S"][q, p])), f"request {b} position {p + 1}: scores"
-        assert g["path"][b].tolist() == o["path"][q].tolist(), f"request {b}: path"
+        if g["path"][b].tolist() != o["path"][q].tolist():
+            assert o["path_margin"][q] < PATH_MARGIN, f"request {b}: path differs without a near-tie"
+            diverged += 1
+            continue
         assert close(g["path_score"][b], o["path_score"][q])
-        assert g["accept_len"][b] == o["accept_len"][q], f"request {b}: accept length"
-        assert g["out_tokens"][b].tolist() == o["out_tokens"][q].tolist(), f"request {b}: tokens"
-    return excluded
+        same = (g["accept_len"][b] == o["accept_len"][q]
+                and g["out_tokens"][b].tolist() == o["out_tokens"][q].tolist())
+        if not same:
+            assert T > 0 and (o["acc_margin"][q] < ACC_MARGIN or o["gumbel_margin"][q] < GUMBEL_MARGIN), \
+                f"request {b}: verification differs without a near-tie"
+            diverged += 1
+    return diverged
 
 
 def _invariants(g, spec, npd, T):
@@ -99,8 +110,8 @@ def test_fused_small(lib, orc, spec, mode, T):
     g = _run(data, spec, mode, T, seed=spec.seed + 100)
     o = orc.select_verify(npd["h"], npd["W"], npd["Wg"], npd["A"], npd["Bt"], npd["x0"], npd["Z"],
                           path_mode=mode, temperature=T, seed=spec.seed + 100)
-    excluded = _compare(g, o, spec, list(range(spec.B)), T)
-    assert excluded <= max(1, spec.B // 5)
+    diverged = _compare(g, o, spec, list(range(spec.B)), T)
+    assert diverged <= max(1, spec.B // 8)
     _invariants(g, spec, npd, T)
 
 
@@ -134,5 +145,5 @@ def test_fused_full_size(lib, orc, spec, reqs):
             o = orc.select_verify(npd["h"], npd["W"], npd["Wg"], npd["A"], npd["Bt"], npd["x0"],
                                   npd["Z"], path_mode=mode, temperature=T, seed=spec.seed,
                                   reqs=reqs)
-            excluded = _compare(g, o, spec, reqs, T)
-            assert excluded <= max(1, len(reqs) // 2), f"{excluded} of {len(reqs)} excluded"
+            diverged = _compare(g, o, spec, reqs, T)
+            assert diverged <= max(1, len(reqs) // 2), f"{diverged} of {len(reqs)} diverged"

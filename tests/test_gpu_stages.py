@@ -57,8 +57,8 @@ def test_lmhead_topk(lib, orc, spec, variant, monkeypatch):
     torch.cuda.synchronize()
     assert binding.dfs_get_device_error(ws) == binding.DFS_OK
     o_ids, o_U, o_gap, _ = _oracle_candidates(orc, npd, spec)
-    n, excl = compare_topk(to_cpu(ids), to_cpu(U), o_ids, o_U, o_gap)
-    assert excl <= max(1, n // 10), f"{excl}/{n} rows excluded as near-ties"
+    n, near, diverged = compare_topk(to_cpu(ids), to_cpu(U), o_ids, o_U, o_gap)
+    assert diverged <= max(1, n // 50), f"{diverged}/{n} rows diverged on near-ties ({near} near)"
 
 
 @pytest.mark.parametrize("spec", SHAPES, ids=lambda s: s.name)
@@ -106,16 +106,16 @@ def test_path_select(lib, orc, P, values, mode):
     torch.cuda.synchronize()
     path, score = to_cpu(path), to_cpu(score)
     fn = orc.path_viterbi if mode == binding.DFS_PATH_VITERBI else orc.path_greedy
-    excluded = 0
+    diverged = 0
     for b in range(B):
         o_path, _, o_score, margin = fn(S[b].astype(np.float64), ids[b])
-        # integer lattices are exact in fp32, so ties must be broken identically there
-        if values == "random" and margin < PATH_MARGIN:
-            excluded += 1
+        if path[b].tolist() != o_path.tolist():
+            # integer lattices are exact in fp32, so ties must be broken identically there
+            assert values == "random" and margin < PATH_MARGIN, f"request {b}: path differs"
+            diverged += 1
             continue
-        assert path[b].tolist() == o_path.tolist(), f"request {b}"
         assert close(score[b], o_score)
-    assert excluded <= B // 8
+    assert diverged <= B // 16
 
 
 def _planted_path(rng, Z, L, agree):
@@ -164,11 +164,10 @@ def test_verify_sampling(lib, orc, T, L, V):
     out, acc = binding.dfs_verify(dims, torch.from_numpy(path).cuda(), Zt, T, seed, ws)
     torch.cuda.synchronize()
     out, acc = to_cpu(out), to_cpu(acc)
-    excluded = 0
+    diverged = 0
     for b in range(B):
         o_out, o_acc, am, gm = orc.verify_sampling(Znp[b], path[b], T, seed, b=b)
-        if am < ACC_MARGIN or gm < GUMBEL_MARGIN:
-            excluded += 1
-            continue
-        assert acc[b] == o_acc and out[b].tolist() == o_out.tolist(), f"request {b}"
-    assert excluded <= B // 10
+        if acc[b] != o_acc or out[b].tolist() != o_out.tolist():
+            assert am < ACC_MARGIN or gm < GUMBEL_MARGIN, f"request {b}: differs without a near-tie"
+            diverged += 1
+    assert diverged <= B // 16
