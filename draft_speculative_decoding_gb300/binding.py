@@ -44,6 +44,7 @@ SIGNATURES = {
     "dfs_path_select": ([_DP, _P, _P, _I, _P, _P, _P], _I),
     "dfs_verify": ([_DP, _P, _P, ctypes.c_float, ctypes.c_uint64, _P, _P, _P, ctypes.c_size_t, _P],
                    _I),
+    "dfs_verify_noalloc": ([_DP, _P, _P, ctypes.c_float, ctypes.c_uint64, _P, _P, _P], _I),
     "dfs_select_verify": ([_DP, _P, _P, _P, _P, _P, _P, _P, _I, ctypes.c_float, ctypes.c_uint64,
                            _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
 }
@@ -184,6 +185,18 @@ def dfs_verify(dims: Dims, path, target_logits, temperature: float, seed: int, w
     _check("dfs_verify", load().dfs_verify(
         ctypes.byref(dims), _ptr(path), _ptr(target_logits), float(temperature),
         int(seed) & (2**64 - 1), _ptr(out), _ptr(acc), _ptr(ws), ws.numel(), _stream(stream)))
+    return out, acc
+
+
+def dfs_verify_noalloc(dims: Dims, path, target_logits, temperature: float, seed: int,
+                       stream=None):
+    """dfs_verify with the library's built-in scratch: no workspace, nothing allocated by
+    the library (the outputs below are allocated here, by the caller's side)."""
+    out = torch.empty(dims.B, dims.L, dtype=torch.int32, device=path.device)
+    acc = torch.empty(dims.B, dtype=torch.int32, device=path.device)
+    _check("dfs_verify_noalloc", load().dfs_verify_noalloc(
+        ctypes.byref(dims), _ptr(path), _ptr(target_logits), float(temperature),
+        int(seed) & (2**64 - 1), _ptr(out), _ptr(acc), _stream(stream)))
     return out, acc
 
 

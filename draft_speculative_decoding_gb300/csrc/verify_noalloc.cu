@@ -1,0 +1,139 @@
+// verify_noalloc.cu -- dfs_verify_noalloc: the verification step (target-row statistics,
+// greedy or rejection-sampling acceptance, redraw) with its scratch memory built into the
+// library instead of passed in by the caller.
+//
+// It exists for callers that cannot allocate device memory at the point where they verify:
+// code running inside a serving loop whose memory pool is owned by another component,
+// plugins handed only the input and output tensors of one step, or a host thread that must
+// not enter the CUDA allocator (which can synchronise the device). Such a caller passes its
+// inputs and outputs and nothing else.
+//
+// The scratch is one file-scope device array of kScratchBytes. Every GPU that loads the
+// library holds it until the process exits. All calls share it and it keeps the last
+// call's contents; the counters that must start at zero are cleared by the first kernel of
+// each call. Calls whose work overlaps on the GPU (different streams, or different host
+// threads) race on the array: issue them in order on one stream.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/dfs.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = size_t(4) << 20;  // 4 MiB
+constexpr size_t kAlign = 256;
+
+static __device__ __align__(256) unsigned char g_verify_scratch[kScratchBytes];
+
+inline size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+// The device address of g_verify_scratch on the current device. In host code the array's
+// name only stands in for the symbol; the address a kernel can use comes from the runtime,
+// once per device, with that device current (the first call on each device does this).
+void* scratch_on_current_device() {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int dfs_verify_noalloc(const dfs_dims* d, const int32_t* path,
+                                  const void* target_logits, float temperature, uint64_t seed,
+                                  int32_t* out_tokens, int32_t* accept_len, void* stream) {
+  if (d == nullptr || path == nullptr || target_logits == nullptr || out_tokens == nullptr ||
+      accept_len == nullptr)
+    return DFS_ERR_INVALID;
+  if (!aligned16(path) || !aligned16(target_logits) || !aligned16(out_tokens) ||
+      !aligned16(accept_len))
+    return DFS_ERR_INVALID;
+  if (d->B < 1 || d->L < 2 || d->V < 1) return DFS_ERR_INVALID;
+  if (!(temperature >= 0.f)) return DFS_ERR_INVALID;
+  if (d->K != dfs::kK || d->L > dfs::kMaxL || d->V < dfs::kK || d->V % 8 != 0 ||
+      (d->zdtype != DFS_BF16 && d->zdtype != DFS_FP32))
+    return DFS_ERR_UNSUPPORTED;
+
+  const size_t B = static_cast<size_t>(d->B);
+  const size_t rows = B * static_cast<size_t>(d->L);
+  const int nchunk = (d->V + dfs::kZChunk - 1) / dfs::kZChunk;
+  const int nrchunk = (d->V + dfs::kRChunk - 1) / dfs::kRChunk;
+  // Layout inside the array: the two counter arrays first (cleared together each call).
+  size_t off = 0;
+  const size_t o_cnt = off;
+  off = up(off + 4 * B);
+  const size_t o_rcnt = off;
+  off = up(off + 4 * B);
+  const size_t zero_end = off;
+  const size_t o_zmax = off;
+  off = up(off + 4 * rows * nchunk);
+  const size_t o_zarg = off;
+  off = up(off + 4 * rows * nchunk);
+  const size_t o_zsum = off;
+  off = up(off + 4 * rows * nchunk);
+  const size_t o_info = off;
+  off = up(off + 16 * B);
+  const size_t o_gkey = off;
+  off = up(off + 4 * B * nrchunk);
+  const size_t o_gidx = off;
+  off = up(off + 4 * B * nrchunk);
+  const size_t o_err = off;
+  off = up(off + 16);
+  if (off > kScratchBytes) return DFS_ERR_WORKSPACE;  // the built-in scratch is too small
+
+  char* base = static_cast<char*>(scratch_on_current_device());
+  if (base == nullptr) return DFS_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  dfs::ZReduceLaunch z{};
+  z.Z = target_logits;
+  z.zdtype = d->zdtype;
+  z.rows = static_cast<int>(rows);
+  z.V = d->V;
+  z.nchunk = nchunk;
+  z.inv_T = temperature > 0.f ? 1.0f / temperature : 0.f;
+  z.zmax = reinterpret_cast<float*>(base + o_zmax);
+  z.zarg = reinterpret_cast<int*>(base + o_zarg);
+  z.zsum = reinterpret_cast<float*>(base + o_zsum);
+  z.zero_ptr = reinterpret_cast<int*>(base + o_cnt);
+  z.zero_count = static_cast<int>(zero_end / 4);
+  if (dfs::launch_zreduce(z, s) != cudaSuccess) return DFS_ERR_CUDA;
+
+  dfs::TailLaunch t{};
+  t.B = d->B;
+  t.L = d->L;
+  t.V = d->V;
+  t.zdtype = d->zdtype;
+  t.Z = target_logits;
+  t.zmax = z.zmax;
+  t.zarg = z.zarg;
+  t.zsum = z.zsum;
+  t.nchunk = nchunk;
+  t.nrchunk = nrchunk;
+  t.T = temperature;
+  t.seed = seed;
+  t.path = const_cast<int*>(path);
+  t.out_tokens = out_tokens;
+  t.accept_len = accept_len;
+  t.resample_info = reinterpret_cast<int*>(base + o_info);
+  t.counters = reinterpret_cast<int*>(base + o_cnt);
+  t.gumbel_key = reinterpret_cast<float*>(base + o_gkey);
+  t.gumbel_idx = reinterpret_cast<int*>(base + o_gidx);
+  t.resample_counters = reinterpret_cast<int*>(base + o_rcnt);
+  t.err = reinterpret_cast<int*>(base + o_err);
+  if (dfs::launch_verify(t, s) != cudaSuccess) return DFS_ERR_CUDA;
+  if (temperature > 0.f && dfs::launch_resample(t, s) != cudaSuccess) return DFS_ERR_CUDA;
+  return DFS_OK;
+}

@@ -158,6 +158,25 @@ int dfs_verify(const dfs_dims* dims, const int32_t* path, const void* target_log
                float temperature, uint64_t seed, int32_t* out_tokens, int32_t* accept_len,
                void* ws, size_t ws_bytes, void* stream);
 
+/* dfs_verify without a workspace argument, for callers that cannot allocate device memory
+ * at the point where they verify: a step that is handed only its input and output tensors,
+ * code whose device memory pool belongs to another component, or a host thread that must
+ * not enter the CUDA allocator. The pages have no counterpart; this is a packaging of
+ * dfs_verify with identical results, and no allocation happens in it.
+ *   Scratch: a 4 MiB device array built into the library, held by every GPU that loads the
+ *   library until the process exits. The call returns DFS_ERR_WORKSPACE when the shape
+ *   needs more, roughly when 12 * B * L * ceil(V / 4096) + B * (24 + 8 * ceil(V / 8192))
+ *   bytes exceed 4 MiB (B * L up to about 9000 at V = 151936).
+ *   Set-up: the first call on each device asks the runtime for the array's device address,
+ *   with that device current; make that first call before any stream capture.
+ *   Sharing: all calls use the one array, which keeps the last call's contents; each call
+ *   clears the counters it needs. Calls that overlap on the GPU (other streams, other host
+ *   threads) race on it: issue them one after another on one stream.
+ *   Arguments: as dfs_verify; of dims only B, L, K, V and zdtype are read. */
+int dfs_verify_noalloc(const dfs_dims* dims, const int32_t* path, const void* target_logits,
+                       float temperature, uint64_t seed, int32_t* out_tokens, int32_t* accept_len,
+                       void* stream);
+
 /* The whole step, a1..a6, fused: the LM head, gate, pair scores, path and
  * verification above in one enqueue, with the same inputs and outputs.
  * cand_ids_opt, cand_U_opt, S_opt and path_score_opt may be NULL. */
