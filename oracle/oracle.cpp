@@ -25,7 +25,8 @@
  *   orc_path_greedy .......... hand-worked golden lattice; A = 0 gives top-1
  *   orc_verify_greedy ........ equality with target-argmax decoding
  *   orc_verify_sampling ...... chi-square of emitted-token marginals against
- *                              the target softmax; limiting cases
+ *                              the target softmax (1e6 draws; and draws over a
+ *                              vocabulary of several redraw chunks); limiting cases
  *   orc_philox4x64 ........... numpy.random.Philox raw output
  *   accept length ............ closed form that reproduces the [Blog] Table 1
  *                              verify lengths 4.27 / 6.79
@@ -107,24 +108,27 @@ inline double u01(uint64_t x) {
 /* Counter layout shared by definition (not by code) with the GPU path:
  *   key     = (seed, 0)
  *   accept  : counter (0, t, b, 0), word 0           -- position t = 1..L-1
- *   gumbel  : counter (v >> 2, t, b, 1), word v & 3  -- row t-1 verifies position t;
- *             the bonus row L-1 uses t = L                                     */
-double uniform_accept(uint64_t seed, int64_t b, int t) {
-  uint64_t ctr[4] = {0ULL, static_cast<uint64_t>(t), static_cast<uint64_t>(b), 0ULL};
+ *   chunk   : counter (0, t, b, 2), word 0           -- the redraw's chunk choice
+ *   gumbel  : counter (v >> 2, t, b, 1), word v & 3  -- the redraw within the chunk
+ * The redraw from row t-1 uses position t; the bonus row L-1 uses t = L. */
+double uniform_counter(uint64_t seed, int64_t b, int t, uint64_t idx, uint64_t stream, int word) {
+  uint64_t ctr[4] = {idx, static_cast<uint64_t>(t), static_cast<uint64_t>(b), stream};
   uint64_t key[2] = {seed, 0ULL};
   uint64_t o[4];
   philox4x64_10(ctr, key, o);
-  return u01(o[0]);
+  return u01(o[word]);
 }
 
+double uniform_accept(uint64_t seed, int64_t b, int t) { return uniform_counter(seed, b, t, 0, 0, 0); }
+
 double uniform_gumbel(uint64_t seed, int64_t b, int t, int64_t v) {
-  uint64_t ctr[4] = {static_cast<uint64_t>(v) >> 2, static_cast<uint64_t>(t),
-                     static_cast<uint64_t>(b), 1ULL};
-  uint64_t key[2] = {seed, 0ULL};
-  uint64_t o[4];
-  philox4x64_10(ctr, key, o);
-  return u01(o[v & 3]);
+  return uniform_counter(seed, b, t, static_cast<uint64_t>(v) >> 2, 1, static_cast<int>(v & 3));
 }
+
+double uniform_chunk(uint64_t seed, int64_t b, int t) { return uniform_counter(seed, b, t, 0, 2, 0); }
+
+/* Tokens per chunk of the two-stage redraw. */
+const int64_t kRedrawChunk = 4096;
 
 /* log-sum-exp of z/T over one row, in double. */
 double row_lse(const void* Z, int zdtype, int64_t off, int64_t V, double T) {
@@ -135,16 +139,16 @@ double row_lse(const void* Z, int zdtype, int64_t off, int64_t V, double T) {
   return m + std::log(s);
 }
 
-/* Gumbel-max draw from softmax(z/T) restricted to v != excl (excl < 0: none):
+/* Gumbel-max draw from softmax(z/T) restricted to v in [lo, hi), v != excl:
  * argmax_v z_v/T + G_v with G_v = -log(-log U_v). The argmax of independent
  * Gumbel-perturbed logits is an exact sample from the renormalised softmax
- * (Gumbel 1954; the Gumbel-max trick). Returns the token and the relative
- * gap between the two largest keys. */
-int64_t gumbel_argmax(const void* Z, int zdtype, int64_t off, int64_t V, double T, uint64_t seed,
-                      int64_t b, int t, int64_t excl, double* rel_gap) {
+ * (Gumbel 1954; the Gumbel-max trick). Returns the token and the relative gap
+ * between the two largest keys. */
+int64_t gumbel_argmax(const void* Z, int zdtype, int64_t off, int64_t lo, int64_t hi, double T,
+                      uint64_t seed, int64_t b, int t, int64_t excl, double* rel_gap) {
   int64_t best = -1;
   double bk = -kInf, second = -kInf;
-  for (int64_t v = 0; v < V; ++v) {
+  for (int64_t v = lo; v < hi; ++v) {
     if (v == excl) continue;
     double g = -std::log(-std::log(uniform_gumbel(seed, b, t, v)));
     double key = widen(Z, zdtype, off + v) / T + g;
@@ -158,6 +162,43 @@ int64_t gumbel_argmax(const void* Z, int zdtype, int64_t off, int64_t V, double 
   }
   *rel_gap = (second == -kInf) ? kInf : rel(bk - second, bk);
   return best;
+}
+
+/* An exact draw from p = softmax(z/T) with token excl removed (excl < 0: none) and
+ * renormalised, in two stages: (1) a chunk of kRedrawChunk consecutive tokens is chosen
+ * with probability proportional to its mass under the residual distribution, by one
+ * uniform against the chunks' cumulative masses in vocabulary order (if rounding leaves
+ * no chunk above the target, the last chunk with mass is taken); (2) the token is the
+ * Gumbel-max over that chunk. P(v) = (mass_c / total) (p_v / mass_c) = p_v / total.
+ * margin = the smaller of the chunk choice's relative distance to a cumulative boundary
+ * and the Gumbel draw's relative top-2 gap. */
+int64_t redraw(const void* Z, int zdtype, int64_t off, int64_t V, double T, uint64_t seed,
+               int64_t b, int t, int64_t excl, double* margin) {
+  double m = -kInf;
+  for (int64_t v = 0; v < V; ++v) m = std::max(m, widen(Z, zdtype, off + v) / T);
+  const int64_t nchunk = (V + kRedrawChunk - 1) / kRedrawChunk;
+  std::vector<double> mass(nchunk, 0.0);
+  for (int64_t c = 0; c < nchunk; ++c)
+    for (int64_t v = c * kRedrawChunk; v < std::min(V, (c + 1) * kRedrawChunk); ++v)
+      if (v != excl) mass[c] += std::exp(widen(Z, zdtype, off + v) / T - m);
+  double total = 0.0;
+  for (int64_t c = 0; c < nchunk; ++c) total += mass[c];
+  const double target = uniform_chunk(seed, b, t) * total;
+  int64_t pick = -1, last_nonzero = 0;
+  double cum = 0.0, cmargin = kInf;
+  for (int64_t c = 0; c < nchunk; ++c) {
+    cum += mass[c];
+    if (mass[c] > 0.0) last_nonzero = c;
+    if (c + 1 < nchunk) cmargin = std::min(cmargin, std::fabs(cum - target) / total);
+    if (pick < 0 && cum > target) pick = c;
+  }
+  if (pick < 0) pick = last_nonzero;
+  double gmargin;
+  const int64_t y = gumbel_argmax(Z, zdtype, off, pick * kRedrawChunk,
+                                  std::min(V, (pick + 1) * kRedrawChunk), T, seed, b, t, excl,
+                                  &gmargin);
+  *margin = std::min(cmargin, gmargin);
+  return y;
 }
 
 }  // namespace
@@ -387,10 +428,10 @@ int orc_verify_greedy(int zdtype, const void* Z, int L, int64_t V, const int32_t
  * deterministic proposal. p_i = softmax(Z[i]/T). For t = 1..L-1: accept x_t
  * when U < p_{t-1}(x_t); on the first rejection emit a draw from p_{t-1}
  * with x_t removed and renormalised and stop (accept_len = t); when all are
- * accepted emit a bonus draw from p_{L-1} (accept_len = L).
+ * accepted emit a bonus draw from p_{L-1} (accept_len = L). Draws use the
+ * two-stage redraw above.
  * acc_margin = smallest |U - p| / p over the tests made; gum_margin = the
- * relative top-2 gap of the Gumbel draw. b is the request's batch index (it
- * is part of the random counter). */
+ * redraw's margin. b is the request's batch index (part of the counter). */
 int orc_verify_sampling(int zdtype, const void* Z, int L, int64_t V, const int32_t* path,
                         double T, uint64_t seed, int64_t b, int32_t* out, int32_t* accept_len,
                         double* acc_margin, double* gum_margin) {
@@ -407,13 +448,13 @@ int orc_verify_sampling(int zdtype, const void* Z, int L, int64_t V, const int32
       out[t - 1] = static_cast<int32_t>(x);
       continue;
     }
-    out[t - 1] = static_cast<int32_t>(gumbel_argmax(Z, zdtype, off, V, T, seed, b, t, x, gum_margin));
+    out[t - 1] = static_cast<int32_t>(redraw(Z, zdtype, off, V, T, seed, b, t, x, gum_margin));
     *accept_len = t;
     *acc_margin = am;
     return 0;
   }
   const int64_t off = static_cast<int64_t>(L - 1) * V;
-  out[L - 1] = static_cast<int32_t>(gumbel_argmax(Z, zdtype, off, V, T, seed, b, L, -1, gum_margin));
+  out[L - 1] = static_cast<int32_t>(redraw(Z, zdtype, off, V, T, seed, b, L, -1, gum_margin));
   *accept_len = L;
   *acc_margin = am;
   return 0;

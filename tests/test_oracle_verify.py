@@ -217,3 +217,42 @@ def test_sampling_depends_on_request_index_and_seed(orc):
     s = [tuple(orc.verify_sampling(Z, path, 1.0, seed=sd, b=0)[0]) for sd in range(50)]
     assert len(set(a)) > 10 and len(set(s)) > 10
     assert tuple(orc.verify_sampling(Z, path, 1.0, seed=5, b=3)[0].tolist()) == a[3]
+
+
+@pytest.fixture(scope="module")
+def multichunk_runs(orc):
+    """A vocabulary of three redraw chunks (4096, 4096, 1000 tokens) with very different
+    masses; the proposal has negligible probability, so every draw is a redraw."""
+    rng = np.random.default_rng(99)
+    V, T = 2 * 4096 + 1000, 1.0
+    z = rng.standard_normal(V)
+    z[4096:8192] += 1.0
+    z[8192:] += 2.0
+    x = 17
+    z[x] = -40.0
+    Z = np.stack([z, rng.standard_normal(V)]).astype(np.float32)
+    n = 120_000
+    out, acc = orc.verify_sampling_many(Z, np.array([x], np.int32), T, seed0=31, n=n)
+    return dict(Z=Z, T=T, x=x, out=out, acc=acc, n=n, V=V)
+
+
+def test_redraw_chunk_choice_follows_residual_mass(multichunk_runs):
+    r = multichunk_runs
+    assert np.all(r["acc"] == 1)
+    p = _softmax(r["Z"][0], r["T"])
+    p[r["x"]] = 0.0
+    p /= p.sum()
+    chunk = r["out"][:, 0] // 4096
+    counts = np.bincount(chunk, minlength=3).astype(np.float64)
+    expect = np.array([p[:4096].sum(), p[4096:8192].sum(), p[8192:].sum()])
+    assert _chi2_pvalue(counts, expect) > 0.01
+
+
+def test_redraw_token_distribution_is_residual_target(multichunk_runs):
+    r = multichunk_runs
+    p = _softmax(r["Z"][0], r["T"])
+    p[r["x"]] = 0.0
+    p /= p.sum()
+    counts = np.bincount(r["out"][:, 0], minlength=r["V"]).astype(np.float64)
+    assert counts[r["x"]] == 0
+    assert _chi2_pvalue(counts, p) > 0.01
