@@ -32,24 +32,25 @@ int device_sm_count() {
   return cache[dev];
 }
 
-// Tile-shape choice for row groups of 129..256 rows: 0 = automatic, 1 = two 128-row MMA
-// tiles x 128 vocabulary columns (double-buffered TMEM), 2 = two tiles x 256 columns
-// (single-buffered). Read from DFS_LMHEAD_VARIANT on each call, for tuning.
+// Tile-shape choice for row groups of 129..256 rows: 0 = automatic (4), 1 = two 128-row MMA
+// tiles x 128 vocabulary columns with a deep W ring, 2 = two tiles x 256 columns
+// (single-buffered TMEM), 3 = as 1 with a deeper hidden-row ring, 4 = row-split pairs.
+// Read from DFS_LMHEAD_VARIANT on each call, for tuning.
 int lmhead_variant_override() {
   const char* s = std::getenv("DFS_LMHEAD_VARIANT");
   const int v = s ? std::atoi(s) : 0;
-  return (v < 0 || v > 2) ? 0 : v;
+  return (v <= 0 || v > 4) ? 4 : v;  // automatic: row-split pairs
 }
 
+
 struct Layout {
-  size_t err, counters, rcounters;
+  size_t err, counters;
   size_t part_val, part_idx, gate;
   size_t zmax, zarg, zsum;
   size_t cand_ids, cand_U, S, path;
-  size_t rinfo, gkey, gidx;
   size_t logits;
   size_t total;
-  int G, nchunk, nrchunk;
+  int G, nchunk;
 };
 
 int check_dims(const dfs_dims* d) {
@@ -58,6 +59,7 @@ int check_dims(const dfs_dims* d) {
   if ((d->dtype != DFS_BF16 && d->dtype != DFS_FP32) || (d->zdtype != DFS_BF16 && d->zdtype != DFS_FP32))
     return DFS_ERR_UNSUPPORTED;
   if (d->K != kK || d->L > dfs::kMaxL || d->V < kK || d->V % 8 != 0) return DFS_ERR_UNSUPPORTED;
+  if (d->V > dfs::kMaxZChunks * dfs::kZChunk) return DFS_ERR_UNSUPPORTED;
   if (d->r % 8 != 0 || d->r > dfs::kMaxRank) return DFS_ERR_UNSUPPORTED;
   if (d->dtype == DFS_BF16 && d->d % 64 != 0) return DFS_ERR_UNSUPPORTED;
   if (static_cast<long long>(d->B) * d->L > (1LL << 30)) return DFS_ERR_UNSUPPORTED;
@@ -67,9 +69,10 @@ int check_dims(const dfs_dims* d) {
 bool make_layout(const dfs_dims& d, Layout* L) {
   const int sms = device_sm_count();
   if (sms <= 0) return false;
-  L->G = d.dtype == DFS_BF16 ? (sms < dfs::kMaxLists ? sms : dfs::kMaxLists) : 1;
+  // one list per CTA of the persistent LM-head grid: a multiple of 4 so clusters tile it
+  L->G = d.dtype == DFS_BF16 ? ((sms < dfs::kMaxLists ? sms : dfs::kMaxLists) / 4) * 4 : 1;
+  if (L->G < 1) L->G = 1;
   L->nchunk = (d.V + dfs::kZChunk - 1) / dfs::kZChunk;
-  L->nrchunk = (d.V + dfs::kRChunk - 1) / dfs::kRChunk;
   const size_t rows = static_cast<size_t>(d.B) * d.L;
   const size_t P = static_cast<size_t>(d.L - 1);
   size_t off = 0;
@@ -80,7 +83,6 @@ bool make_layout(const dfs_dims& d, Layout* L) {
   };
   L->err = take(16);
   L->counters = take(4 * static_cast<size_t>(d.B));
-  L->rcounters = take(4 * static_cast<size_t>(d.B));
   L->part_val = take(4 * rows * L->G * kK);
   L->part_idx = take(4 * rows * L->G * kK);
   L->gate = take(4 * rows * d.r);
@@ -91,12 +93,15 @@ bool make_layout(const dfs_dims& d, Layout* L) {
   L->cand_U = take(4 * d.B * P * kK);
   L->S = take(4 * d.B * P * kK * kK);
   L->path = take(4 * d.B * P);
-  L->rinfo = take(16 * static_cast<size_t>(d.B));
-  L->gkey = take(4 * static_cast<size_t>(d.B) * L->nrchunk);
-  L->gidx = take(4 * static_cast<size_t>(d.B) * L->nrchunk);
   L->logits = take(d.dtype == DFS_FP32 ? 4 * rows * d.V : 0);
   L->total = off;
   return true;
+}
+
+// Partial top-16 lists per row that the LM-head kernel leaves for the tail.
+int lists_per_row(const dfs_dims& d, const Layout& L) {
+  return (d.dtype == DFS_BF16 &&
+          dfs::lmhead_row_split(d.B * d.L, lmhead_variant_override(), L.G)) ? L.G / 2 : L.G;
 }
 
 template <typename T>
@@ -144,16 +149,11 @@ dfs::TailLaunch tail_args(const dfs_dims& d, const Layout& L, void* ws) {
   t.zarg = at<int>(ws, L.zarg);
   t.zsum = at<float>(ws, L.zsum);
   t.nchunk = L.nchunk;
-  t.nrchunk = L.nrchunk;
   t.cand_ids = at<int>(ws, L.cand_ids);
   t.cand_U = at<float>(ws, L.cand_U);
   t.S = at<float>(ws, L.S);
   t.path = at<int>(ws, L.path);
-  t.resample_info = at<int>(ws, L.rinfo);
   t.counters = at<int>(ws, L.counters);
-  t.gumbel_key = at<float>(ws, L.gkey);
-  t.gumbel_idx = at<int>(ws, L.gidx);
-  t.resample_counters = at<int>(ws, L.rcounters);
   t.err = at<int>(ws, L.err);
   return t;
 }
@@ -168,18 +168,34 @@ cudaError_t run_zreduce(const dfs_dims& d, const Layout& L, void* ws, const void
 // With Z != nullptr the target-logit row statistics (and the per-call counter reset) are
 // produced alongside: by the tensor-core kernel's spare warps, or by the standalone
 // reduction kernel on the fp32 path.
+// CTAs per cluster of the LM-head kernel (they share the hidden-row tiles by TMA
+// multicast): 1, 2 or 4, default 2. Read from DFS_LMHEAD_CLUSTER on each call, for tuning.
+int lmhead_cluster() {
+  const char* s = std::getenv("DFS_LMHEAD_CLUSTER");
+  const int v = s ? std::atoi(s) : 2;
+  return (v == 1 || v == 2 || v == 4) ? v : 2;
+}
+
+// Where the target-logit row statistics are computed: 1 = by the LM-head kernel's spare
+// warps (default), 0 = by the standalone reduction kernel before it. Read from DFS_Z_FUSED
+// on each call, for tuning; both do the same work.
+bool z_fused() {
+  const char* s = std::getenv("DFS_Z_FUSED");
+  return s == nullptr || std::atoi(s) != 0;
+}
+
 cudaError_t run_lmhead(const dfs_dims& d, const Layout& L, void* ws, const void* hidden,
                        const void* W, const void* Wg, bool vocab, bool gate, cudaStream_t s,
                        const void* Z = nullptr, float T = 0.f) {
   const int rows = d.B * d.L;
-  if (Z != nullptr && d.dtype != DFS_BF16) {
+  if (Z != nullptr && (d.dtype != DFS_BF16 || !z_fused())) {
     cudaError_t ez = run_zreduce(d, L, ws, Z, T, s);
     if (ez != cudaSuccess) return ez;
   }
   if (vocab && g_trace_start != nullptr && cudaEventRecord(g_trace_start, s) != cudaSuccess)
     return cudaErrorInvalidResourceHandle;
   cudaError_t e = run_lmhead_kernels(d, L, ws, hidden, W, Wg, vocab, gate, s, rows,
-                                     d.dtype == DFS_BF16 ? Z : nullptr, T);
+                                     (d.dtype == DFS_BF16 && z_fused()) ? Z : nullptr, T);
   if (e == cudaSuccess && vocab && g_trace_stop != nullptr) e = cudaEventRecord(g_trace_stop, s);
   return e;
 }
@@ -205,6 +221,7 @@ cudaError_t run_lmhead_kernels(const dfs_dims& d, const Layout& L, void* ws, con
     a.gate_out = at<float>(ws, L.gate);
     a.err = at<int>(ws, L.err);
     a.lmhead_variant = lmhead_variant_override();
+    a.cluster = lmhead_cluster();
     if (Z != nullptr) {
       a.Z = Z;
       a.zdtype = d.zdtype;
@@ -249,7 +266,7 @@ cudaError_t run_zreduce(const dfs_dims& d, const Layout& L, void* ws, const void
   z.zmax = at<float>(ws, L.zmax);
   z.zarg = at<int>(ws, L.zarg);
   z.zsum = at<float>(ws, L.zsum);
-  // the counters and the resample counters are adjacent 256-byte aligned regions
+  // the per-request counters, cleared at the start of each call
   z.zero_ptr = at<int>(ws, L.counters);
   z.zero_count = static_cast<int>((L.part_val - L.counters) / 4);
   return dfs::launch_zreduce(z, s);
@@ -317,6 +334,7 @@ int dfs_lmhead_topk(const dfs_dims* dims, const void* hidden, const void* W_voca
   cudaError_t e = run_lmhead(*dims, L, ws, hidden, W_vocab, nullptr, true, false, s);
   if (e != cudaSuccess) return DFS_ERR_CUDA;
   dfs::TailLaunch t = tail_args(*dims, L, ws);
+  t.G = lists_per_row(*dims, L);
   t.cand_ids = cand_ids;
   t.cand_U = cand_U;
   return cuda_rc(dfs::launch_merge(t, s));
@@ -386,7 +404,6 @@ int dfs_verify(const dfs_dims* dims, const int32_t* path, const void* target_log
   t.out_tokens = out_tokens;
   t.accept_len = accept_len;
   if (dfs::launch_verify(t, s) != cudaSuccess) return DFS_ERR_CUDA;
-  if (temperature > 0.f && dfs::launch_resample(t, s) != cudaSuccess) return DFS_ERR_CUDA;
   return DFS_OK;
 }
 
@@ -411,6 +428,7 @@ int dfs_select_verify(const dfs_dims* dims, const void* hidden, const void* W_vo
       cudaSuccess)
     return DFS_ERR_CUDA;
   dfs::TailLaunch t = tail_args(*dims, L, ws);
+  t.G = lists_per_row(*dims, L);
   t.A = A;
   t.Bt = Btab;
   t.x0 = last_verified;
@@ -426,7 +444,6 @@ int dfs_select_verify(const dfs_dims* dims, const void* hidden, const void* W_vo
   t.out_tokens = out_tokens;
   t.accept_len = accept_len;
   if (dfs::launch_tail_fused(t, s) != cudaSuccess) return DFS_ERR_CUDA;
-  if (temperature > 0.f && dfs::launch_resample(t, s) != cudaSuccess) return DFS_ERR_CUDA;
   return DFS_OK;
 }
 

@@ -12,8 +12,8 @@ constexpr int kK = 16;          // candidates kept per draft position
 constexpr int kMaxL = 16;       // longest block handled
 constexpr int kMaxRank = 512;   // widest selector rank handled
 constexpr int kMaxLists = 256;  // partial top-16 lists merged per row
-constexpr int kZChunk = 4096;   // target-logit elements per row-statistics unit
-constexpr int kRChunk = 8192;   // target-logit elements per redraw block
+constexpr int kZChunk = 4096;   // target-logit elements per row-statistics unit and redraw chunk
+constexpr int kMaxZChunks = 1024;  // chunks per target row handled (V <= 4194304)
 
 // ---- a1 (+a2): LM head with fused top-16 (and gate) on the tensor cores ----
 struct LmheadLaunch {
@@ -28,8 +28,11 @@ struct LmheadLaunch {
   int G;               // grid of the vocabulary launch = lists per row
   float* gate_out;     // [rows_total][r]
   int* err;
-  int lmhead_variant;  // 0 = automatic; 1 = two M-tiles x 128 vocab (double-buffered TMEM);
-                       // 2 = two M-tiles x 256 vocab (single-buffered TMEM)
+  int lmhead_variant;  // 0 = automatic; 1 = two M-tiles x 128 vocab, deep W ring;
+                       // 2 = two M-tiles x 256 vocab (single-buffered TMEM);
+                       // 3 = as 1 with a deeper hidden-row ring;
+                       // 4 = row-split pairs (128 rows x 256 columns per CTA, W multicast)
+  int cluster;         // CTAs per cluster sharing hidden-row tiles by multicast (1, 2 or 4)
   // Target-logit row statistics computed by the kernel's spare warps (z_rows = 0: none).
   const void* Z;       // [z_rows, V]
   int zdtype, z_rows, z_nchunk;
@@ -41,6 +44,9 @@ struct LmheadLaunch {
   int zero_count;
 };
 cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s);
+// Whether a call with these rows runs as row-split pairs (then each row gets G / 2 partial
+// lists instead of G).
+bool lmhead_row_split(int rows_total, int variant, int G);
 
 // ---- a1 (+a2) for fp32 inputs, on CUDA cores ----
 struct LmheadSimtLaunch {
@@ -86,7 +92,6 @@ struct TailLaunch {
   const int* zarg;
   const float* zsum;
   int nchunk;                // row-statistics chunks per target row
-  int nrchunk;               // redraw chunks per target row
   float T;                   // 0 = greedy verification
   uint64_t seed;
   int path_mode;
@@ -97,11 +102,7 @@ struct TailLaunch {
   float* path_score;         // [B] or null
   int* out_tokens;           // [B][L]
   int* accept_len;           // [B]
-  int* resample_info;        // [B][4]: row, excluded token, output slot, active
   int* counters;             // [B]
-  float* gumbel_key;         // [B][nrchunk]
-  int* gumbel_idx;
-  int* resample_counters;    // [B]
   int* err;
 };
 // Fused tail for dfs_select_verify: (L-1) x B blocks; the last block of each request
@@ -112,6 +113,5 @@ cudaError_t launch_merge(const TailLaunch& a, cudaStream_t s);    // partial lis
 cudaError_t launch_pair(const TailLaunch& a, cudaStream_t s);     // cand + gate -> S
 cudaError_t launch_path(const TailLaunch& a, cudaStream_t s);     // S -> path
 cudaError_t launch_verify(const TailLaunch& a, cudaStream_t s);   // path + Z stats -> out
-cudaError_t launch_resample(const TailLaunch& a, cudaStream_t s); // T > 0 draws
 
 }  // namespace dfs

@@ -42,4 +42,12 @@ __device__ __forceinline__ float uniform_accept(uint64_t seed, int b, int t) {
   return u01_from_word(c[0]);
 }
 
+// Chunk-choice uniform of the redraw for draft position t of request b: counter
+// (0, t, b, 2), word 0.
+__device__ __forceinline__ float uniform_chunk(uint64_t seed, int b, int t) {
+  uint64_t c[4] = {0ull, static_cast<uint64_t>(t), static_cast<uint64_t>(b), 2ull};
+  philox4x64_10(c, seed, 0ull);
+  return u01_from_word(c[0]);
+}
+
 }  // namespace dfs

@@ -1,6 +1,6 @@
-// select_tail.cu -- everything after the LM head: target-logit row statistics, the
-// merge of partial top-16 lists, bilinear pair scores, greedy / Viterbi paths, greedy
-// and rejection-sampling verification, and the Gumbel-max redraw.
+// select_tail.cu -- everything after the LM head: target-logit row statistics, the merge
+// of partial top-16 lists, bilinear pair scores, greedy / Viterbi paths, greedy and
+// rejection-sampling verification with the redraw.
 //
 // Sources:
 //   "DFlash 2: Keep Drafting Parallel", section "A lightweight path selector":
@@ -12,10 +12,11 @@
 //     equals autoregressive decoding; sampling keeps the target distribution).
 //   Table 1 caption of the blog: the verify length counts the verifier's next token.
 //
-// Memory-bound parts read with 16-byte coalesced loads; the dependent small steps
-// (merge, pair scores, path) run in one block per (request, position), and the last
-// block of a request to finish (an atomic counter, no spinning) selects the path and
-// verifies it.
+// The work here is small and latency-bound, so it is organised around round trips: one
+// block per (request, position) merges, scores and hands its 16 x 16 scores to the last
+// block of its request (an atomic counter, no spinning), which selects the path and
+// verifies it. Every global-to-shared copy issues all of a thread's loads before any
+// store, so a phase costs one memory round trip.
 #include "common.cuh"
 #include "kernels.h"
 #include "philox.cuh"
@@ -49,6 +50,79 @@ __device__ __forceinline__ void load8(const void* base, int is_bf16, size_t idx,
 __device__ __forceinline__ float load1(const void* base, int is_bf16, size_t idx) {
   return is_bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(base)[idx])
                  : static_cast<const float*>(base)[idx];
+}
+
+// A contiguous run of 16-byte chunks to copy from global to shared memory.
+struct Seg {
+  const uint4* src;
+  uint4* dst;
+  int n;
+};
+
+// Chunk j of the concatenated segments: its source and destination (static indexing only,
+// so the segment table stays in registers).
+template <int kNSeg>
+__device__ __forceinline__ void seg_locate(const Seg (&seg)[kNSeg], int j, const uint4*& src,
+                                           uint4*& dst) {
+  src = nullptr;
+  dst = nullptr;
+#pragma unroll
+  for (int q = 0; q < kNSeg; ++q) {
+    if (src == nullptr) {
+      if (j < seg[q].n) {
+        src = seg[q].src + j;
+        dst = seg[q].dst + j;
+      } else {
+        j -= seg[q].n;
+      }
+    }
+  }
+}
+
+// Copies the segments with every thread's loads issued before its stores (one round trip).
+template <int kMaxPer, int kNSeg>
+__device__ __forceinline__ void staged_copy(const Seg (&seg)[kNSeg]) {
+  int total = 0;
+#pragma unroll
+  for (int q = 0; q < kNSeg; ++q) total += seg[q].n;
+  uint4 r[kMaxPer];
+#pragma unroll
+  for (int k = 0; k < kMaxPer; ++k) {
+    const int j = threadIdx.x + k * blockDim.x;
+    if (j < total) {
+      const uint4* src;
+      uint4* dst;
+      seg_locate(seg, j, src, dst);
+      r[k] = __ldcg(src);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kMaxPer; ++k) {
+    const int j = threadIdx.x + k * blockDim.x;
+    if (j < total) {
+      const uint4* src;
+      uint4* dst;
+      seg_locate(seg, j, src, dst);
+      *dst = r[k];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ packed keys
+// (value desc, id asc) as one unsigned 64-bit key: larger key = ranks first.
+__device__ __forceinline__ unsigned long long pack_key(float v, int id) {
+  const uint32_t u = __float_as_uint(v + 0.0f);  // -0 -> +0, so equal values compare equal
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(o) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(id));
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, k, off);
+    k = o > k ? o : k;
+  }
+  return k;
 }
 
 // ------------------------------------------------------------------ target rows
@@ -88,31 +162,32 @@ __global__ void __launch_bounds__(128) k_zreduce(const void* Z, int is_bf16, int
   }
 }
 
-// Merged statistics of one target row, computed by one warp.
+// Merged statistics of one target row, computed by one warp (a lane's chunk loads are
+// issued together).
 __device__ RowStat row_stat_warp(const TailLaunch& a, int row) {
   RowStat st = rowstat_empty();
-  const float inv_T = a.T > 0.f ? 1.0f / a.T : 0.f;
-  for (int c = threadIdx.x & 31; c < a.nchunk; c += 32) {
-    const size_t o = static_cast<size_t>(row) * a.nchunk + c;
-    RowStat v{__ldcg(a.zmax + o), __ldcg(a.zarg + o), a.T > 0.f ? __ldcg(a.zsum + o) : 0.f};
-    st = combine(st, v, inv_T);
+  const bool soft = a.T > 0.f;
+  const float inv_T = soft ? 1.0f / a.T : 0.f;
+  const int lane = threadIdx.x & 31;
+  for (int c0 = 0; c0 < a.nchunk; c0 += 128) {
+    float m[4], s[4];
+    int ix[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int c = c0 + lane + 32 * k;
+      const size_t o = static_cast<size_t>(row) * a.nchunk + c;
+      const bool in = c < a.nchunk;
+      m[k] = in ? __ldcg(a.zmax + o) : -INFINITY;
+      ix[k] = in ? __ldcg(a.zarg + o) : kIntMax;
+      s[k] = (in && soft) ? __ldcg(a.zsum + o) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) st = combine(st, RowStat{m[k], ix[k], s[k]}, inv_T);
   }
   return warp_combine(st, inv_T);
 }
 
 // ------------------------------------------------------------------ top-16 merge
-// Copy the G partial lists (G x 16 values and ids, contiguous) of one row into shared memory.
-__device__ __forceinline__ void stage_lists(const TailLaunch& a, int row, float* sv, int* si) {
-  const size_t base = static_cast<size_t>(row) * a.G * kK;
-  const int n4 = a.G * kK / 4;
-  const float4* pv = reinterpret_cast<const float4*>(a.part_val + base);
-  const int4* pi = reinterpret_cast<const int4*>(a.part_idx + base);
-  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-    reinterpret_cast<float4*>(sv)[i] = __ldcg(pv + i);
-    reinterpret_cast<int4*>(si)[i] = __ldcg(pi + i);
-  }
-}
-
 // One warp merges nl <= 256 sorted lists of 16 into the top 16 (value desc, id asc): a
 // 16-round tournament, lane l watching the heads of lists l, l+32, ...
 __device__ void merge_lists_warp(const float* sv, const int* si, int nl, float* outv, int* outi) {
@@ -137,18 +212,14 @@ __device__ void merge_lists_warp(const float* sv, const int* si, int nl, float* 
         bi = hi[s];
         bs = s;
       }
-    float wv = bv;
-    int wi = bi;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, wv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, wi, off);
-      if (ranks_before(ov, oi, wv, wi)) {
-        wv = ov;
-        wi = oi;
+    const unsigned long long mine = bs >= 0 ? pack_key(bv, bi) : 0ull;
+    const unsigned long long best = warp_max_u64(mine);
+    if (best == 0ull) {  // fewer than 16 orderable candidates (e.g. NaN logits): sentinel
+      if (lane == 0) {
+        outv[k] = -INFINITY;
+        outi[k] = -1;
       }
-    }
-    if (bs >= 0 && bi == wi && bv == wv) {
+    } else if (bs >= 0 && mine == best) {
 #pragma unroll
       for (int s = 0; s < 8; ++s)
         if (s == bs) {
@@ -157,50 +228,72 @@ __device__ void merge_lists_warp(const float* sv, const int* si, int nl, float* 
           hv[s] = head[s] < kK ? sv[l * kK + head[s]] : -INFINITY;
           hi[s] = head[s] < kK ? si[l * kK + head[s]] : kIntMax;
         }
-    }
-    if (lane == 0) {
-      outv[k] = wv;
-      outi[k] = wi;
+      outv[k] = bv;
+      outi[k] = bi;
     }
   }
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ pair scores
-struct PairSmem {
-  float* P;     // [16][r+4]: A(a) (.) g_t
-  float* Q;     // [16][r+4]: B(c)
-  float* g;     // [r]
-};
-
 // S_t(a, c) = U_t(c) + sum_j A(a)_j g_j B(c)_j for the 16 x 16 pairs of one position.
 // prev_tok[a] is the a-th predecessor token (all x0 for position 1); cur_tok/cur_U the
-// position's candidates. Thread (a = tid/16, c = tid%16) returns its score.
-__device__ float pair_scores_block(const TailLaunch& a, const PairSmem& sm, const int* prev_tok,
-                                   const int* cur_tok, const float* cur_U, const float* gate_row) {
+// position's candidates; g (the gate row, shared memory) is already in place. Thread
+// (a = tid/16, c = tid%16) returns its score. P and Q are [16][r+4] fp32 scratch rows.
+__device__ float pair_scores_block(const TailLaunch& a, float* P, float* Q, const float* g,
+                                   const int* prev_tok, const int* cur_tok, const float* cur_U) {
   const int r = a.r, rs = r + 4;
-  for (int j = threadIdx.x; j < r; j += blockDim.x) sm.g[j] = __ldcg(gate_row + j);
-  __syncthreads();
-  const int per_row = r / 8;  // 8-element chunks per table row
-  for (int idx = threadIdx.x; idx < 32 * per_row; idx += blockDim.x) {
-    const int which = idx / per_row, ch = idx % per_row;
-    const bool isP = which < 16;
-    const int slot = isP ? which : which - 16;
-    const int tok = isP ? prev_tok[slot] : cur_tok[slot];
-    float x[8];
-    if (tok >= 0 && tok < a.V) {
-      load8(isP ? a.A : a.Bt, a.dtype == 0, static_cast<size_t>(tok) * r + ch * 8, x);
-    } else {  // an id outside the vocabulary (bad input) scores as a zero embedding
+  const int is_bf16 = a.dtype == 0;
+  const int per_row = r * (is_bf16 ? 2 : 4) / 16;  // 16-byte chunks per table row
+  const int total = 32 * per_row;
+  constexpr int kMaxPer = 16;                      // r <= 512, fp32: 32 * 128 / 256
+  uint4 raw[kMaxPer];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = 0.f;
+  for (int k = 0; k < kMaxPer; ++k) {
+    const int i = threadIdx.x + k * kTailThreads;
+    if (i < total) {
+      const int row = i / per_row, ch = i - row * per_row;
+      const bool isP = row < 16;
+      const int tok = isP ? prev_tok[row] : cur_tok[row - 16];
+      if (tok >= 0 && tok < a.V) {
+        const char* base = static_cast<const char*>(isP ? a.A : a.Bt) +
+                           static_cast<size_t>(tok) * r * (is_bf16 ? 2 : 4);
+        raw[k] = __ldg(reinterpret_cast<const uint4*>(base) + ch);
+      } else {  // an id outside the vocabulary (bad input) scores as a zero embedding
+        raw[k] = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
-    float* dst = (isP ? sm.P : sm.Q) + slot * rs + ch * 8;
+  }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) dst[j] = isP ? x[j] * sm.g[ch * 8 + j] : x[j];
+  for (int k = 0; k < kMaxPer; ++k) {
+    const int i = threadIdx.x + k * kTailThreads;
+    if (i < total) {
+      const int row = i / per_row, ch = i - row * per_row;
+      const bool isP = row < 16;
+      float* dst = (isP ? P + row * rs : Q + (row - 16) * rs);
+      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+      if (is_bf16) {
+        const int e0 = ch * 8;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = bf16_bits_to_float(w[j] & 0xFFFFu), hi = bf16_bits_to_float(w[j] >> 16);
+          dst[e0 + 2 * j] = isP ? lo * g[e0 + 2 * j] : lo;
+          dst[e0 + 2 * j + 1] = isP ? hi * g[e0 + 2 * j + 1] : hi;
+        }
+      } else {
+        const int e0 = ch * 4;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float x = __uint_as_float(w[j]);
+          dst[e0 + j] = isP ? x * g[e0 + j] : x;
+        }
+      }
+    }
   }
   __syncthreads();
   const int ai = threadIdx.x >> 4, ci = threadIdx.x & 15;
-  const float4* pr = reinterpret_cast<const float4*>(sm.P + ai * rs);
-  const float4* qr = reinterpret_cast<const float4*>(sm.Q + ci * rs);
+  const float4* pr = reinterpret_cast<const float4*>(P + ai * rs);
+  const float4* qr = reinterpret_cast<const float4*>(Q + ci * rs);
   float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
   for (int j = 0; j < r / 4; ++j) {
     const float4 p = pr[j], q = qr[j];
@@ -213,10 +306,10 @@ __device__ float pair_scores_block(const TailLaunch& a, const PairSmem& sm, cons
 }
 
 // ------------------------------------------------------------------ path
-// One warp; S [P][16][16] and ids [P][16] in shared memory. Lanes 0..15 hold candidates.
-// Writes path_tok[P] (shared) and returns the path score in lane 0.
+// One warp; S [P][16][16], ids [P][16] and delta [16] in shared memory. Writes
+// path_tok[P] (shared) and returns the path score in every lane.
 __device__ float path_warp(const float* S, const int* ids, int P, int mode, int* path_tok,
-                           unsigned char* bp) {
+                           unsigned char* bp, float* delta) {
   const int lane = threadIdx.x & 31;
   const bool act = lane < kK;
   if (mode == 0) {
@@ -224,60 +317,48 @@ __device__ float path_warp(const float* S, const int* ids, int P, int mode, int*
     int a = 0;
     float total = 0.f;
     for (int p = 0; p < P; ++p) {
-      float v = act ? S[(p * kK + a) * kK + lane] : -INFINITY;
-      int id = act ? ids[p * kK + lane] : kIntMax;
-      int c = lane;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, id, off);
-        const int oc = __shfl_xor_sync(0xffffffffu, c, off);
-        if (ranks_before(ov, oi, v, id)) {
-          v = ov;
-          id = oi;
-          c = oc;
-        }
-      }
-      if (lane == 0) path_tok[p] = id;
-      total += v;
+      const float v = act ? S[(p * kK + a) * kK + lane] : -INFINITY;
+      const unsigned long long key = act ? pack_key(v, ids[p * kK + lane]) : 0ull;
+      const unsigned long long best = warp_max_u64(key);
+      const int c = __ffs(__ballot_sync(0xffffffffu, act && key == best)) - 1;
+      total += __shfl_sync(0xffffffffu, v, c);
+      if (lane == 0) path_tok[p] = ids[p * kK + c];
       a = c;
     }
+    __syncwarp();
     return total;
   }
   // Viterbi: delta_1(c) = S_1(x0, c); delta_t(c) = max_a delta_{t-1}(a) + S_t(a, c)
-  float delta = act ? S[lane] : -INFINITY;
+  if (act) delta[lane] = S[lane];
+  __syncwarp();
   for (int p = 1; p < P; ++p) {
-    float best = -INFINITY;
-    int best_id = kIntMax, best_a = 0;
+    float bv = -INFINITY;
+    int ba = 0;
+    unsigned long long bk = 0ull;
+    if (act) {
 #pragma unroll
-    for (int aa = 0; aa < kK; ++aa) {
-      const float da = __shfl_sync(0xffffffffu, delta, aa);
-      const float v = da + (act ? S[(p * kK + aa) * kK + lane] : 0.f);
-      const int pid = ids[(p - 1) * kK + aa];
-      if (ranks_before(v, pid, best, best_id)) {
-        best = v;
-        best_id = pid;
-        best_a = aa;
+      for (int aa = 0; aa < kK; ++aa) {
+        const float v = delta[aa] + S[(p * kK + aa) * kK + lane];
+        const unsigned long long k = pack_key(v, ids[(p - 1) * kK + aa]);
+        if (k > bk) {
+          bk = k;
+          bv = v;
+          ba = aa;
+        }
       }
     }
-    if (act) bp[p * kK + lane] = static_cast<unsigned char>(best_a);
-    delta = act ? best : -INFINITY;
-  }
-  float v = delta;
-  int id = act ? ids[(P - 1) * kK + lane] : kIntMax;
-  int c = lane;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-    const int oi = __shfl_xor_sync(0xffffffffu, id, off);
-    const int oc = __shfl_xor_sync(0xffffffffu, c, off);
-    if (ranks_before(ov, oi, v, id)) {
-      v = ov;
-      id = oi;
-      c = oc;
+    __syncwarp();
+    if (act) {
+      delta[lane] = bv;
+      bp[p * kK + lane] = static_cast<unsigned char>(ba);
     }
+    __syncwarp();
   }
-  __syncwarp();
+  const float v = act ? delta[lane] : -INFINITY;
+  const unsigned long long key = act ? pack_key(v, ids[(P - 1) * kK + lane]) : 0ull;
+  const unsigned long long best = warp_max_u64(key);
+  const int c = __ffs(__ballot_sync(0xffffffffu, act && key == best)) - 1;
+  const float score = __shfl_sync(0xffffffffu, v, c);
   if (lane == 0) {
     int cur = c;
     for (int p = P - 1; p >= 0; --p) {
@@ -286,88 +367,160 @@ __device__ float path_warp(const float* S, const int* ids, int P, int mode, int*
     }
   }
   __syncwarp();
-  return v;
+  return score;
 }
 
 // ------------------------------------------------------------------ verify
-// Verification of request b given its path (shared memory). Uses every warp of the block
-// for the row statistics, then thread 0 walks the positions.
-__device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, float* rm, float* rl,
-                             int* ry) {
+struct VerifySmem {
+  float rm[kMaxL], rl[kMaxL], zx[kMaxL];
+  int ry[kMaxL];
+  int info[4];
+  float mass[kMaxZChunks];
+  unsigned long long gk[kTailThreads / 32];
+};
+
+// Verification of request b given its path (shared memory), by the whole block: row
+// statistics (one warp per row), the acceptance tests of all positions in parallel (one lane
+// each), then for T > 0 the redraw: a chunk of the row chosen by its residual mass, and the
+// Gumbel-max inside it.
+__device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, VerifySmem& vs) {
   const int L = a.L, P = L - 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool soft = a.T > 0.f;
+  const float inv_T = soft ? 1.0f / a.T : 0.f;
+  const int is_bf16 = a.zdtype == 0;
   for (int i = warp; i < L; i += blockDim.x >> 5) {
     const RowStat st = row_stat_warp(a, b * L + i);
     if (lane == 0) {
-      rm[i] = st.m;
-      ry[i] = st.i;
-      rl[i] = a.T > 0.f ? logf(st.s) : 0.f;
+      vs.rm[i] = st.m;
+      vs.ry[i] = st.i;
+      vs.rl[i] = soft ? logf(st.s) : 0.f;
     }
   }
   __syncthreads();
-  if (threadIdx.x != 0) return;
   int* out = a.out_tokens + static_cast<size_t>(b) * L;
-  if (!(a.T > 0.f)) {
-    int n = 0;
-    while (n < P && path_tok[n] == ry[n]) ++n;
-    for (int i = 0; i < L; ++i) out[i] = i < n ? path_tok[i] : (i == n ? ry[n] : -1);
-    a.accept_len[b] = n + 1;
-    return;
-  }
-  const float inv_T = 1.0f / a.T;
-  int* info = a.resample_info + static_cast<size_t>(b) * 4;
-  for (int i = 0; i < L; ++i) out[i] = -1;
-  for (int t = 1; t <= P; ++t) {
-    const int x = path_tok[t - 1];
-    const bool in_vocab = x >= 0 && x < a.V;  // an out-of-vocabulary proposal has p = 0
-    const float z = in_vocab
-        ? load1(a.Z, a.zdtype == 0, (static_cast<size_t>(b) * L + (t - 1)) * a.V + x) : -INFINITY;
-    const float p = expf((z - rm[t - 1]) * inv_T - rl[t - 1]);
-    const float u = uniform_accept(a.seed, b, t);
-    if (u < p) {
-      out[t - 1] = x;
-      continue;
+  if (warp == 0) {
+    bool ok = false;
+    if (lane < P) {
+      const int x = path_tok[lane];  // the proposal for position lane + 1, verified by row lane
+      if (!soft) {
+        ok = x == vs.ry[lane];
+      } else {
+        const bool in_vocab = x >= 0 && x < a.V;  // an out-of-vocabulary proposal has p = 0
+        const float z = in_vocab ? load1(a.Z, is_bf16, (static_cast<size_t>(b) * L + lane) * a.V + x)
+                                 : -INFINITY;
+        vs.zx[lane] = z;
+        const float p = expf((z - vs.rm[lane]) * inv_T - vs.rl[lane]);
+        ok = uniform_accept(a.seed, b, lane + 1) < p;
+      }
     }
-    info[0] = t - 1;  // row redrawn from
-    info[1] = x;      // token removed from it
-    info[2] = t - 1;  // output slot
-    info[3] = 1;
-    a.accept_len[b] = t;
-    return;
+    const unsigned fail = __ballot_sync(0xffffffffu, lane < P && !ok);
+    const int n = fail ? __ffs(fail) - 1 : P;  // accepted drafts
+    if (lane < L && (lane != n || !soft))
+      out[lane] = lane < n ? path_tok[lane] : (lane == n ? vs.ry[n] : -1);
+    if (lane == 0) {
+      a.accept_len[b] = n + 1;
+      vs.info[0] = n;
+    }
   }
-  info[0] = P;
-  info[1] = -1;
-  info[2] = P;
-  info[3] = 1;
-  a.accept_len[b] = L;
+  if (!soft) return;
+  __syncthreads();
+  // redraw from row n (the rejected position's row, or the bonus row L-1 when n = P), with
+  // the rejected proposal removed; the draw's counter position is n + 1
+  const int n = vs.info[0];
+  const int excl = n < P ? path_tok[n] : -1;
+  const size_t grow = static_cast<size_t>(b) * L + n;
+  if (warp == 0) {
+    const float M = vs.rm[n];
+    const bool ex_in = excl >= 0 && excl < a.V;
+    const float ex_mass = ex_in ? expf((vs.zx[n] - M) * inv_T) : 0.f;
+    for (int c = lane; c < a.nchunk; c += 32) {
+      const size_t o = grow * a.nchunk + c;
+      float m = __ldcg(a.zsum + o) * expf((__ldcg(a.zmax + o) - M) * inv_T);
+      if (ex_in && c == excl / kZChunk) m = fmaxf(m - ex_mass, 0.f);
+      vs.mass[c] = m;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      float total = 0.f;
+      for (int c = 0; c < a.nchunk; ++c) total += vs.mass[c];
+      const float target = uniform_chunk(a.seed, b, n + 1) * total;
+      int pick = -1, last_nonzero = 0;
+      float cum = 0.f;
+      for (int c = 0; c < a.nchunk; ++c) {
+        cum += vs.mass[c];
+        if (vs.mass[c] > 0.f) last_nonzero = c;
+        if (pick < 0 && cum > target) pick = c;
+      }
+      vs.info[1] = pick < 0 ? last_nonzero : pick;
+    }
+  }
+  __syncthreads();
+  const int lo = vs.info[1] * kZChunk;
+  const int hi = min(a.V, lo + kZChunk);
+  const int v0 = lo + threadIdx.x * 16;  // kZChunk = 16 tokens x 256 threads
+  unsigned long long best = 0ull;
+  if (v0 < hi) {
+    float x[2][8];
+    load8(a.Z, is_bf16, grow * a.V + v0, x[0]);
+    if (v0 + 8 < hi) load8(a.Z, is_bf16, grow * a.V + v0 + 8, x[1]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int vq = v0 + 4 * q;
+      if (vq >= hi) break;
+      uint64_t c[4] = {static_cast<uint64_t>(vq >> 2), static_cast<uint64_t>(n + 1),
+                       static_cast<uint64_t>(b), 1ull};
+      philox4x64_10(c, a.seed, 0ull);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int v = vq + w;
+        if (v == excl) continue;
+        const float key = x[q >> 1][(q & 1) * 4 + w] * inv_T - logf(-logf(u01_from_word(c[w])));
+        const unsigned long long k = pack_key(key, v);
+        best = k > best ? k : best;
+      }
+    }
+  }
+  best = warp_max_u64(best);
+  if (lane == 0) vs.gk[warp] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long f = 0ull;
+    for (int w = 0; w < kTailThreads / 32; ++w) f = vs.gk[w] > f ? vs.gk[w] : f;
+    out[n] = static_cast<int>(~static_cast<uint32_t>(f & 0xffffffffu));
+  }
 }
 
 // ------------------------------------------------------------------ shared memory plan
 struct TailSmem {
   float* lv_cur; int* li_cur;    // staged partial lists of position t   [G*16]
   float* lv_prev; int* li_prev;  // staged partial lists of position t-1 [G*16]
+  float* g;                      // gate row [r]
   float* cand_U; int* cand_id;   // merged candidates of t   [16]
   float* prev_U; int* prev_id;   // merged candidates of t-1 [16]
   int* prev_tok;                 // predecessor tokens [16]
-  PairSmem pair;
+  float* P; float* Q;            // [16][r+4]
   float* S_all; int* ids_all;    // last block: [P][16][16], [P][16]
   unsigned char* bp;             // [16][16]
+  float* delta;                  // [16]
   int* path_tok;                 // [16]
-  float* rm; float* rl; int* ry; // [16] row statistics
   int* flag;
+  VerifySmem* vs;
 };
 
-__host__ __device__ inline size_t tail_smem_bytes(int G, int r, bool lists2) {
+__host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
   size_t n = 0;
-  n += static_cast<size_t>(G) * kK * 8 * (lists2 ? 2 : 1);
-  n += 16 * 4 * 5;
-  n += 2 * 16 * static_cast<size_t>(r + 4) * 4 + static_cast<size_t>(r) * 4;
-  n += static_cast<size_t>(kMaxL) * kK * kK * 4 + kMaxL * kK * 4;
-  n += kMaxL * kK + 16 * 4 * 4 + 64;
+  n += 4 * (static_cast<size_t>(G) * kK * 4 + 16);
+  n += static_cast<size_t>(r) * 4 + 16;
+  n += 5 * 80;
+  n += 2 * (16 * static_cast<size_t>(r + 4) * 4 + 16);
+  n += static_cast<size_t>(kMaxL) * kK * kK * 4 + kMaxL * kK * 4 + 32;
+  n += kMaxL * kK + 16 + 80 + 80 + 16;
+  n += sizeof(VerifySmem) + 16;
   return n + 256;
 }
 
-__device__ TailSmem carve(uint8_t* base, int G, int r, bool lists2) {
+__device__ TailSmem carve(uint8_t* base, int G, int r) {
   TailSmem s;
   uint8_t* p = base;
   auto take = [&](size_t bytes) {
@@ -378,48 +531,44 @@ __device__ TailSmem carve(uint8_t* base, int G, int r, bool lists2) {
   const size_t lb = static_cast<size_t>(G) * kK * 4;
   s.lv_cur = reinterpret_cast<float*>(take(lb));
   s.li_cur = reinterpret_cast<int*>(take(lb));
-  if (lists2) {
-    s.lv_prev = reinterpret_cast<float*>(take(lb));
-    s.li_prev = reinterpret_cast<int*>(take(lb));
-  } else {
-    s.lv_prev = nullptr;
-    s.li_prev = nullptr;
-  }
+  s.lv_prev = reinterpret_cast<float*>(take(lb));
+  s.li_prev = reinterpret_cast<int*>(take(lb));
+  s.g = reinterpret_cast<float*>(take(static_cast<size_t>(r) * 4));
   s.cand_U = reinterpret_cast<float*>(take(64));
   s.cand_id = reinterpret_cast<int*>(take(64));
   s.prev_U = reinterpret_cast<float*>(take(64));
   s.prev_id = reinterpret_cast<int*>(take(64));
   s.prev_tok = reinterpret_cast<int*>(take(64));
-  s.pair.P = reinterpret_cast<float*>(take(16 * static_cast<size_t>(r + 4) * 4));
-  s.pair.Q = reinterpret_cast<float*>(take(16 * static_cast<size_t>(r + 4) * 4));
-  s.pair.g = reinterpret_cast<float*>(take(static_cast<size_t>(r) * 4));
+  s.P = reinterpret_cast<float*>(take(16 * static_cast<size_t>(r + 4) * 4));
+  s.Q = reinterpret_cast<float*>(take(16 * static_cast<size_t>(r + 4) * 4));
   s.S_all = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * kK * 4));
   s.ids_all = reinterpret_cast<int*>(take(kMaxL * kK * 4));
   s.bp = take(kMaxL * kK);
+  s.delta = reinterpret_cast<float*>(take(64));
   s.path_tok = reinterpret_cast<int*>(take(64));
-  s.rm = reinterpret_cast<float*>(take(64));
-  s.rl = reinterpret_cast<float*>(take(64));
-  s.ry = reinterpret_cast<int*>(take(64));
   s.flag = reinterpret_cast<int*>(take(16));
+  s.vs = reinterpret_cast<VerifySmem*>(take(sizeof(VerifySmem)));
   return s;
 }
 
-// Path and verification of request b, run by the block that completes it. S and the
-// candidates of every position are read back from global memory.
+// Path and verification of request b, run by the block that completes it. The scores and
+// candidates of every position are read back from global memory in one round trip.
 __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
   const int P = a.L - 1;
-  const float* Sg = a.S + static_cast<size_t>(b) * P * kK * kK;
-  const int* Ig = a.cand_ids + static_cast<size_t>(b) * P * kK;
-  for (int i = threadIdx.x; i < P * kK * kK; i += blockDim.x) sm.S_all[i] = __ldcg(Sg + i);
-  for (int i = threadIdx.x; i < P * kK; i += blockDim.x) sm.ids_all[i] = __ldcg(Ig + i);
+  const Seg seg[2] = {
+      {reinterpret_cast<const uint4*>(a.S + static_cast<size_t>(b) * P * kK * kK),
+       reinterpret_cast<uint4*>(sm.S_all), P * kK * kK / 4},
+      {reinterpret_cast<const uint4*>(a.cand_ids + static_cast<size_t>(b) * P * kK),
+       reinterpret_cast<uint4*>(sm.ids_all), P * kK / 4}};
+  staged_copy<5, 2>(seg);
   __syncthreads();
   if (threadIdx.x < 32) {
-    const float score = path_warp(sm.S_all, sm.ids_all, P, a.path_mode, sm.path_tok, sm.bp);
+    const float score = path_warp(sm.S_all, sm.ids_all, P, a.path_mode, sm.path_tok, sm.bp, sm.delta);
+    if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
     if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < P; i += blockDim.x) a.path[static_cast<size_t>(b) * P + i] = sm.path_tok[i];
-  verify_block(a, b, sm.path_tok, sm.rm, sm.rl, sm.ry);
+  verify_block(a, b, sm.path_tok, *sm.vs);
 }
 
 // ------------------------------------------------------------------ kernels
@@ -427,13 +576,22 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
 // 16 x 16 pairs of position t, and the last block of request b runs path + verification.
 __global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_constant__ TailLaunch a) {
   extern __shared__ __align__(16) uint8_t tail_smem[];
-  grid_dependents_launch();  // a following redraw kernel may take free SMs and wait there
-  grid_dependency_wait();    // the LM-head kernel's results (launched as its dependent)
+  grid_dependency_wait();  // the LM-head kernel's results (launched as its dependent)
   const int t = blockIdx.x + 1, b = blockIdx.y, L = a.L, P = L - 1;
-  TailSmem sm = carve(tail_smem, a.G, a.r, true);
+  TailSmem sm = carve(tail_smem, a.G, a.r);
   const int warp = threadIdx.x >> 5;
-  stage_lists(a, b * L + t, sm.lv_cur, sm.li_cur);
-  if (t >= 2) stage_lists(a, b * L + t - 1, sm.lv_prev, sm.li_prev);
+  const size_t lst = static_cast<size_t>(a.G) * kK;
+  const size_t rc = static_cast<size_t>(b) * L + t;
+  const int n4 = a.G * kK / 4;
+  const Seg seg[5] = {
+      {reinterpret_cast<const uint4*>(a.gate + rc * a.r), reinterpret_cast<uint4*>(sm.g), a.r / 4},
+      {reinterpret_cast<const uint4*>(a.part_val + rc * lst), reinterpret_cast<uint4*>(sm.lv_cur), n4},
+      {reinterpret_cast<const uint4*>(a.part_idx + rc * lst), reinterpret_cast<uint4*>(sm.li_cur), n4},
+      {reinterpret_cast<const uint4*>(a.part_val + (rc - 1) * lst), reinterpret_cast<uint4*>(sm.lv_prev),
+       t >= 2 ? n4 : 0},
+      {reinterpret_cast<const uint4*>(a.part_idx + (rc - 1) * lst), reinterpret_cast<uint4*>(sm.li_prev),
+       t >= 2 ? n4 : 0}};
+  staged_copy<17, 5>(seg);  // G <= 256, r <= 512: 4 * 1024 + 128 chunks over 256 threads
   __syncthreads();
   if (warp == 0) merge_lists_warp(sm.lv_cur, sm.li_cur, a.G, sm.cand_U, sm.cand_id);
   if (warp == 1 && t >= 2) merge_lists_warp(sm.lv_prev, sm.li_prev, a.G, sm.prev_U, sm.prev_id);
@@ -445,8 +603,7 @@ __global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_consta
     a.cand_U[o] = sm.cand_U[threadIdx.x];
   }
   __syncthreads();
-  const float s = pair_scores_block(a, sm.pair, sm.prev_tok, sm.cand_id, sm.cand_U,
-                                    a.gate + static_cast<size_t>(b * L + t) * a.r);
+  const float s = pair_scores_block(a, sm.P, sm.Q, sm.g, sm.prev_tok, sm.cand_id, sm.cand_U);
   a.S[(static_cast<size_t>(b) * P + (t - 1)) * kK * kK + threadIdx.x] = s;
   __threadfence();
   __syncthreads();
@@ -462,8 +619,13 @@ __global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_consta
 __global__ void __launch_bounds__(kTailThreads) k_merge(const __grid_constant__ TailLaunch a) {
   extern __shared__ __align__(16) uint8_t tail_smem[];
   const int t = blockIdx.x + 1, b = blockIdx.y, P = a.L - 1;
-  TailSmem sm = carve(tail_smem, a.G, a.r, false);
-  stage_lists(a, b * a.L + t, sm.lv_cur, sm.li_cur);
+  TailSmem sm = carve(tail_smem, a.G, a.r);
+  const size_t lst = static_cast<size_t>(a.G) * kK;
+  const size_t rc = static_cast<size_t>(b) * a.L + t;
+  const Seg seg[2] = {
+      {reinterpret_cast<const uint4*>(a.part_val + rc * lst), reinterpret_cast<uint4*>(sm.lv_cur), a.G * kK / 4},
+      {reinterpret_cast<const uint4*>(a.part_idx + rc * lst), reinterpret_cast<uint4*>(sm.li_cur), a.G * kK / 4}};
+  staged_copy<8, 2>(seg);
   __syncthreads();
   if (threadIdx.x < 32) merge_lists_warp(sm.lv_cur, sm.li_cur, a.G, sm.cand_U, sm.cand_id);
   __syncthreads();
@@ -478,7 +640,10 @@ __global__ void __launch_bounds__(kTailThreads) k_merge(const __grid_constant__ 
 __global__ void __launch_bounds__(kTailThreads) k_pair(const __grid_constant__ TailLaunch a) {
   extern __shared__ __align__(16) uint8_t tail_smem[];
   const int t = blockIdx.x + 1, b = blockIdx.y, L = a.L, P = L - 1;
-  TailSmem sm = carve(tail_smem, 1, a.r, false);
+  TailSmem sm = carve(tail_smem, 1, a.r);
+  const Seg seg[1] = {{reinterpret_cast<const uint4*>(a.gate + (static_cast<size_t>(b) * L + t) * a.r),
+                       reinterpret_cast<uint4*>(sm.g), a.r / 4}};
+  staged_copy<1, 1>(seg);
   if (threadIdx.x < kK) {
     const size_t o = (static_cast<size_t>(b) * P + (t - 1)) * kK + threadIdx.x;
     sm.cand_id[threadIdx.x] = a.cand_ids[o];
@@ -486,119 +651,39 @@ __global__ void __launch_bounds__(kTailThreads) k_pair(const __grid_constant__ T
     sm.prev_tok[threadIdx.x] = t >= 2 ? a.cand_ids[o - kK] : a.x0[b];
   }
   __syncthreads();
-  const float s = pair_scores_block(a, sm.pair, sm.prev_tok, sm.cand_id, sm.cand_U,
-                                    a.gate + static_cast<size_t>(b * L + t) * a.r);
+  const float s = pair_scores_block(a, sm.P, sm.Q, sm.g, sm.prev_tok, sm.cand_id, sm.cand_U);
   a.S[(static_cast<size_t>(b) * P + (t - 1)) * kK * kK + threadIdx.x] = s;
 }
 
-// dfs_path_select: one warp per request.
-__global__ void __launch_bounds__(32) k_path(const __grid_constant__ TailLaunch a) {
-  __shared__ float S_all[kMaxL * kK * kK];
-  __shared__ int ids_all[kMaxL * kK];
+// dfs_path_select: one block per request; four warps stage the scores, one selects.
+__global__ void __launch_bounds__(128) k_path(const __grid_constant__ TailLaunch a) {
+  __shared__ __align__(16) float S_all[kMaxL * kK * kK];
+  __shared__ __align__(16) int ids_all[kMaxL * kK];
   __shared__ unsigned char bp[kMaxL * kK];
+  __shared__ float delta[kK];
   __shared__ int path_tok[kMaxL];
   const int b = blockIdx.x, P = a.L - 1;
-  const float* Sg = a.S + static_cast<size_t>(b) * P * kK * kK;
-  const int* Ig = a.cand_ids + static_cast<size_t>(b) * P * kK;
-  for (int i = threadIdx.x; i < P * kK * kK; i += 32) S_all[i] = Sg[i];
-  for (int i = threadIdx.x; i < P * kK; i += 32) ids_all[i] = Ig[i];
-  __syncwarp();
-  const float score = path_warp(S_all, ids_all, P, a.path_mode, path_tok, bp);
-  __syncwarp();
-  for (int i = threadIdx.x; i < P; i += 32) a.path[static_cast<size_t>(b) * P + i] = path_tok[i];
+  const Seg seg[2] = {
+      {reinterpret_cast<const uint4*>(a.S + static_cast<size_t>(b) * P * kK * kK),
+       reinterpret_cast<uint4*>(S_all), P * kK * kK / 4},
+      {reinterpret_cast<const uint4*>(a.cand_ids + static_cast<size_t>(b) * P * kK),
+       reinterpret_cast<uint4*>(ids_all), P * kK / 4}};
+  staged_copy<8, 2>(seg);  // up to 15 * 68 chunks over 128 threads
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const float score = path_warp(S_all, ids_all, P, a.path_mode, path_tok, bp, delta);
+  if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = path_tok[threadIdx.x];
   if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
 }
 
 // dfs_verify: one block per request, given its path.
 __global__ void __launch_bounds__(kTailThreads) k_verify(const __grid_constant__ TailLaunch a) {
   __shared__ int path_tok[kMaxL];
-  __shared__ float rm[kMaxL], rl[kMaxL];
-  __shared__ int ry[kMaxL];
+  __shared__ VerifySmem vs;
   const int b = blockIdx.x, P = a.L - 1;
-  for (int i = threadIdx.x; i < P; i += blockDim.x) path_tok[i] = a.path[static_cast<size_t>(b) * P + i];
+  if (threadIdx.x < P) path_tok[threadIdx.x] = a.path[static_cast<size_t>(b) * P + threadIdx.x];
   __syncthreads();
-  verify_block(a, b, path_tok, rm, rl, ry);
-}
-
-// Gumbel-max redraw for T > 0: block (chunk, b) scans kRChunk tokens of the row named in
-// resample_info[b]; the last block of the request merges the per-chunk winners.
-__global__ void __launch_bounds__(256) k_resample(const __grid_constant__ TailLaunch a) {
-  grid_dependency_wait();  // the verification kernel's redraw requests
-  const int b = blockIdx.y, chunk = blockIdx.x, L = a.L;
-  const int* info = a.resample_info + static_cast<size_t>(b) * 4;
-  const int row = __ldcg(info), excl = __ldcg(info + 1), slot = __ldcg(info + 2);
-  const float inv_T = 1.0f / a.T;
-  const size_t rbase = (static_cast<size_t>(b) * L + row) * a.V;
-  float bk = -INFINITY;
-  int bi = kIntMax;
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    const int v0 = chunk * kRChunk + g * 2048 + threadIdx.x * 8;
-    if (v0 >= a.V) continue;
-    float x[8];
-    load8(a.Z, a.zdtype == 0, rbase + v0, x);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int vq = v0 + 4 * h;
-      uint64_t c[4] = {static_cast<uint64_t>(vq >> 2), static_cast<uint64_t>(row + 1),
-                       static_cast<uint64_t>(b), 1ull};
-      philox4x64_10(c, a.seed, 0ull);
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const int v = vq + w;
-        const float gmb = -logf(-logf(u01_from_word(c[w])));
-        const float key = x[4 * h + w] * inv_T + gmb;
-        if (v != excl && key > bk) {  // v increases within the thread
-          bk = key;
-          bi = v;
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-    if (ranks_before(ok, oi, bk, bi)) {
-      bk = ok;
-      bi = oi;
-    }
-  }
-  __shared__ float sk[8];
-  __shared__ int si[8];
-  __shared__ int last;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    sk[warp] = bk;
-    si[warp] = bi;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < 8; ++w)
-      if (ranks_before(sk[w], si[w], bk, bi)) {
-        bk = sk[w];
-        bi = si[w];
-      }
-    a.gumbel_key[static_cast<size_t>(b) * a.nrchunk + chunk] = bk;
-    a.gumbel_idx[static_cast<size_t>(b) * a.nrchunk + chunk] = bi;
-    __threadfence();
-    last = (atomicAdd(a.resample_counters + b, 1) == a.nrchunk - 1);
-  }
-  __syncthreads();
-  if (!last || threadIdx.x != 0) return;
-  __threadfence();
-  float fk = -INFINITY;
-  int fi = kIntMax;
-  for (int c = 0; c < a.nrchunk; ++c) {
-    const float k = __ldcg(a.gumbel_key + static_cast<size_t>(b) * a.nrchunk + c);
-    const int i = __ldcg(a.gumbel_idx + static_cast<size_t>(b) * a.nrchunk + c);
-    if (ranks_before(k, i, fk, fi)) {
-      fk = k;
-      fi = i;
-    }
-  }
-  a.out_tokens[static_cast<size_t>(b) * L + slot] = fi;
-  a.resample_counters[b] = 0;
+  verify_block(a, b, path_tok, vs);
 }
 
 // Launch as a programmatic dependent of the previous kernel on the stream: the launch is
@@ -640,14 +725,14 @@ cudaError_t launch_zreduce(const ZReduceLaunch& a, cudaStream_t s) {
 }
 
 cudaError_t launch_tail_fused(const TailLaunch& a, cudaStream_t s) {
-  const size_t bytes = tail_smem_bytes(a.G, a.r, true);
+  const size_t bytes = tail_smem_bytes(a.G, a.r);
   cudaError_t e = set_smem(k_tail_fused, bytes);
   if (e != cudaSuccess) return e;
   return launch_dependent(k_tail_fused, dim3(a.L - 1, a.B), dim3(kTailThreads), bytes, s, a);
 }
 
 cudaError_t launch_merge(const TailLaunch& a, cudaStream_t s) {
-  const size_t bytes = tail_smem_bytes(a.G, a.r, false);
+  const size_t bytes = tail_smem_bytes(a.G, a.r);
   cudaError_t e = set_smem(k_merge, bytes);
   if (e != cudaSuccess) return e;
   k_merge<<<dim3(a.L - 1, a.B), kTailThreads, bytes, s>>>(a);
@@ -655,7 +740,7 @@ cudaError_t launch_merge(const TailLaunch& a, cudaStream_t s) {
 }
 
 cudaError_t launch_pair(const TailLaunch& a, cudaStream_t s) {
-  const size_t bytes = tail_smem_bytes(1, a.r, false);
+  const size_t bytes = tail_smem_bytes(1, a.r);
   cudaError_t e = set_smem(k_pair, bytes);
   if (e != cudaSuccess) return e;
   k_pair<<<dim3(a.L - 1, a.B), kTailThreads, bytes, s>>>(a);
@@ -663,17 +748,13 @@ cudaError_t launch_pair(const TailLaunch& a, cudaStream_t s) {
 }
 
 cudaError_t launch_path(const TailLaunch& a, cudaStream_t s) {
-  k_path<<<a.B, 32, 0, s>>>(a);
+  k_path<<<a.B, 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_verify(const TailLaunch& a, cudaStream_t s) {
   k_verify<<<a.B, kTailThreads, 0, s>>>(a);
   return cudaGetLastError();
-}
-
-cudaError_t launch_resample(const TailLaunch& a, cudaStream_t s) {
-  return launch_dependent(k_resample, dim3(a.nrchunk, a.B), dim3(256), 0, s, a);
 }
 
 }  // namespace dfs

@@ -1,6 +1,6 @@
 // verify_noalloc.cu -- dfs_verify_noalloc: the verification step (target-row statistics,
-// greedy or rejection-sampling acceptance, redraw) with its scratch memory built into the
-// library instead of passed in by the caller.
+// then greedy or rejection-sampling acceptance with the redraw) with its scratch memory
+// built into the library instead of passed in by the caller.
 //
 // It exists for callers that cannot allocate device memory at the point where they verify:
 // code running inside a serving loop whose memory pool is owned by another component,
@@ -63,18 +63,15 @@ extern "C" int dfs_verify_noalloc(const dfs_dims* d, const int32_t* path,
   if (d->B < 1 || d->L < 2 || d->V < 1) return DFS_ERR_INVALID;
   if (!(temperature >= 0.f)) return DFS_ERR_INVALID;
   if (d->K != dfs::kK || d->L > dfs::kMaxL || d->V < dfs::kK || d->V % 8 != 0 ||
-      (d->zdtype != DFS_BF16 && d->zdtype != DFS_FP32))
+      d->V > dfs::kMaxZChunks * dfs::kZChunk || (d->zdtype != DFS_BF16 && d->zdtype != DFS_FP32))
     return DFS_ERR_UNSUPPORTED;
 
   const size_t B = static_cast<size_t>(d->B);
   const size_t rows = B * static_cast<size_t>(d->L);
   const int nchunk = (d->V + dfs::kZChunk - 1) / dfs::kZChunk;
-  const int nrchunk = (d->V + dfs::kRChunk - 1) / dfs::kRChunk;
-  // Layout inside the array: the two counter arrays first (cleared together each call).
+  // Layout inside the array: the counters first (cleared by the first kernel of each call).
   size_t off = 0;
   const size_t o_cnt = off;
-  off = up(off + 4 * B);
-  const size_t o_rcnt = off;
   off = up(off + 4 * B);
   const size_t zero_end = off;
   const size_t o_zmax = off;
@@ -83,12 +80,6 @@ extern "C" int dfs_verify_noalloc(const dfs_dims* d, const int32_t* path,
   off = up(off + 4 * rows * nchunk);
   const size_t o_zsum = off;
   off = up(off + 4 * rows * nchunk);
-  const size_t o_info = off;
-  off = up(off + 16 * B);
-  const size_t o_gkey = off;
-  off = up(off + 4 * B * nrchunk);
-  const size_t o_gidx = off;
-  off = up(off + 4 * B * nrchunk);
   const size_t o_err = off;
   off = up(off + 16);
   if (off > kScratchBytes) return DFS_ERR_WORKSPACE;  // the built-in scratch is too small
@@ -121,19 +112,13 @@ extern "C" int dfs_verify_noalloc(const dfs_dims* d, const int32_t* path,
   t.zarg = z.zarg;
   t.zsum = z.zsum;
   t.nchunk = nchunk;
-  t.nrchunk = nrchunk;
   t.T = temperature;
   t.seed = seed;
   t.path = const_cast<int*>(path);
   t.out_tokens = out_tokens;
   t.accept_len = accept_len;
-  t.resample_info = reinterpret_cast<int*>(base + o_info);
   t.counters = reinterpret_cast<int*>(base + o_cnt);
-  t.gumbel_key = reinterpret_cast<float*>(base + o_gkey);
-  t.gumbel_idx = reinterpret_cast<int*>(base + o_gidx);
-  t.resample_counters = reinterpret_cast<int*>(base + o_rcnt);
   t.err = reinterpret_cast<int*>(base + o_err);
   if (dfs::launch_verify(t, s) != cudaSuccess) return DFS_ERR_CUDA;
-  if (temperature > 0.f && dfs::launch_resample(t, s) != cudaSuccess) return DFS_ERR_CUDA;
   return DFS_OK;
 }

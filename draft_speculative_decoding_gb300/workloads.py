@@ -81,9 +81,10 @@ LONG_BLOCK = WorkloadSpec("long_block_B16_L16_V151936_d4096", B=16, L=16, V=1519
                           r=256, seed=4, agreement=("top1_linear", 0.85, 0.55),
                           path_modes=("viterbi", "greedy"), temperatures=(0.0, 1.0))
 
-# The throughput workload with a 32768-token vocabulary: the same per-tile work, W_vocab
-# (335 MB) still larger than L2, small enough for multi-pass profiler captures.
-THROUGHPUT_PROFILE = THROUGHPUT.with_(name="throughput_B32_L8_V32768_d5120_zipf", V=32768)
+# The throughput workload with a 65536-token vocabulary: the same per-tile work and several
+# tiles per SM, W_vocab (671 MB) still five times L2, small enough for multi-pass profiler
+# captures.
+THROUGHPUT_PROFILE = THROUGHPUT.with_(name="throughput_B32_L8_V65536_d5120_zipf", V=65536)
 
 WORKLOADS = {w.name: w for w in (TINY, SINGLE, SMALL_BATCH, THROUGHPUT, LONG_BLOCK,
                                  THROUGHPUT_PROFILE)}

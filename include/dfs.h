@@ -70,7 +70,7 @@ typedef struct {
   int B;      /* requests in the batch, >= 1                                 */
   int L;      /* block length incl. the verified slot, 2..16                 */
   int K;      /* candidates kept per position; must be 16                    */
-  int V;      /* vocabulary size, >= K; multiple of 8                        */
+  int V;      /* vocabulary size, >= K, <= 4194304; multiple of 8            */
   int d;      /* drafter hidden width; multiple of 64 for BF16               */
   int r;      /* selector rank (A/B table width, gate width); multiple of 8, <= 512 */
   int dtype;  /* dfs_dtype of hidden, W_vocab, W_g, A, Btab                  */
@@ -149,8 +149,11 @@ int dfs_path_select(const dfs_dims* dims, const float* S, const int32_t* cand_id
  *     at the first rejection the emitted token is a draw from p_{t-1} with x_t removed
  *     and renormalised; after L-1 acceptances a bonus token is drawn from p_{L-1}.
  *     Draws: Philox4x64-10 (Salmon et al., SC'11), key (seed, 0); the accept test of
- *     position t uses counter (0, t, b, 0) word 0; the draw from row t-1 (t = L for the
- *     bonus row) uses Gumbel-max over v with counter (v>>2, t, b, 1) word v&3;
+ *     position t uses counter (0, t, b, 0) word 0. The draw from row t-1 (t = L for the
+ *     bonus row) is exact in two stages: a chunk of 4096 consecutive tokens is chosen
+ *     with probability proportional to its residual mass (one uniform, counter
+ *     (0, t, b, 2) word 0, against the cumulative masses in vocabulary order), then the
+ *     Gumbel-max over that chunk, with counter (v>>2, t, b, 1) word v&3 for token v;
  *     U = ((word >> 41) + 0.5) * 2^-23 (exact in fp32).
  *   out_tokens [B, L] int32 out: the emitted tokens, then -1
  *   accept_len [B] int32 out: tokens emitted, 1..L (includes the verifier's token) */
@@ -165,8 +168,8 @@ int dfs_verify(const dfs_dims* dims, const int32_t* path, const void* target_log
  * dfs_verify with identical results, and no allocation happens in it.
  *   Scratch: a 4 MiB device array built into the library, held by every GPU that loads the
  *   library until the process exits. The call returns DFS_ERR_WORKSPACE when the shape
- *   needs more, roughly when 12 * B * L * ceil(V / 4096) + B * (24 + 8 * ceil(V / 8192))
- *   bytes exceed 4 MiB (B * L up to about 9000 at V = 151936).
+ *   needs more, roughly when 12 * B * L * ceil(V / 4096) + 4 * B bytes exceed 4 MiB
+ *   (B * L up to about 9000 at V = 151936).
  *   Set-up: the first call on each device asks the runtime for the array's device address,
  *   with that device current; make that first call before any stream capture.
  *   Sharing: all calls use the one array, which keeps the last call's contents; each call
