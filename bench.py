@@ -180,18 +180,20 @@ def run_ours(args):
             ev[1].record(stream)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        n0 = binding.dfs_launch_count()
         e0.record(stream)
         for i in range(K):
             if trace:
                 binding.dfs_set_trace_events(*tr[i])
             step(W + i, T)
         e1.record(stream)
+        n1 = binding.dfs_launch_count()
         torch.cuda.synchronize()
         binding.dfs_set_trace_events(None, None)
         replicas.barrier()
         ms = e0.elapsed_time(e1) / K
         lm = statistics.mean(a.elapsed_time(b) for a, b in tr) if trace else None
-        return ms, lm
+        return ms, lm, n1 - n0
 
     uuid = None
     try:
@@ -200,14 +202,14 @@ def run_ours(args):
     except Exception:
         uuid = None
     clocks = ClockSampler(uuid)
-    ms_greedy, _ = timed(0.0, args.steps, args.warmup)
+    ms_greedy, _, launches = timed(0.0, args.steps, args.warmup)
     clk = clocks.stop()
     # the dominant kernel's own duration, from events recorded around it on its stream (a
     # separate pass: an event between two kernels stops the second launching early)
-    _, lm_ms = timed(0.0, args.steps, 1, trace=True)
+    _, lm_ms, _ = timed(0.0, args.steps, 1, trace=True)
     assert binding.dfs_get_device_error(ws) == binding.DFS_OK
     accept = outs[2].float().mean().item()
-    ms_samp, _ = timed(args.sampling_temperature, max(10, args.steps // 2), args.warmup)
+    ms_samp, _, _ = timed(args.sampling_temperature, max(10, args.steps // 2), args.warmup)
     accept_samp = outs[2].float().mean().item()
 
     # end to end through the public API: inputs from pinned host memory each step, results
@@ -249,18 +251,23 @@ def run_ours(args):
     lm_max = replicas.max_over_ranks(lm_ms)
 
     peaks, peak_src = measured_peaks()
-    w_bytes = spec.d * spec.V * 2  # the LM head, read once per launch
+    # algorithmic bytes of one call, all read by the LM-head kernel: the vocabulary
+    # projection once and the target logits once (their row statistics are folded into the
+    # same kernel); hidden rows, gate projection and outputs (< 0.5 %) are not counted.
+    # Algorithmic flops: the B*(L-1) draft rows against the vocabulary and gate projections.
+    w_bytes = spec.d * spec.V * 2
     z_bytes = spec.B * spec.L * spec.V * 2
-    achieved = w_bytes / (lm_max * 1e-3) / 1e9
-    step_achieved = (w_bytes + z_bytes) / (ms_max * 1e-3) / 1e9
+    lm_bytes = w_bytes + z_bytes
+    lm_flops = 2.0 * spec.B * (spec.L - 1) * spec.d * (spec.V + spec.r)
+    achieved = lm_bytes / (lm_max * 1e-3) / 1e9
+    tflops = lm_flops / (lm_max * 1e-3) / 1e12
+    step_achieved = lm_bytes / (ms_max * 1e-3) / 1e9
     traffic = ncu_traffic(args.workload)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(data, spec, args.cpu_seconds)
 
-    row_groups = (spec.B * spec.L + 255) // 256
-    launches_greedy = 2 + row_groups
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -270,23 +277,27 @@ def run_ours(args):
             "config": {"workload": spec.name, "B": spec.B, "L": spec.L, "K": 16, "V": spec.V,
                        "d": spec.d, "r": spec.r, "path_mode": args.path_mode,
                        "temperature": 0.0, "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2: W_vocab 1.56 GB read every step; "
-                             f"{nrot} rotating target-logit buffers"},
+                       "l2": f"inputs larger than L2: W_vocab {w_bytes / 1e9:.2f} GB read "
+                             f"every step; {nrot} rotating target-logit and hidden buffers"},
             "hbm_roofline_frac_step": round(step_achieved / peaks["hbm_gbs"], 4),
             "roofline": {"kernel": "k_lmhead_tc (LM head + fused top-16 + gate tiles)",
                          "bound": "hbm", "achieved": round(achieved, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4),
-                         "traffic": traffic, "algorithmic_bytes_per_launch": w_bytes,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": lm_bytes,
                          "ms_per_launch": round(lm_max, 4),
-                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                         "tensor": {"achieved": round(tflops, 1), "unit": "TFLOP/s",
+                                    "peak": peaks["bf16_tflops"],
+                                    "frac": round(tflops / peaks["bf16_tflops"], 4),
+                                    "flops_per_launch": lm_flops}},
             "e2e": {"value": round(value_e2e, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)},
             "sampling": {"temperature": args.sampling_temperature, "value": round(value_samp, 1),
                          "unit": UNIT, "ms_per_step": round(ms_samp, 4),
                          "mean_accept_len": round(accept_samp, 3)},
             "mean_accept_len": round(accept, 3),
-            "gpu_launches": launches_greedy * args.steps,
+            "gpu_launches": launches,
             "clocks": clk,
             "cpu_baseline": cpu,
         }

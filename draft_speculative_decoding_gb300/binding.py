@@ -37,6 +37,7 @@ SIGNATURES = {
     "dfs_status_string": ([_I], ctypes.c_char_p),
     "dfs_workspace_size": ([_DP], ctypes.c_size_t),
     "dfs_set_trace_events": ([_P, _P], _I),
+    "dfs_launch_count": ([], ctypes.c_uint64),
     "dfs_workspace_init": ([_P, ctypes.c_size_t, _P], _I),
     "dfs_get_device_error": ([_P, ctypes.c_size_t, ctypes.POINTER(_I), _P], _I),
     "dfs_lmhead_topk": ([_DP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
@@ -138,6 +139,11 @@ def dfs_set_trace_events(start=None, stop=None):
     _check("dfs_set_trace_events", load().dfs_set_trace_events(
         None if start is None else ctypes.c_void_p(start.cuda_event),
         None if stop is None else ctypes.c_void_p(stop.cuda_event)))
+
+
+def dfs_launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load().dfs_launch_count())
 
 
 def dfs_get_device_error(ws: torch.Tensor, stream=None) -> int:

@@ -3,6 +3,7 @@
 // allocates, frees or synchronises except dfs_get_device_error.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
@@ -272,11 +273,19 @@ cudaError_t run_zreduce(const dfs_dims& d, const Layout& L, void* ws, const void
   return dfs::launch_zreduce(z, s);
 }
 
+std::atomic<unsigned long long> g_launches{0};
+
 }  // namespace
+
+namespace dfs {
+void note_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n)); }
+}  // namespace dfs
 
 extern "C" {
 
 int dfs_version(void) { return 1; }
+
+uint64_t dfs_launch_count(void) { return g_launches.load(); }
 
 int dfs_set_trace_events(void* start, void* stop) {
   g_trace_start = static_cast<cudaEvent_t>(start);

@@ -43,6 +43,10 @@ struct LmheadLaunch {
   int* zero_ptr;       // counters cleared for the later kernels of the call
   int zero_count;
 };
+// Adds n to the process-wide count of kernels this library has launched. Every launch site
+// calls it once the runtime has accepted the launch; dfs_launch_count reads the total.
+void note_launches(int n);
+
 cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s);
 // Whether a call with these rows runs as row-split pairs (then each row gets G / 2 partial
 // lists instead of G).

@@ -163,7 +163,9 @@ cudaError_t launch_lmhead_simt(const LmheadSimtLaunch& a, cudaStream_t s) {
     k_row_top16<<<a.rows_total, 256, 0, s>>>(a.logits_ws, a.V, a.L, a.part_val, a.part_idx);
   }
   if (a.gate) k_gate_simt<<<a.rows_total, 256, 0, s>>>(a.hidden, a.Wg, a.rows_total, a.L, a.d, a.r, a.gate_out);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launches((a.vocab ? 2 : 0) + (a.gate ? 1 : 0));
+  return e;
 }
 
 }  // namespace dfs

@@ -580,7 +580,9 @@ cudaError_t launch_cfg(const LmheadParams& prm, int grid, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, prm);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
 }
 
 template <int MT, int NT, int NBUF, int SW, int SH>

@@ -702,7 +702,15 @@ cudaError_t launch_dependent(K kern, dim3 grid, dim3 block, size_t smem, cudaStr
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
+}
+
+// The status of a plain launch, counted when the runtime accepted it.
+cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) note_launches(1);
+  return e;
 }
 
 template <typename K>
@@ -721,7 +729,7 @@ cudaError_t launch_zreduce(const ZReduceLaunch& a, cudaStream_t s) {
   else
     k_zreduce<false><<<grid, 128, 0, s>>>(a.Z, a.zdtype == 0, a.V, a.nchunk, 0.f, a.zmax,
                                           a.zarg, a.zsum, a.zero_ptr, a.zero_count);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_tail_fused(const TailLaunch& a, cudaStream_t s) {
@@ -736,7 +744,7 @@ cudaError_t launch_merge(const TailLaunch& a, cudaStream_t s) {
   cudaError_t e = set_smem(k_merge, bytes);
   if (e != cudaSuccess) return e;
   k_merge<<<dim3(a.L - 1, a.B), kTailThreads, bytes, s>>>(a);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_pair(const TailLaunch& a, cudaStream_t s) {
@@ -744,17 +752,17 @@ cudaError_t launch_pair(const TailLaunch& a, cudaStream_t s) {
   cudaError_t e = set_smem(k_pair, bytes);
   if (e != cudaSuccess) return e;
   k_pair<<<dim3(a.L - 1, a.B), kTailThreads, bytes, s>>>(a);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_path(const TailLaunch& a, cudaStream_t s) {
   k_path<<<a.B, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_verify(const TailLaunch& a, cudaStream_t s) {
   k_verify<<<a.B, kTailThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 }  // namespace dfs

@@ -101,6 +101,11 @@ int dfs_get_device_error(void* ws, size_t ws_bytes, int* err, void* stream);
  * LM-head kernel and `stop` just after it. NULL, NULL disables. Host-side only. */
 int dfs_set_trace_events(void* start, void* stop);
 
+/* The number of kernels this library has launched in this process, over all calls,
+ * threads and devices (launches the CUDA runtime accepted). Host-side only; never
+ * fails. Differences between two reads count the kernels of the calls in between. */
+uint64_t dfs_launch_count(void);
+
 /* Step a1 -- LM head and keep top-16 ("The right tokens are already there";
  * "A lightweight path selector": U_t(b) is the drafter's own logit).
  *   hidden   [B, L, d]   dtype

@@ -41,6 +41,7 @@ def test_binding_covers_every_declared_symbol():
 
 def test_host_only_calls(lib):
     assert lib.dfs_version() == 1
+    launches = binding.dfs_launch_count()
     assert binding.status_string(binding.DFS_ERR_WORKSPACE) == "workspace too small"
     # invalid dims are rejected on the host before any device work
     assert lib.dfs_workspace_size(None) == 0
@@ -58,3 +59,5 @@ def test_host_only_calls(lib):
                                0, ctypes.c_void_p(0x3000), None, None) == binding.DFS_ERR_INVALID
     assert lib.dfs_path_select(ctypes.byref(ok), ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000),
                                7, ctypes.c_void_p(0x3000), None, None) == binding.DFS_ERR_INVALID
+    # calls rejected on the host launch nothing
+    assert binding.dfs_launch_count() == launches

@@ -124,6 +124,21 @@ def test_fused_is_deterministic(lib):
         assert np.array_equal(a[k], b[k]), k
 
 
+def test_fused_launch_count(lib):
+    """One fused call launches the LM-head kernel once per group of up to 256 draft rows,
+    then the tail once (target-row statistics folded into the LM-head kernel)."""
+    for spec in (SMALL[1], SMALL[3]):
+        data = wl.generate(spec, "cuda")
+        dims = dims_for(spec)
+        ws = binding.alloc_workspace(dims)
+        before = binding.dfs_launch_count()
+        binding.dfs_select_verify(dims, data["h"], data["W"], data["Wg"], data["A"], data["Bt"],
+                                  data["x0"], data["Z"], binding.DFS_PATH_GREEDY, 0.0, 1, ws)
+        torch.cuda.synchronize()
+        rows = spec.B * spec.L
+        assert binding.dfs_launch_count() - before == (rows + 255) // 256 + 1
+
+
 FULL = [
     (wl.SINGLE, None),                  # B=1: every request
     (wl.SMALL_BATCH, [0, 5]),
