@@ -58,7 +58,7 @@ def measured_peaks():
 
 def lmhead_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("lmhead_tc.cu", "common.cuh"):
+    for name in ("lmhead_tc.cu", "common.cuh", "rowstat.cuh"):
         with open(os.path.join(ROOT, "draft_speculative_decoding_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -263,6 +263,8 @@ def run_ours(args):
     tflops = lm_flops / (lm_max * 1e-3) / 1e12
     step_achieved = lm_bytes / (ms_max * 1e-3) / 1e9
     traffic = ncu_traffic(args.workload)
+    lm_kernel = ("k_lmhead_pair" if spec.B * spec.L > 128 else "k_lmhead_tc") + \
+        " (LM head + top-16 + gate tiles + target-row statistics)"
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -280,7 +282,7 @@ def run_ours(args):
                        "l2": f"inputs larger than L2: W_vocab {w_bytes / 1e9:.2f} GB read "
                              f"every step; {nrot} rotating target-logit and hidden buffers"},
             "hbm_roofline_frac_step": round(step_achieved / peaks["hbm_gbs"], 4),
-            "roofline": {"kernel": "k_lmhead_tc (LM head + fused top-16 + gate tiles)",
+            "roofline": {"kernel": lm_kernel,
                          "bound": "hbm", "achieved": round(achieved, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4),

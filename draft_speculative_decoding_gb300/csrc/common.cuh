@@ -239,15 +239,81 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D, M = 128.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int n, bool b_mn_major) {
+// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D (M = 128 per CTA; M = 256 for
+// an MMA across a CTA pair).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int n, bool b_mn_major, int m = 128) {
   return (1u << 4)                          // D format: f32
          | (1u << 7)                        // A format: bf16
          | (1u << 10)                       // B format: bf16
          | (0u << 15)                       // A K-major
          | ((b_mn_major ? 1u : 0u) << 16)   // B major-ness
          | (static_cast<uint32_t>(n >> 3) << 17)
-         | (static_cast<uint32_t>(128 >> 4) << 24);
+         | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- CTA pairs
+// A CTA pair is the two CTAs of a cluster whose ranks differ in bit 0; an MMA issued with
+// cta_group::2 by the even one (the leader) computes M = 256 rows, 128 in each CTA's tensor
+// memory, from A rows held 128 per CTA and a B tile held half (N/2 columns) per CTA.
+
+// The shared::cluster address of the object at shared::cta address `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive (release, cluster scope) on a barrier given by its shared::cluster address,
+// possibly in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// 2D tiled load into this CTA's shared memory whose completion is counted on the barrier at
+// shared::cluster address `bar` (this CTA's or its pair peer's).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, uint32_t bar,
+                                                 int c0, int c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Tensor memory for pair MMAs: one warp of each CTA of the pair executes these together.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Pair MMA, issued by one thread of the leader CTA.
+__device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the barrier at `bar`'s offset in each CTA of cta_mask once every pair MMA
+// issued so far by this thread has completed.
+__device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
 }
 
 }  // namespace dfs

@@ -33,16 +33,13 @@ int device_sm_count() {
   return cache[dev];
 }
 
-// Tile-shape choice for row groups of 129..256 rows: 0 = automatic (4), 1 = two 128-row MMA
-// tiles x 128 vocabulary columns with a deep W ring, 2 = two tiles x 256 columns
-// (single-buffered TMEM), 3 = as 1 with a deeper hidden-row ring, 4 = row-split pairs.
-// Read from DFS_LMHEAD_VARIANT on each call, for tuning.
+// Tile-shape choice for row groups of 129..256 rows: 5 (default) = CTA pairs with pair MMAs,
+// each CTA staging half of the W tile; 4 = CTA pairs with per-CTA MMAs sharing each W tile
+// by multicast. Read from DFS_LMHEAD_VARIANT on each call, for tuning.
 int lmhead_variant_override() {
   const char* s = std::getenv("DFS_LMHEAD_VARIANT");
-  const int v = s ? std::atoi(s) : 0;
-  return (v <= 0 || v > 4) ? 4 : v;  // automatic: row-split pairs
+  return (s != nullptr && std::atoi(s) == 4) ? 4 : 5;
 }
-
 
 struct Layout {
   size_t err, counters;

@@ -28,10 +28,9 @@ struct LmheadLaunch {
   int G;               // grid of the vocabulary launch = lists per row
   float* gate_out;     // [rows_total][r]
   int* err;
-  int lmhead_variant;  // 0 = automatic; 1 = two M-tiles x 128 vocab, deep W ring;
-                       // 2 = two M-tiles x 256 vocab (single-buffered TMEM);
-                       // 3 = as 1 with a deeper hidden-row ring;
-                       // 4 = row-split pairs (128 rows x 256 columns per CTA, W multicast)
+  int lmhead_variant;  // row groups of 129..256 rows: 5 = CTA pairs with pair MMAs (each
+                       // CTA stages half of the W tile); 4 = CTA pairs with per-CTA MMAs
+                       // (the W tile multicast to both)
   int cluster;         // CTAs per cluster sharing hidden-row tiles by multicast (1, 2 or 4)
   // Target-logit row statistics computed by the kernel's spare warps (z_rows = 0: none).
   const void* Z;       // [z_rows, V]
@@ -48,8 +47,8 @@ struct LmheadLaunch {
 void note_launches(int n);
 
 cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s);
-// Whether a call with these rows runs as row-split pairs (then each row gets G / 2 partial
-// lists instead of G).
+// Whether a call with these rows runs on CTA pairs that split the rows (then each row gets
+// G / 2 partial lists, one per pair, instead of G).
 bool lmhead_row_split(int rows_total, int variant, int G);
 
 // ---- a1 (+a2) for fp32 inputs, on CUDA cores ----

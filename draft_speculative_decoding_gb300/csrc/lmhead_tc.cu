@@ -10,28 +10,28 @@
 // of one row group and every v of the vocabulary, then per row the 16 largest
 // (logit, id) pairs. The logits never leave the SM.
 //
-// Design:
-//   * persistent grid, one CTA per SM; CTA i takes vocabulary tiles i, i+G, ...;
-//   * two TMA producers fill two rings of shared memory guarded by mbarriers, 128-byte
-//     swizzle: warp 0 streams W_vocab (the MN-major B operand, vocabulary contiguous,
-//     64x64 boxes) through a deep ring, because HBM latency times the per-SM share of
-//     bandwidth needs ~100 KB of W in flight per SM; warp 2 feeds the hidden rows (the
-//     K-major A operand, L2-resident, 64x128 boxes) through a shallow ring;
-//   * warp 1 issues tcgen05.mma (M = 128 rows, N = NT vocabulary columns, K = 16 per
-//     instruction) into TMEM accumulators, NBUF of them so the epilogue of one tile
-//     overlaps the MMAs of the next;
-//   * warps 4.. (4 per 128-row tile) drain TMEM with tcgen05.ld: each thread owns one
-//     row and keeps its running top-16 in registers (unsorted, weakest member tracked); per
-//     32-column load it tests the maximum against the weakest, then visits only the
-//     lane's own candidates, so a warp does not run insertion code for its other lanes;
-//     at the end it sorts the 16 and writes them as one partial list of the row (the tail
-//     kernel merges the G lists of a row).
-//   * gate tiles use W_g [r, d] (K-major) as the B operand; their epilogue applies the
-//     sigmoid and stores g[m, j] in fp32;
-//   * four more warps (3 and the last three) stream the target logits (16-byte loads,
-//     read once, 8 per lane in flight) and write per-chunk row statistics (max, argmax,
-//     sum of exp) for verification, so those bytes move while the tensor pipe works on W
-//     instead of in a kernel of their own.
+// Design (both kernels persistent, one CTA per SM, warp-specialised):
+//   * a TMA producer thread streams W_vocab (the MN-major B operand, vocabulary contiguous,
+//     64x64 boxes, 128-byte swizzle, evict-first) and the hidden rows (the K-major A operand,
+//     L2-resident, evict-last) through rings of shared memory guarded by mbarriers;
+//   * one thread issues tcgen05.mma (bf16 in, fp32 accumulate, K = 16 per instruction) into
+//     two TMEM accumulators, so the epilogue of one tile overlaps the MMAs of the next;
+//   * four epilogue warps drain TMEM with tcgen05.ld, one row per thread, keeping the row's
+//     running top-16 in registers (sorted, so the entry threshold is the last member); a
+//     32-column chunk is first tested by its maximum, then only the lane's candidates are
+//     inserted; at the end each thread writes its sorted list as one partial list of its row
+//     (the tail kernel merges the partial lists of a row);
+//   * gate tiles use W_g [r, d] (K-major) as the B operand; their epilogue applies the sigmoid
+//     and stores g[m, j] in fp32;
+//   * four more warps stream the target logits (16-byte loads, read once, a whole 4096-token
+//     chunk per warp in flight) and write per-chunk row statistics (max, argmax, sum of exp)
+//     for verification, so those bytes move while the tensor pipe works on W.
+// k_lmhead_tc serves row groups of up to 128 rows (M = 128 x N = 256 per CTA; clusters share
+// the hidden-row tiles by multicast) and, as variant 4, CTA pairs that split 256 rows with
+// the W tile multicast to both. k_lmhead_pair serves 129..256 rows with pair MMAs
+// (cta_group::2, M = 256 x N = 256 across two SMs): each CTA stages only half of the W tile,
+// which halves the shared-memory bytes per MMA -- at 256 rows the tensor pipe must run near
+// full rate alongside the HBM stream, and shared-memory bandwidth, not HBM, was the limit.
 // Every mbarrier wait is bounded; on expiry the kernel sets the error word, stops all
 // roles, and frees its tensor memory.
 #include <cuda.h>
@@ -44,6 +44,8 @@
 #include "rowstat.cuh"
 
 namespace dfs {
+
+static_assert(kZChunk == 16 * 256, "zchunk_stat_warp covers a chunk as 16 loads x 32 lanes x 8");
 
 struct LmheadParams {
   CUtensorMap tm_h;  // hidden [rows_total, d], box 64 (k) x 128 (rows)
@@ -91,15 +93,13 @@ struct LmCfg {
   static constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
 };
 
-// A row's running top-16, unsorted, with its weakest member tracked (lowest value; among
-// equal values the highest id, which ranks last). Ids arrive in increasing order, so a new
-// value enters only when it beats the weakest strictly.
+// A row's running top-16, kept sorted by (value desc, id asc); v[15] is the entry threshold.
+// A thread offers the columns of its row in increasing id order (tiles in increasing order,
+// columns increasing within a tile), so a newcomer ranks after every member of equal value:
+// it enters only when it beats v[15] strictly, and goes after the members >= it.
 struct Top16 {
   float v[kK];
   int i[kK];
-  float wv;  // weakest value (the entry threshold)
-  int wi;    // its id
-  int wp;    // its slot
 };
 
 __device__ __forceinline__ void top16_init(Top16& t) {
@@ -108,48 +108,22 @@ __device__ __forceinline__ void top16_init(Top16& t) {
     t.v[k] = -INFINITY;
     t.i[k] = 0x7fffffff;
   }
-  t.wv = -INFINITY;
-  t.wi = 0x7fffffff;
-  t.wp = 0;
 }
 
-// Replace the weakest member by (x, id) (caller checked x > t.wv), then find the new weakest.
-__device__ __forceinline__ void top16_replace(Top16& t, float x, int id) {
+// Insert (x, id) (caller checked x > t.v[15]): the members >= x keep their slots, the rest
+// shift down one. Every output slot depends only on two comparisons, so the 16 updates
+// issue independently instead of as a chain.
+__device__ __forceinline__ void top16_insert(Top16& t, float x, int id) {
+  bool ge[kK];
 #pragma unroll
-  for (int k = 0; k < kK; ++k) {
-    const bool here = k == t.wp;
-    t.v[k] = here ? x : t.v[k];
-    t.i[k] = here ? id : t.i[k];
+  for (int k = 0; k < kK; ++k) ge[k] = t.v[k] >= x;
+#pragma unroll
+  for (int k = kK - 1; k >= 1; --k) {
+    t.v[k] = ge[k] ? t.v[k] : (ge[k - 1] ? x : t.v[k - 1]);
+    t.i[k] = ge[k] ? t.i[k] : (ge[k - 1] ? id : t.i[k - 1]);
   }
-  float wv = t.v[0];
-  int wi = t.i[0], wp = 0;
-#pragma unroll
-  for (int k = 1; k < kK; ++k) {
-    const bool weaker = t.v[k] < wv || (t.v[k] == wv && t.i[k] > wi);
-    wv = weaker ? t.v[k] : wv;
-    wi = weaker ? t.i[k] : wi;
-    wp = weaker ? k : wp;
-  }
-  t.wv = wv;
-  t.wi = wi;
-  t.wp = wp;
-}
-
-// Sort into (value desc, id asc): odd-even transposition, static indices only.
-__device__ __forceinline__ void top16_sort(Top16& t) {
-#pragma unroll
-  for (int pass = 0; pass < kK; ++pass) {
-#pragma unroll
-    for (int k = pass & 1; k + 1 < kK; k += 2) {
-      const bool swap = t.v[k + 1] > t.v[k] || (t.v[k + 1] == t.v[k] && t.i[k + 1] < t.i[k]);
-      const float a = t.v[k], b = t.v[k + 1];
-      const int ia = t.i[k], ib = t.i[k + 1];
-      t.v[k] = swap ? b : a;
-      t.v[k + 1] = swap ? a : b;
-      t.i[k] = swap ? ib : ia;
-      t.i[k + 1] = swap ? ia : ib;
-    }
-  }
+  t.v[0] = ge[0] ? t.v[0] : x;
+  t.i[0] = ge[0] ? t.i[0] : id;
 }
 
 // r[j] for a run-time j in 0..31 by a five-level select tree (keeps r in registers).
@@ -166,22 +140,35 @@ __device__ __forceinline__ uint32_t pick32(const uint32_t (&r)[32], int j) {
   return (j & 1) ? d[1] : d[0];
 }
 
-// Offer 32 consecutive logits (ids cbase..cbase+31, those at or past lim ignored): a cheap
-// maximum test first, then only the lanes' actual candidates, lowest id first.
+// Offer 32 consecutive logits (ids cbase..cbase+31, those at or past lim ignored): a
+// tree maximum against the threshold first, then only the lane's candidates, lowest id
+// first.
 __device__ __forceinline__ void top16_offer32(Top16& t, const uint32_t (&r)[32], int cbase, int lim) {
-  float mx = -INFINITY;
+  float m[16];
+  if (lim >= 32) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) mx = fmaxf(mx, j < lim ? __uint_as_float(r[j]) : -INFINITY);
-  if (!(mx > t.wv)) return;
+    for (int k = 0; k < 16; ++k) m[k] = fmaxf(__uint_as_float(r[k]), __uint_as_float(r[k + 16]));
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      m[k] = fmaxf(k < lim ? __uint_as_float(r[k]) : -INFINITY,
+                   k + 16 < lim ? __uint_as_float(r[k + 16]) : -INFINITY);
+  }
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int k = 0; k < w; ++k) m[k] = fmaxf(m[k], m[k + w]);
+  const float thr = t.v[kK - 1];
+  if (!(m[0] > thr)) return;
   uint32_t mask = 0;
 #pragma unroll
   for (int j = 0; j < 32; ++j)
-    mask |= (j < lim && __uint_as_float(r[j]) > t.wv) ? (1u << j) : 0u;
+    mask |= (j < lim && __uint_as_float(r[j]) > thr) ? (1u << j) : 0u;
   while (mask) {
     const int j = __ffs(mask) - 1;
     mask &= mask - 1;
     const float x = __uint_as_float(pick32(r, j));
-    if (x > t.wv) top16_replace(t, x, cbase + j);
+    if (x > t.v[kK - 1]) top16_insert(t, x, cbase + j);
   }
 }
 
@@ -428,23 +415,8 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
     const int is_bf16 = p.zdtype == 0;
     for (int u = blockIdx.x * Cfg::kZWarps + zw; u < n_units; u += gridDim.x * Cfg::kZWarps) {
       const int row = u / p.z_nchunk, chunk = u - row * p.z_nchunk;
-      const size_t rbase = static_cast<size_t>(row) * p.V;
-      RowStat st = rowstat_empty();
-#pragma unroll 1
-      for (int bt = 0; bt < 2; ++bt) {
-        float x[8][8];
-        int v0[8];
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          v0[g] = chunk * kZChunk + (bt * 8 + g) * 256 + lane * 8;
-          if (v0[g] < p.V) load8_stream(p.Z, is_bf16, rbase + v0[g], x[g]);
-        }
-        if (p.z_inv_T > 0.f)
-          rowstat_fold<8, true>(st, x, v0, p.V, p.z_inv_T);
-        else
-          rowstat_fold<8, false>(st, x, v0, p.V, 0.f);
-      }
-      st = warp_combine(st, p.z_inv_T);
+      const RowStat st = zchunk_stat_warp(p.Z, is_bf16, static_cast<size_t>(row) * p.V, chunk,
+                                          p.V, p.z_inv_T, lane);
       if (lane == 0) {
         const size_t o = static_cast<size_t>(row) * p.z_nchunk + chunk;
         p.zmax[o] = st.m;
@@ -499,7 +471,6 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
       }
     }
     if (p.write_partials && valid) {
-      top16_sort(top);
       // one list per CTA computing the row: per cluster for a row-split pair
       const size_t off = (static_cast<size_t>(grow) * p.G + (RS ? cid : blockIdx.x)) * kK;
       float4* pv = reinterpret_cast<float4*>(p.part_val + off);
@@ -521,6 +492,260 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
   if (CL > 1) cluster_sync();  // no CTA leaves while a peer may still signal its barriers
+}
+
+
+// ------------------------------------------------------------------ CTA-pair kernel
+// Row groups of 129..256 rows on CTA pairs with pair MMAs (cta_group::2): the pair takes one
+// 256-column vocabulary tile at a time; each CTA stages its own 128 hidden rows and HALF of
+// the W tile (128 columns), and the leader's M = 256 x N = 256 MMAs read the B halves of
+// both CTAs, so each SM's shared memory takes and serves half the W bytes it would as a
+// lone M = 128 x N = 256 CTA. A stage holds one k-block (64) of both operands; the leader's
+// full barrier counts both CTAs' bytes; the MMA commits release both CTAs' stages and signal
+// both CTAs' accumulators; both CTAs' epilogue warps release an accumulator on the leader.
+template <int S>
+struct PairCfg {
+  static constexpr int kHalfBytes = 128 * 128;  // 128 vocabulary columns (or W_g rows) x 64 k
+  static constexpr int kHBytes = 128 * 128;     // 128 hidden rows x 64 k
+  static constexpr int kStage = kHalfBytes + kHBytes;
+  static constexpr int kNBuf = 2;
+  static constexpr int kAccCols = 256;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kEpiWarps = 4;  // warps 4..7, one TMEM lane quarter each
+  static constexpr int kZWarps = 4;    // warps 2, 3, 8, 9
+  static constexpr int kThreads = 32 * 10;
+  static constexpr int kBarBytes = 8 * (2 * S + 2 * kNBuf) + 16;
+  static constexpr size_t kSmem = 1024 + size_t(S) * kStage + kBarBytes;
+  static_assert(kSmem <= 232448, "shared memory");
+  static_assert(kAccCols * kNBuf <= kTmemCols, "TMEM");
+};
+
+template <int S>
+__global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
+    k_lmhead_pair(const __grid_constant__ LmheadParams p) {
+  using Cfg = PairCfg<S>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* ring = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + size_t(S) * Cfg::kStage);
+  uint64_t* full = bars;            // leader: both CTAs' bytes of a stage have landed
+  uint64_t* empty = bars + S;       // each CTA: the pair MMAs reading a stage are done
+  uint64_t* tfull = bars + 2 * S;   // each CTA: an accumulator is complete
+  uint64_t* tempty = tfull + Cfg::kNBuf;  // leader: both CTAs have drained an accumulator
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + Cfg::kNBuf);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < Cfg::kNBuf; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 2 * Cfg::kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&p.tm_h);
+    prefetch_tensormap(&p.tm_w);
+    prefetch_tensormap(&p.tm_g);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before either signals the other's
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  grid_dependents_launch();
+
+  const int n_tiles = p.n_vocab_tiles + p.n_gate_tiles;
+  const int cid = blockIdx.x >> 1;
+  const int ncl = gridDim.x >> 1;
+  const int KB = p.d / 64;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------- TMA producer: W half + hidden rows
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_keep = policy_evict_last();
+      const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);  // the leader's barriers
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = cid; ok && tile < n_tiles; tile += ncl) {
+        const bool is_vocab = tile < p.n_vocab_tiles;
+        const int n0 = (is_vocab ? tile : tile - p.n_vocab_tiles) * 256 + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * Cfg::kStage);
+          const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
+          const uint32_t sw = smem_u32(ring + size_t(stage) * Cfg::kStage);
+          if (is_vocab) {
+            tma_load_2d_pair(sw, &p.tm_w, fb, n0, kb * 64, pol_stream);
+            tma_load_2d_pair(sw + 8192, &p.tm_w, fb, n0 + 64, kb * 64, pol_stream);
+          } else {
+            tma_load_2d_pair(sw, &p.tm_g, fb, kb * 64, n0, pol_keep);
+          }
+          tma_load_2d_pair(sw + Cfg::kHalfBytes, &p.tm_h, fb, kb * 64,
+                           p.row0 + static_cast<int>(rank) * 128, pol_keep);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // The releases of the last stages arrive from the leader's commits; this CTA may exit
+      // only after they have landed on its barriers.
+      if (ok) {
+        for (int i = 0; i < S; ++i) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, p.err, abort_flag)) break;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------- pair MMA issuer (leader)
+      constexpr uint32_t kIdescVocab = idesc_bf16_f32(256, true, 256);
+      constexpr uint32_t kIdescGate = idesc_bf16_f32(256, false, 256);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = cid; ok && tile < n_tiles; tile += ncl) {
+        const bool is_vocab = tile < p.n_vocab_tiles;
+        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sw = smem_u32(ring + size_t(stage) * Cfg::kStage);
+          const uint32_t sh = sw + Cfg::kHalfBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bdesc = is_vocab ? smem_desc_sw128(sw + kk * 2048, 8192, 1024)
+                                            : smem_desc_sw128(sw + kk * 32, 0, 1024);
+            const uint64_t adesc = smem_desc_sw128(sh + kk * 32, 0, 1024);
+            tc_mma_bf16_pair(d0, adesc, bdesc, is_vocab ? kIdescVocab : kIdescGate,
+                             (kb | kk) != 0);
+          }
+          tc_commit_pair_multicast(smem_u32(&empty[stage]), 0x3);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(smem_u32(&tfull[acc]), 0x3);
+        if (++acc == Cfg::kNBuf) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 2 || warp == 3 || warp >= 8) {
+    // ------------------------------------------------ target-logit row statistics
+    const int zw = warp < 4 ? warp - 2 : warp - 6;
+    if (blockIdx.x == 0 && p.zero_ptr != nullptr)
+      for (int i = zw * 32 + lane; i < p.zero_count; i += 32 * Cfg::kZWarps) p.zero_ptr[i] = 0;
+    const int n_units = p.z_rows * p.z_nchunk;
+    const int is_bf16 = p.zdtype == 0;
+    for (int u = blockIdx.x * Cfg::kZWarps + zw; u < n_units; u += gridDim.x * Cfg::kZWarps) {
+      const int row = u / p.z_nchunk, chunk = u - row * p.z_nchunk;
+      const RowStat st = zchunk_stat_warp(p.Z, is_bf16, static_cast<size_t>(row) * p.V, chunk,
+                                          p.V, p.z_inv_T, lane);
+      if (lane == 0) {
+        const size_t o = static_cast<size_t>(row) * p.z_nchunk + chunk;
+        p.zmax[o] = st.m;
+        p.zarg[o] = st.i;
+        if (p.z_inv_T > 0.f) p.zsum[o] = st.s;
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const int row = static_cast<int>(rank) * 128 + q * 32 + lane;
+    const int grow = p.row0 + row;
+    const bool valid = row < p.rows && (grow % p.L) != 0;  // skip each block's verified slot
+    const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
+    Top16 top;
+    top16_init(top);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cid; tile < n_tiles; tile += ncl) {
+      const bool is_vocab = tile < p.n_vocab_tiles;
+      const int n0 = (is_vocab ? tile : tile - p.n_vocab_tiles) * 256;
+      if (!mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, p.err, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * Cfg::kAccCols);
+      for (int c = 0; c < 8; ++c) {
+        uint32_t rr[32];
+        __syncwarp();  // tcgen05.ld is warp-collective; lanes diverged on row validity
+        tmem_ld_32x32b_x32(tbase + c * 32, rr);
+        tmem_ld_wait();
+        if (!valid) continue;
+        const int cbase = n0 + c * 32;
+        if (is_vocab) {
+          top16_offer32(top, rr, cbase, p.V - cbase);  // columns past V are not tokens
+        } else {
+          float* dst = p.gate_out + static_cast<size_t>(grow) * p.r;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (cbase + j < p.r) dst[cbase + j] = 1.0f / (1.0f + expf(-__uint_as_float(rr[j])));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
+      if (++acc == Cfg::kNBuf) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+    if (p.write_partials && valid) {
+      const size_t off = (static_cast<size_t>(grow) * p.G + cid) * kK;  // one list per pair
+      float4* pv = reinterpret_cast<float4*>(p.part_val + off);
+      int4* pi = reinterpret_cast<int4*>(p.part_idx + off);
+#pragma unroll
+      for (int j = 0; j < kK / 4; ++j) {
+        pv[j] = make_float4(top.v[4 * j], top.v[4 * j + 1], top.v[4 * j + 2], top.v[4 * j + 3]);
+        pi[j] = make_int4(top.i[4 * j], top.i[4 * j + 1], top.i[4 * j + 2], top.i[4 * j + 3]);
+      }
+    }
+  }
+
+  // -------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // every pair MMA and every TMEM read of both CTAs is complete
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+  }
+  cluster_sync();  // neither CTA leaves while its peer may still use the pair's resources
 }
 
 // ------------------------------------------------------------------ host side
@@ -585,6 +810,34 @@ cudaError_t launch_cfg(const LmheadParams& prm, int grid, cudaStream_t s) {
   return e;
 }
 
+template <int S>
+cudaError_t launch_pair(const LmheadParams& prm, int grid, cudaStream_t s) {
+  using Cfg = PairCfg<S>;
+  auto kern = k_lmhead_pair<S>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::kSmem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
+}
+
 template <int MT, int NT, int NBUF, int SW, int SH>
 cudaError_t launch_cluster(const LmheadParams& prm, int grid, int cl, cudaStream_t s) {
   if (cl == 4 && grid % 4 == 0) return launch_cfg<MT, NT, NBUF, SW, SH, 4>(prm, grid, s);
@@ -595,7 +848,8 @@ cudaError_t launch_cluster(const LmheadParams& prm, int grid, int cl, cudaStream
 }  // namespace
 
 bool lmhead_row_split(int rows_total, int variant, int G) {
-  return rows_total > 128 && variant == 4 && G % 2 == 0;
+  (void)variant;  // both shapes for 129..256 rows leave one partial list per CTA pair
+  return rows_total > 128 && G % 2 == 0;
 }
 
 cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
@@ -611,7 +865,8 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
   prm.V = a.V;
   prm.d = a.d;
   prm.r = a.r;
-  const bool rs = a.vocab && lmhead_row_split(a.rows_total, a.lmhead_variant, a.G);
+  // More than 128 rows: CTA pairs split each row group (gate-only launches included)
+  const bool rs = lmhead_row_split(a.rows_total, a.lmhead_variant, a.vocab ? a.G : 2);
   prm.G = rs ? a.G / 2 : a.G;  // partial lists per row: one per CTA, or per pair when split
   prm.part_val = a.part_val;
   prm.part_idx = a.part_idx;
@@ -632,35 +887,30 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
     prm.zero_ptr = first ? a.zero_ptr : nullptr;
     prm.zero_count = first ? a.zero_count : 0;
     prm.rows = a.rows_total - row0 < 256 ? a.rows_total - row0 : 256;
-    // Row groups of up to 128 rows: one M tile x 256 vocabulary columns, double-buffered
-    // TMEM. Up to 256 rows: two M tiles x 128 columns with double-buffered TMEM (variants
-    // 1 and 3 differ in how the 224 KB of rings split between W and the hidden rows), or
-    // x 256 columns with one TMEM buffer (variant 2), or a row-split pair (variant 4: two
-    // CTAs of 128 rows x 256 columns sharing each W tile by multicast).
-    const bool two = prm.rows > 128;
-    const int variant = rs ? 4 : two ? (a.lmhead_variant >= 1 && a.lmhead_variant <= 3 ? a.lmhead_variant : 1) : 0;
-    const int NT = (variant == 1 || variant == 3) ? 128 : 256;
+    // Row groups of up to 128 rows: one M tile x 256 vocabulary columns per CTA,
+    // double-buffered TMEM, clusters sharing the hidden rows. 129..256 rows: CTA pairs on
+    // one 256-column tile, 128 rows each: pair MMAs with each CTA staging half of the W tile
+    // (variant 5, the default), or per-CTA MMAs with the W tile multicast to both CTAs
+    // (variant 4).
+    const int variant = rs ? (a.lmhead_variant == 4 ? 4 : 5) : 0;
+    const int NT = 256;
     prm.n_vocab_tiles = a.vocab ? (a.V + NT - 1) / NT : 0;
     prm.n_gate_tiles = a.gate ? (a.r + NT - 1) / NT : 0;
     prm.write_partials = a.vocab ? 1 : 0;
     if (!encode_bf16_2d(&prm.tm_g, a.gate ? a.Wg : a.hidden, a.d, a.gate ? a.r : a.rows_total,
-                        64, static_cast<uint32_t>(a.gate ? (variant == 4 ? NT / 2 : NT) : 128)))
+                        64, static_cast<uint32_t>(a.gate ? (variant >= 4 ? NT / 2 : NT) : 128)))
       return cudaErrorInvalidValue;
-    const int grid = a.vocab ? a.G : (prm.n_gate_tiles > 0 ? prm.n_gate_tiles : 1);
+    const int grid = a.vocab ? a.G : (prm.n_gate_tiles > 0 ? prm.n_gate_tiles : 1) * (rs ? 2 : 1);
     cudaError_t e;
     // Clusters share the hidden rows by multicast; the gate-only launch (a tile or two)
     // runs without.
     const int cl = a.vocab ? a.cluster : 1;
-    if (variant == 4)
+    if (variant == 5)
+      e = launch_pair<7>(prm, grid, s);
+    else if (variant == 4)
       e = launch_cfg<1, 256, 2, 5, 4, 2, 1>(prm, grid, s);
-    else if (variant == 0)
-      e = launch_cluster<1, 256, 2, 5, 4>(prm, grid, cl, s);
-    else if (variant == 1)
-      e = launch_cluster<2, 128, 2, 8, 3>(prm, grid, cl, s);
-    else if (variant == 2)
-      e = launch_cluster<2, 256, 1, 4, 3>(prm, grid, cl, s);
     else
-      e = launch_cluster<2, 128, 2, 6, 4>(prm, grid, cl, s);
+      e = launch_cluster<1, 256, 2, 5, 4>(prm, grid, cl, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

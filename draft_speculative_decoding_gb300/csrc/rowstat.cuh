@@ -93,4 +93,86 @@ __device__ __forceinline__ void rowstat_fold(RowStat& st, const float (&x)[NG][8
   }
 }
 
+// The same statistics over NG groups of 8 bf16 elements still packed as loaded (16 bytes
+// per group), so twice as many loads fit in the registers a thread keeps in flight. One
+// pass, one group unpacked at a time: the running maximum is raised group by group and the
+// running sum rescaled by exp((old max - new max) / T) when it rises (the online form of
+// the same sum). Indices within a thread increase, so ties keep the lower index.
+template <int NG, bool kSoft>
+__device__ __forceinline__ void rowstat_fold_bf16(RowStat& st, const uint4 (&q)[NG],
+                                                  const int (&v0)[NG], int V, float inv_T) {
+  float m = -INFINITY, s = 0.f;
+  int mi = kIntMaxRs;
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    if (v0[g] >= V) continue;
+    const uint32_t w[4] = {q[g].x, q[g].y, q[g].z, q[g].w};
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      x[j] = bf16_bits_to_float((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
+    float gm = x[0];
+    int gj = 0;
+#pragma unroll
+    for (int j = 1; j < 8; ++j)
+      if (x[j] > gm) {
+        gm = x[j];
+        gj = j;
+      }
+    if (gm > m) {
+      if (kSoft) s *= expf((m - gm) * inv_T);
+      m = gm;
+      mi = v0[g] + gj;
+    }
+    if (kSoft && m != -INFINITY) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s += expf((x[j] - m) * inv_T);
+    }
+  }
+  if (m == -INFINITY) return;
+  if (kSoft) {
+    st = combine(st, RowStat{m, mi, s}, inv_T);
+  } else if (m > st.m) {
+    st.m = m;
+    st.i = mi;
+  }
+}
+
+// Statistics of one kZChunk-element chunk of one target row by one warp: every lane's loads
+// are issued together (16 x 16 bytes for bf16), then folded and combined across the warp.
+__device__ __forceinline__ RowStat zchunk_stat_warp(const void* Z, int is_bf16, size_t rbase,
+                                                    int chunk, int V, float inv_T, int lane) {
+  RowStat st = rowstat_empty();
+  if (is_bf16) {
+    uint4 q[16];
+    int v0[16];
+#pragma unroll
+    for (int g = 0; g < 16; ++g) {
+      v0[g] = chunk * 4096 + g * 256 + lane * 8;
+      if (v0[g] < V)
+        q[g] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(Z) + rbase + v0[g]));
+    }
+    if (inv_T > 0.f)
+      rowstat_fold_bf16<16, true>(st, q, v0, V, inv_T);
+    else
+      rowstat_fold_bf16<16, false>(st, q, v0, V, 0.f);
+  } else {
+#pragma unroll 1
+    for (int bt = 0; bt < 2; ++bt) {
+      float x[8][8];
+      int v0[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        v0[g] = chunk * 4096 + (bt * 8 + g) * 256 + lane * 8;
+        if (v0[g] < V) load8_stream(Z, 0, rbase + v0[g], x[g]);
+      }
+      if (inv_T > 0.f)
+        rowstat_fold<8, true>(st, x, v0, V, inv_T);
+      else
+        rowstat_fold<8, false>(st, x, v0, V, 0.f);
+    }
+  }
+  return warp_combine(st, inv_T);
+}
+
 }  // namespace dfs
