@@ -17,6 +17,7 @@ the same workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -36,8 +37,10 @@ UNIT = "blocks/s"
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    # defaults: our arm times 2000 steps (about 0.6 s at the bench workload, long enough for
+    # the clock samples to see the kernels under load); the oracle arm 50 one-request steps
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="throughput_B32_L8_V151936_d5120_zipf")
     ap.add_argument("--path-mode", choices=["greedy", "viterbi"], default="greedy")
@@ -79,8 +82,9 @@ def ncu_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    """nvidia-smi clocks, power and throttle reasons every 50 ms; the summary keeps only the
+    samples whose own timestamp falls inside the marked (timed) window."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
@@ -88,8 +92,9 @@ class ClockSampler:
         self.rows = []
         self.proc = None
         self.thread = None
+        self.window = [None, None]
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "200"]
+               "-lms", "50"]
         if gpu_uuid:
             cmd += ["-i", gpu_uuid]
         try:
@@ -104,13 +109,26 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 7:
+            if len(parts) >= 8:
                 self.rows.append(parts)
+
+    def mark_start(self):
+        self.window[0] = datetime.datetime.now()
+
+    def mark_end(self):
+        self.window[1] = datetime.datetime.now()
+
+    @staticmethod
+    def _when(ts: str):
+        try:
+            return datetime.datetime.strptime(ts, "%Y/%m/%d %H:%M:%S.%f")
+        except ValueError:
+            return None
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.15)  # let the sample that covers the window's end arrive
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -118,15 +136,21 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        if not self.rows:
-            return None
-        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        t0, t1 = self.window
+        rows = self.rows
+        if t0 is not None and t1 is not None:
+            rows = [r for r in rows if (w := self._when(r[0])) is not None and t0 <= w <= t1]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i] == "Active"})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(self.rows)}
+                "power_w_median": statistics.median(pw) if pw else None,
+                "samples": len(rows)}
 
 
 # ------------------------------------------------------------------- our implementation
@@ -167,7 +191,7 @@ def run_ours(args):
                                   Zs[i % nrot] if Z is None else Z, mode, T, spec.seed + i, ws,
                                   outputs=outs, stream=stream)
 
-    def timed(T, K, W, trace=False):
+    def timed(T, K, W, trace=False, clocks=None):
         for i in range(W):
             step(i, T)
         torch.cuda.synchronize()
@@ -181,6 +205,8 @@ def run_ours(args):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         n0 = binding.dfs_launch_count()
+        if clocks is not None:
+            clocks.mark_start()
         e0.record(stream)
         for i in range(K):
             if trace:
@@ -189,6 +215,8 @@ def run_ours(args):
         e1.record(stream)
         n1 = binding.dfs_launch_count()
         torch.cuda.synchronize()
+        if clocks is not None:
+            clocks.mark_end()
         binding.dfs_set_trace_events(None, None)
         replicas.barrier()
         ms = e0.elapsed_time(e1) / K
@@ -202,7 +230,7 @@ def run_ours(args):
     except Exception:
         uuid = None
     clocks = ClockSampler(uuid)
-    ms_greedy, _, launches = timed(0.0, args.steps, args.warmup)
+    ms_greedy, _, launches = timed(0.0, args.steps, args.warmup, clocks=clocks)
     clk = clocks.stop()
     # the dominant kernel's own duration, from events recorded around it on its stream (a
     # separate pass: an event between two kernels stops the second launching early)
@@ -377,6 +405,10 @@ def run_reference(args):
 
 def main():
     args = parse_args()
+    if args.steps is None:
+        args.steps = 50 if args.impl == "reference" else 2000
+    if args.warmup is None:
+        args.warmup = 3 if args.impl == "reference" else 20
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -172,6 +172,23 @@ __device__ __forceinline__ void top16_offer32(Top16& t, const uint32_t (&r)[32],
   }
 }
 
+// sigmoid of 32 gate pre-activations (columns cbase.. of row `dst`), 16-byte stores; r is a
+// multiple of 8, so each group of 4 is wholly inside or outside the r columns.
+__device__ __forceinline__ void store_gate32(float* dst, const uint32_t (&r)[32], int cbase,
+                                             int r_cols) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    if (cbase + j < r_cols) {
+      float4 g;
+      g.x = 1.0f / (1.0f + expf(-__uint_as_float(r[j])));
+      g.y = 1.0f / (1.0f + expf(-__uint_as_float(r[j + 1])));
+      g.z = 1.0f / (1.0f + expf(-__uint_as_float(r[j + 2])));
+      g.w = 1.0f / (1.0f + expf(-__uint_as_float(r[j + 3])));
+      *reinterpret_cast<float4*>(dst + cbase + j) = g;
+    }
+  }
+}
+
 template <int MT, int NT, int NBUF, int SW, int SH, int CL, int RS>
 __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads, 1)
     k_lmhead_tc(const __grid_constant__ LmheadParams p) {
@@ -455,11 +472,7 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
         if (is_vocab) {
           top16_offer32(top, rr, cbase, p.V - cbase);  // columns past V are not tokens
         } else {
-          float* dst = p.gate_out + static_cast<size_t>(grow) * p.r;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (cbase + j < p.r) dst[cbase + j] = 1.0f / (1.0f + expf(-__uint_as_float(rr[j])));
-          }
+          store_gate32(p.gate_out + static_cast<size_t>(grow) * p.r, rr, cbase, p.r);
         }
       }
       tc_fence_before();
@@ -503,6 +516,21 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
 // lone M = 128 x N = 256 CTA. A stage holds one k-block (64) of both operands; the leader's
 // full barrier counts both CTAs' bytes; the MMA commits release both CTAs' stages and signal
 // both CTAs' accumulators; both CTAs' epilogue warps release an accumulator on the leader.
+// Tile t (0 .. n_tiles - 1) of the pair kernel, taken by pair t mod ncl. The gate tiles
+// sit in the last slots of the first round: done early (their epilogue overlaps later
+// MMAs), by the pairs that get one tile fewer when the tiles do not divide evenly. The
+// vocabulary tiles fill the other slots in order. n0 = first column (or W_g row).
+struct PairTile {
+  bool vocab;
+  int n0;
+};
+__device__ __forceinline__ PairTile pair_tile(int t, int ncl, int n_gate, int n_tiles) {
+  const int first_round = ncl < n_tiles ? ncl : n_tiles;
+  const int g0 = first_round > n_gate ? first_round - n_gate : 0;
+  if (t >= g0 && t < g0 + n_gate) return {false, (t - g0) * 256};
+  return {true, (t < g0 ? t : t - n_gate) * 256};
+}
+
 template <int S>
 struct PairCfg {
   static constexpr int kHalfBytes = 128 * 128;  // 128 vocabulary columns (or W_g rows) x 64 k
@@ -582,8 +610,9 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = cid; ok && tile < n_tiles; tile += ncl) {
-        const bool is_vocab = tile < p.n_vocab_tiles;
-        const int n0 = (is_vocab ? tile : tile - p.n_vocab_tiles) * 256 + static_cast<int>(rank) * 128;
+        const PairTile pt = pair_tile(tile, ncl, p.n_gate_tiles, n_tiles);
+        const bool is_vocab = pt.vocab;
+        const int n0 = pt.n0 + static_cast<int>(rank) * 128;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, p.err, abort_flag)) {
             ok = false;
@@ -629,7 +658,7 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = cid; ok && tile < n_tiles; tile += ncl) {
-        const bool is_vocab = tile < p.n_vocab_tiles;
+        const bool is_vocab = pair_tile(tile, ncl, p.n_gate_tiles, n_tiles).vocab;
         if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
@@ -693,8 +722,9 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = cid; tile < n_tiles; tile += ncl) {
-      const bool is_vocab = tile < p.n_vocab_tiles;
-      const int n0 = (is_vocab ? tile : tile - p.n_vocab_tiles) * 256;
+      const PairTile pt = pair_tile(tile, ncl, p.n_gate_tiles, n_tiles);
+      const bool is_vocab = pt.vocab;
+      const int n0 = pt.n0;
       if (!mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, p.err, abort_flag)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -709,11 +739,7 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
         if (is_vocab) {
           top16_offer32(top, rr, cbase, p.V - cbase);  // columns past V are not tokens
         } else {
-          float* dst = p.gate_out + static_cast<size_t>(grow) * p.r;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (cbase + j < p.r) dst[cbase + j] = 1.0f / (1.0f + expf(-__uint_as_float(rr[j])));
-          }
+          store_gate32(p.gate_out + static_cast<size_t>(grow) * p.r, rr, cbase, p.r);
         }
       }
       tc_fence_before();
