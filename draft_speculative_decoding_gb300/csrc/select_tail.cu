@@ -188,8 +188,29 @@ __device__ RowStat row_stat_warp(const TailLaunch& a, int row) {
 }
 
 // ------------------------------------------------------------------ top-16 merge
-// One warp merges nl <= 256 sorted lists of 16 into the top 16 (value desc, id asc): a
-// 16-round tournament, lane l watching the heads of lists l, l+32, ...
+// A float as an unsigned key with the same order (larger float -> larger key; -0 == +0).
+__device__ __forceinline__ uint32_t ord_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The lane holding the warp's best (value desc, id asc) candidate, among lanes with
+// `has`; ties on both (only possible for empty-list sentinels) go to the lowest lane.
+// Returns -1 when no lane has a candidate. Two single-instruction warp reductions.
+__device__ __forceinline__ int warp_best_lane(bool has, float v, int id) {
+  const uint32_t key = has ? ord_key(v) : 0u;
+  const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
+  if (mx == 0u) return -1;
+  const bool top = has && key == mx;
+  const uint32_t mid = __reduce_min_sync(0xffffffffu, top ? static_cast<uint32_t>(id) : 0xffffffffu);
+  const unsigned w = __ballot_sync(0xffffffffu, top && static_cast<uint32_t>(id) == mid);
+  return __ffs(w) - 1;
+}
+
+// One warp merges nl <= 256 sorted lists of 16 into the top 16 (value desc, id asc): lane l
+// watches the heads of lists l, l+32, ...; each of the 16 rounds takes the warp's best lane
+// head, and only the winning lane advances its list and rescans its heads. Ids are unique
+// across lists (the vocabulary tiles partition V), so (value, id) orders them totally.
 __device__ void merge_lists_warp(const float* sv, const int* si, int nl, float* outv, int* outi) {
   const int lane = threadIdx.x & 31;
   int head[8];
@@ -202,34 +223,49 @@ __device__ void merge_lists_warp(const float* sv, const int* si, int nl, float* 
     hv[s] = l < nl ? sv[l * kK] : -INFINITY;
     hi[s] = l < nl ? si[l * kK] : kIntMax;
   }
-  for (int k = 0; k < kK; ++k) {
-    float bv = -INFINITY;
-    int bi = kIntMax, bs = -1;
+  // this lane's best head (slot bs), kept across rounds until the lane wins
+  float bv = -INFINITY;
+  int bi = kIntMax, bs = -1;
 #pragma unroll
-    for (int s = 0; s < 8; ++s)
-      if (ranks_before(hv[s], hi[s], bv, bi)) {
-        bv = hv[s];
-        bi = hi[s];
-        bs = s;
-      }
-    const unsigned long long mine = bs >= 0 ? pack_key(bv, bi) : 0ull;
-    const unsigned long long best = warp_max_u64(mine);
-    if (best == 0ull) {  // fewer than 16 orderable candidates (e.g. NaN logits): sentinel
+  for (int s = 0; s < 8; ++s)
+    if (lane + 32 * s < nl && (bs < 0 || ranks_before(hv[s], hi[s], bv, bi))) {
+      bv = hv[s];
+      bi = hi[s];
+      bs = s;
+    }
+#pragma unroll 1
+  for (int k = 0; k < kK; ++k) {
+    const int wl = warp_best_lane(bs >= 0, bv, bi);
+    if (wl < 0) {  // fewer than 16 candidates in all (e.g. NaN logits): sentinel
       if (lane == 0) {
         outv[k] = -INFINITY;
         outi[k] = -1;
       }
-    } else if (bs >= 0 && mine == best) {
+      continue;
+    }
+    if (lane == wl) {
+      outv[k] = bv;
+      outi[k] = bi;
 #pragma unroll
       for (int s = 0; s < 8; ++s)
         if (s == bs) {
           const int l = lane + 32 * s;
           ++head[s];
-          hv[s] = head[s] < kK ? sv[l * kK + head[s]] : -INFINITY;
-          hi[s] = head[s] < kK ? si[l * kK + head[s]] : kIntMax;
+          const bool more = head[s] < kK;
+          hv[s] = more ? sv[l * kK + head[s]] : -INFINITY;
+          hi[s] = more ? si[l * kK + head[s]] : kIntMax;
+          if (!more) head[s] = kK + 1;  // exhausted
         }
-      outv[k] = bv;
-      outi[k] = bi;
+      bs = -1;
+      bv = -INFINITY;
+      bi = kIntMax;
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        if (lane + 32 * s < nl && head[s] < kK && (bs < 0 || ranks_before(hv[s], hi[s], bv, bi))) {
+          bv = hv[s];
+          bi = hi[s];
+          bs = s;
+        }
     }
   }
   __syncwarp();
@@ -316,11 +352,11 @@ __device__ float path_warp(const float* S, const int* ids, int P, int mode, int*
     // greedy: x_t = argmax_c S_t(x_{t-1}, c)
     int a = 0;
     float total = 0.f;
+#pragma unroll 1
     for (int p = 0; p < P; ++p) {
       const float v = act ? S[(p * kK + a) * kK + lane] : -INFINITY;
-      const unsigned long long key = act ? pack_key(v, ids[p * kK + lane]) : 0ull;
-      const unsigned long long best = warp_max_u64(key);
-      const int c = __ffs(__ballot_sync(0xffffffffu, act && key == best)) - 1;
+      int c = warp_best_lane(act, v, act ? ids[p * kK + lane] : kIntMax);
+      c = c < 0 ? 0 : c;  // no orderable score at all (NaN row): take candidate 0
       total += __shfl_sync(0xffffffffu, v, c);
       if (lane == 0) path_tok[p] = ids[p * kK + c];
       a = c;
@@ -331,6 +367,7 @@ __device__ float path_warp(const float* S, const int* ids, int P, int mode, int*
   // Viterbi: delta_1(c) = S_1(x0, c); delta_t(c) = max_a delta_{t-1}(a) + S_t(a, c)
   if (act) delta[lane] = S[lane];
   __syncwarp();
+#pragma unroll 1
   for (int p = 1; p < P; ++p) {
     float bv = -INFINITY;
     int ba = 0;
@@ -355,9 +392,8 @@ __device__ float path_warp(const float* S, const int* ids, int P, int mode, int*
     __syncwarp();
   }
   const float v = act ? delta[lane] : -INFINITY;
-  const unsigned long long key = act ? pack_key(v, ids[(P - 1) * kK + lane]) : 0ull;
-  const unsigned long long best = warp_max_u64(key);
-  const int c = __ffs(__ballot_sync(0xffffffffu, act && key == best)) - 1;
+  int c = warp_best_lane(act, v, act ? ids[(P - 1) * kK + lane] : kIntMax);
+  c = c < 0 ? 0 : c;
   const float score = __shfl_sync(0xffffffffu, v, c);
   if (lane == 0) {
     int cur = c;
