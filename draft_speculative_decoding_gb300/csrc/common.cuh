@@ -80,13 +80,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // kErrTimeout in *err and the CTA-wide abort flag) when the limit expires or another
 // role of the CTA has already aborted.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* err,
-                                                  volatile int* abort_flag) {
+                                                  volatile int* abort_flag,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(err, kErrTimeout);
       *abort_flag = 1;
       return false;

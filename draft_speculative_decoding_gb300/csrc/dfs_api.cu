@@ -177,6 +177,19 @@ int lmhead_cluster() {
 // Where the target-logit row statistics are computed: 1 = by the LM-head kernel's spare
 // warps (default), 0 = by the standalone reduction kernel before it. Read from DFS_Z_FUSED
 // on each call, for tuning; both do the same work.
+// Test hooks for the failure path, read on each call: DFS_DEBUG_WAIT_LIMIT_NS sets the limit
+// of the LM-head kernels' bounded waits (unset: 1 s); DFS_DEBUG_STALL_MMA=1 keeps their MMA
+// issuer idle, so that the producers' and the epilogue's waits run out.
+unsigned long long debug_wait_limit_ns() {
+  const char* s = std::getenv("DFS_DEBUG_WAIT_LIMIT_NS");
+  const long long v = s ? std::atoll(s) : 0;
+  return v > 0 ? static_cast<unsigned long long>(v) : 0ull;
+}
+int debug_stall_mma() {
+  const char* s = std::getenv("DFS_DEBUG_STALL_MMA");
+  return (s != nullptr && std::atoi(s) != 0) ? 1 : 0;
+}
+
 bool z_fused() {
   const char* s = std::getenv("DFS_Z_FUSED");
   return s == nullptr || std::atoi(s) != 0;
@@ -220,6 +233,8 @@ cudaError_t run_lmhead_kernels(const dfs_dims& d, const Layout& L, void* ws, con
     a.err = at<int>(ws, L.err);
     a.lmhead_variant = lmhead_variant_override();
     a.cluster = lmhead_cluster();
+    a.wait_limit_ns = debug_wait_limit_ns();
+    a.stall_mma = debug_stall_mma();
     if (Z != nullptr) {
       a.Z = Z;
       a.zdtype = d.zdtype;

@@ -32,6 +32,10 @@ struct LmheadLaunch {
                        // CTA stages half of the W tile); 4 = CTA pairs with per-CTA MMAs
                        // (the W tile multicast to both)
   int cluster;         // CTAs per cluster sharing hidden-row tiles by multicast (1, 2 or 4)
+  // Test hooks: the limit of every bounded wait (0: the default), and a switch that keeps the
+  // MMA issuer idle so that the other roles' waits run out and report DFS_ERR_TIMEOUT.
+  unsigned long long wait_limit_ns;
+  int stall_mma;
   // Target-logit row statistics computed by the kernel's spare warps (z_rows = 0: none).
   const void* Z;       // [z_rows, V]
   int zdtype, z_rows, z_nchunk;

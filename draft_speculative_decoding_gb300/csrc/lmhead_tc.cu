@@ -67,6 +67,8 @@ struct LmheadParams {
   float* zsum;
   int* zero_ptr;
   int zero_count;
+  unsigned long long wait_limit_ns;  // every bounded wait gives up after this long
+  int stall_mma;                     // test hook: the MMA issuer stays idle
 };
 
 template <int MT, int NT, int NBUF, int SW, int SH, int CL, int RS>
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
         // padding tiles load boxes wholly past the vocabulary: zeros
         const int n0 = is_pad ? ((p.V + 63) / 64) * 64 : (is_vocab ? tile : tile - p.n_vocab_tiles) * NT;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&wempty[stage]), phase ^ 1, p.err, abort_flag)) {
+          if (!mbar_wait_bounded(smem_u32(&wempty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -307,7 +309,7 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
       // last releases have arrived on its barriers.
       if (RS && ok) {
         for (int i = 0; i < SW; ++i) {
-          if (!mbar_wait_bounded(smem_u32(&wempty[stage]), phase ^ 1, p.err, abort_flag)) break;
+          if (!mbar_wait_bounded(smem_u32(&wempty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) break;
           if (++stage == SW) {
             stage = 0;
             phase ^= 1;
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
       for (int sup = cid; ok && sup < n_loop; sup += ncl) {
         const int tile = RS ? sup : sup * CL + rank;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&hempty[stage]), phase ^ 1, p.err, abort_flag)) {
+          if (!mbar_wait_bounded(smem_u32(&hempty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
       // cluster (their releases arrive on this CTA's barriers).
       if (CL > 1 && !RS && ok) {
         for (int i = 0; i < SH; ++i) {
-          if (!mbar_wait_bounded(smem_u32(&hempty[stage]), phase ^ 1, p.err, abort_flag)) break;
+          if (!mbar_wait_bounded(smem_u32(&hempty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) break;
           if (++stage == SH) {
             stage = 0;
             phase ^= 1;
@@ -361,7 +363,7 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && !p.stall_mma) {
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t kIdescVocab = idesc_bf16_f32(NT, true);
       constexpr uint32_t kIdescGate = idesc_bf16_f32(NT, false);
@@ -373,12 +375,12 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
       for (int sup = cid; ok && sup < n_loop; sup += ncl) {
         const int tile = RS ? sup : sup * CL + rank;
         const bool is_vocab = tile < p.n_vocab_tiles || tile >= n_tiles;
-        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, abort_flag)) break;
+        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&wfull[ws]), wph, p.err, abort_flag) ||
-              !mbar_wait_bounded(smem_u32(&hfull[hs]), hph, p.err, abort_flag)) {
+          if (!mbar_wait_bounded(smem_u32(&wfull[ws]), wph, p.err, abort_flag, p.wait_limit_ns) ||
+              !mbar_wait_bounded(smem_u32(&hfull[hs]), hph, p.err, abort_flag, p.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
       const bool is_pad = tile >= n_tiles;
       const bool is_vocab = tile < p.n_vocab_tiles;
       const int n0 = (is_vocab ? tile : tile - p.n_vocab_tiles) * NT;
-      if (!mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, p.err, abort_flag)) break;
+      if (!mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, p.err, abort_flag, p.wait_limit_ns)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * Cfg::kAccCols + mt * NT);
@@ -614,7 +616,7 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
         const bool is_vocab = pt.vocab;
         const int n0 = pt.n0 + static_cast<int>(rank) * 128;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, p.err, abort_flag)) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -639,7 +641,7 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
       // only after they have landed on its barriers.
       if (ok) {
         for (int i = 0; i < S; ++i) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, p.err, abort_flag)) break;
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) break;
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
@@ -648,7 +650,7 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && leader) {
+    if (lane == 0 && leader && !p.stall_mma) {
       // ------------------------------------------------------- pair MMA issuer (leader)
       constexpr uint32_t kIdescVocab = idesc_bf16_f32(256, true, 256);
       constexpr uint32_t kIdescGate = idesc_bf16_f32(256, false, 256);
@@ -659,11 +661,11 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
       bool ok = true;
       for (int tile = cid; ok && tile < n_tiles; tile += ncl) {
         const bool is_vocab = pair_tile(tile, ncl, p.n_gate_tiles, n_tiles).vocab;
-        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, abort_flag)) break;
+        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, p.err, abort_flag)) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, p.err, abort_flag, p.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -725,7 +727,7 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
       const PairTile pt = pair_tile(tile, ncl, p.n_gate_tiles, n_tiles);
       const bool is_vocab = pt.vocab;
       const int n0 = pt.n0;
-      if (!mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, p.err, abort_flag)) break;
+      if (!mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, p.err, abort_flag, p.wait_limit_ns)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * Cfg::kAccCols);
@@ -898,6 +900,8 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
   prm.part_idx = a.part_idx;
   prm.gate_out = a.gate_out;
   prm.err = a.err;
+  prm.wait_limit_ns = a.wait_limit_ns > 0 ? a.wait_limit_ns : kWaitLimitNs;
+  prm.stall_mma = a.stall_mma;
   for (int row0 = 0; row0 < a.rows_total; row0 += 256) {
     prm.row0 = row0;
     // the target-logit statistics and the counter reset ride on the first launch only
