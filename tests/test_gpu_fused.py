@@ -23,6 +23,14 @@ SMALL = [
     wl.TINY.with_(name="fused_groups", dtype="bf16", B=33, L=9, V=2600, d=128, r=64, seed=33),
     wl.TINY.with_(name="fused_L16", dtype="bf16", B=6, L=16, V=8192, d=192, r=32, seed=34,
                   agreement=("top1_linear", 0.95, 0.6)),
+    # CTA-pair LM head at its edges: one row past a single M tile; exactly 256 rows with two
+    # gate tiles (r = 512) placed among the first round; fewer vocabulary tiles than pairs
+    wl.TINY.with_(name="pairs_129rows", dtype="bf16", B=43, L=3, V=3000, d=128, r=64, seed=35),
+    wl.TINY.with_(name="pairs_256rows_r512", dtype="bf16", B=32, L=8, V=5000, d=192, r=512,
+                  seed=36, zipf=True),
+    wl.TINY.with_(name="pairs_few_tiles", dtype="bf16", B=20, L=8, V=1040, d=64, r=256, seed=37),
+    wl.TINY.with_(name="pairs_L16", dtype="bf16", B=16, L=16, V=6000, d=256, r=256, seed=38,
+                  agreement=("top1_linear", 0.85, 0.55)),
 ]
 
 
