@@ -62,6 +62,11 @@ def _load():
                 "orc_verify_greedy": ([i32, P, i32, i64, P, P, P], i32),
                 "orc_verify_sampling": ([i32, P, i32, i64, P, f64, u64, i64, P, P, P, P], i32),
                 "orc_verify_sampling_many": ([i32, P, i32, i64, P, f64, u64, i64, i64, i32, P, P], i32),
+                "orc_path_sample": ([i32, i32, P, P, f64, u64, i64, P, P, P, P, P], i32),
+                "orc_verify_proposal": ([i32, P, i32, i64, P, P, P, P, i32, f64, u64, i64, P, P,
+                                         P, P], i32),
+                "orc_sample_verify_many": ([i32, P, i32, i64, P, P, i32, f64, u64, i64, i64, i32,
+                                            P, P, P], i32),
                 "orc_philox4x64": ([P, P, P], None),
                 "orc_select_verify": ([i32, i32, P, P, P, P, P, P, P, i64, i32, i64, i64, i64,
                                        i32, i32, f64, u64, P, i64, i32] + [P] * 12, i32),
@@ -216,6 +221,61 @@ def verify_sampling_many(Z, path, T: float, seed0: int, n: int, b: int = 0,
                                             nthreads or default_threads(), _ptr(out), _ptr(acc)),
            "verify_sampling_many")
     return out, acc
+
+
+def path_sample(S, ids, T: float, seed: int, b: int = 0):
+    """Sampled traversal of one request's lattice S [P, K, K], ids [P, K]: (path [P],
+    pidx [P], q [P, K], score, margin)."""
+    S = _c(S, np.float64)
+    P, K, _ = S.shape
+    ids = _c(ids, np.int32)
+    path = np.empty(P, np.int32)
+    pidx = np.empty(P, np.int32)
+    q = np.empty((P, K), np.float64)
+    sc = np.zeros(1, np.float64)
+    mg = np.zeros(1, np.float64)
+    _check(_load().orc_path_sample(P, K, _ptr(S), _ptr(ids), float(T),
+                                   ctypes.c_uint64(seed & (2**64 - 1)), int(b), _ptr(path),
+                                   _ptr(pidx), _ptr(q), _ptr(sc), _ptr(mg)), "path_sample")
+    return path, pidx, q, float(sc[0]), float(mg[0])
+
+
+def verify_proposal(Z, path, cand, q, pidx, T: float, seed: int, b: int = 0):
+    """Z [L, V]; the proposal's candidates cand [P, K], distributions q [P, K] and drawn
+    indices pidx [P]: (out, accept_len, acc_margin, gumbel_margin)."""
+    Z = _c(Z)
+    L, V = Z.shape
+    cand = _c(cand, np.int32)
+    K = cand.shape[1]
+    q = _c(q, np.float64)
+    out = np.empty(L, np.int32)
+    acc = np.zeros(1, np.int32)
+    am = np.zeros(1, np.float64)
+    gm = np.full(1, np.inf, np.float64)
+    _check(_load().orc_verify_proposal(_dtype_code(Z), _ptr(Z), L, V, _ptr(_c(path, np.int32)),
+                                       _ptr(cand), _ptr(q), _ptr(_c(pidx, np.int32)), K, float(T),
+                                       ctypes.c_uint64(seed & (2**64 - 1)), int(b), _ptr(out),
+                                       _ptr(acc), _ptr(am), _ptr(gm)), "verify_proposal")
+    return out, int(acc[0]), float(am[0]), float(gm[0])
+
+
+def sample_verify_many(Z, S, ids, T: float, seed0: int, n: int, b: int = 0,
+                       nthreads: int | None = None):
+    """Sampled traversal + its verification for seeds seed0..seed0+n-1 on a fixed lattice:
+    (paths [n, P], out [n, L], accept_len [n])."""
+    Z = _c(Z)
+    L, V = Z.shape
+    S = _c(S, np.float64)
+    ids = _c(ids, np.int32)
+    K = ids.shape[1]
+    paths = np.empty((n, L - 1), np.int32)
+    out = np.empty((n, L), np.int32)
+    acc = np.empty(n, np.int32)
+    _check(_load().orc_sample_verify_many(_dtype_code(Z), _ptr(Z), L, V, _ptr(S), _ptr(ids), K,
+                                          float(T), ctypes.c_uint64(seed0), int(n), int(b),
+                                          nthreads or default_threads(), _ptr(paths), _ptr(out),
+                                          _ptr(acc)), "sample_verify_many")
+    return paths, out, acc
 
 
 def philox4x64(ctr, key) -> np.ndarray:

@@ -110,6 +110,7 @@ inline double u01(uint64_t x) {
  *   accept  : counter (0, t, b, 0), word 0           -- position t = 1..L-1
  *   chunk   : counter (0, t, b, 2), word 0           -- the redraw's chunk choice
  *   gumbel  : counter (v >> 2, t, b, 1), word v & 3  -- the redraw within the chunk
+ *   path    : counter (0, t, b, 3), word 0           -- the sampled path's draw at t
  * The redraw from row t-1 uses position t; the bonus row L-1 uses t = L. */
 double uniform_counter(uint64_t seed, int64_t b, int t, uint64_t idx, uint64_t stream, int word) {
   uint64_t ctr[4] = {idx, static_cast<uint64_t>(t), static_cast<uint64_t>(b), stream};
@@ -126,6 +127,8 @@ double uniform_gumbel(uint64_t seed, int64_t b, int t, int64_t v) {
 }
 
 double uniform_chunk(uint64_t seed, int64_t b, int t) { return uniform_counter(seed, b, t, 0, 2, 0); }
+
+double uniform_path(uint64_t seed, int64_t b, int t) { return uniform_counter(seed, b, t, 0, 3, 0); }
 
 /* Tokens per chunk of the two-stage redraw. */
 const int64_t kRedrawChunk = 4096;
@@ -199,6 +202,59 @@ int64_t redraw(const void* Z, int zdtype, int64_t off, int64_t V, double T, uint
                                   &gmargin);
   *margin = std::min(cmargin, gmargin);
   return y;
+}
+
+/* An exact draw from the residual r(v) = max(0, p(v) - q(v)) renormalised, with
+ * p = softmax(z/T) over the row and q a proposal that is nonzero only on the K listed
+ * candidates (cand[k] with probability qv[k]); K = 0 draws from p itself. The same two
+ * stages as redraw(): a chunk by its residual mass, then the Gumbel-max over the chunk of
+ * log r(v) + G_v. For a proposal that puts all its mass on one token this is redraw()
+ * with that token excluded (the keys differ from redraw()'s by the constant log-sum-exp
+ * of the row). */
+int64_t redraw_residual(const void* Z, int zdtype, int64_t off, int64_t V, double T, uint64_t seed,
+                        int64_t b, int t, const int32_t* cand, const double* qv, int K,
+                        double* margin) {
+  const double lse = row_lse(Z, zdtype, off, V, T);
+  auto resid = [&](int64_t v) {  // r(v), and whether v is a listed candidate
+    const double pv = std::exp(widen(Z, zdtype, off + v) / T - lse);
+    for (int k = 0; k < K; ++k)
+      if (cand[k] == v) return std::max(0.0, pv - qv[k]);
+    return pv;
+  };
+  const int64_t nchunk = (V + kRedrawChunk - 1) / kRedrawChunk;
+  std::vector<double> mass(nchunk, 0.0);
+  for (int64_t c = 0; c < nchunk; ++c)
+    for (int64_t v = c * kRedrawChunk; v < std::min(V, (c + 1) * kRedrawChunk); ++v)
+      mass[c] += resid(v);
+  double total = 0.0;
+  for (int64_t c = 0; c < nchunk; ++c) total += mass[c];
+  const double target = uniform_chunk(seed, b, t) * total;
+  int64_t pick = -1, last_nonzero = 0;
+  double cum = 0.0, cmargin = kInf;
+  for (int64_t c = 0; c < nchunk; ++c) {
+    cum += mass[c];
+    if (mass[c] > 0.0) last_nonzero = c;
+    if (c + 1 < nchunk) cmargin = std::min(cmargin, std::fabs(cum - target) / total);
+    if (pick < 0 && cum > target) pick = c;
+  }
+  if (pick < 0) pick = last_nonzero;
+  int64_t best = -1;
+  double bk = -kInf, second = -kInf;
+  for (int64_t v = pick * kRedrawChunk; v < std::min(V, (pick + 1) * kRedrawChunk); ++v) {
+    const double rv = resid(v);
+    if (!(rv > 0.0)) continue;
+    const double key = std::log(rv) - std::log(-std::log(uniform_gumbel(seed, b, t, v)));
+    if (best < 0 || key > bk) {
+      second = bk;
+      bk = key;
+      best = v;
+    } else {
+      second = std::max(second, key);
+    }
+  }
+  const double gmargin = (second == -kInf) ? kInf : rel(bk - second, bk);
+  *margin = std::min(cmargin, gmargin);
+  return best;
 }
 
 }  // namespace
@@ -477,6 +533,118 @@ int orc_verify_sampling_many(int zdtype, const void* Z, int L, int64_t V, const 
   return bad ? -1 : 0;
 }
 
+/* Sampled traversal, [Blog] §"A lightweight path selector": the same left-to-right
+ * traversal from the last verified token as the greedy one, with each successor drawn from
+ * the same scores instead of taken as the best: q_t(c) = softmax_c(S_t(x_{t-1}, c) / T)
+ * over position t's K candidates, x_t drawn by one uniform against the cumulative q in
+ * candidate order (if rounding leaves no candidate above it, the last one with mass).
+ * Outputs the path, its candidate indices, q [P][K] (each position's distribution given
+ * the drawn predecessor), the summed scores and the smallest distance of a uniform to a
+ * cumulative boundary. T > 0. */
+int orc_path_sample(int P, int K, const double* S, const int32_t* ids, double T, uint64_t seed,
+                    int64_t b, int32_t* path, int32_t* pidx, double* q, double* score,
+                    double* margin) {
+  if (P < 1 || K < 1 || !(T > 0.0)) return -1;
+  int a = 0;
+  double total = 0.0, mg = kInf;
+  for (int p = 0; p < P; ++p) {
+    const double* row = S + (static_cast<int64_t>(p) * K + a) * K;
+    double m = -kInf;
+    for (int c = 0; c < K; ++c) m = std::max(m, row[c] / T);
+    double z = 0.0;
+    for (int c = 0; c < K; ++c) z += std::exp(row[c] / T - m);
+    double* qp = q + static_cast<int64_t>(p) * K;
+    for (int c = 0; c < K; ++c) qp[c] = std::exp(row[c] / T - m) / z;
+    const double u = uniform_path(seed, b, p + 1);
+    int pick = -1, last = 0;
+    double cum = 0.0;
+    for (int c = 0; c < K; ++c) {
+      cum += qp[c];
+      if (qp[c] > 0.0) last = c;
+      if (c + 1 < K) mg = std::min(mg, std::fabs(cum - u));
+      if (pick < 0 && cum > u) pick = c;
+    }
+    if (pick < 0) pick = last;
+    path[p] = ids[static_cast<int64_t>(p) * K + pick];
+    pidx[p] = pick;
+    total += row[pick];
+    a = pick;
+  }
+  *score = total;
+  *margin = mg;
+  return 0;
+}
+
+/* Speculative-sampling verification of a sampled proposal, [Blog] §"A lightweight path
+ * selector" (rejection sampling recovers the exact target distribution): for t = 1..L-1,
+ * with p = softmax(Z[t-1]/T) and q = q_t (K candidates cand[t-1][*], the drawn one at index
+ * pidx[t-1]): accept x_t when U < p(x_t) / q(x_t); on the first rejection emit a draw from
+ * the residual max(0, p - q) renormalised and stop (accept_len = t); when all are accepted
+ * emit a bonus draw from p_{L-1} (accept_len = L). Each emitted token is distributed as
+ * p given the tokens before it (Leviathan, Kalman, Matias, ICML 2023; Chen et al. 2023).
+ * A proposal that puts all its mass on x_t gives orc_verify_sampling. */
+int orc_verify_proposal(int zdtype, const void* Z, int L, int64_t V, const int32_t* path,
+                        const int32_t* cand, const double* q, const int32_t* pidx, int K, double T,
+                        uint64_t seed, int64_t b, int32_t* out, int32_t* accept_len,
+                        double* acc_margin, double* gum_margin) {
+  if (L < 2 || V < 2 || K < 1 || !(T > 0.0)) return -1;
+  for (int i = 0; i < L; ++i) out[i] = -1;
+  double am = kInf;
+  for (int t = 1; t < L; ++t) {
+    const int64_t off = static_cast<int64_t>(t - 1) * V;
+    const int64_t x = path[t - 1];
+    const double p = std::exp(widen(Z, zdtype, off + x) / T - row_lse(Z, zdtype, off, V, T));
+    const double qx = q[static_cast<int64_t>(t - 1) * K + pidx[t - 1]];
+    const double ratio = p / qx;
+    const double u = uniform_accept(seed, b, t);
+    am = std::min(am, std::fabs(u - ratio) / ratio);
+    if (u < ratio) {
+      out[t - 1] = static_cast<int32_t>(x);
+      continue;
+    }
+    out[t - 1] = static_cast<int32_t>(redraw_residual(Z, zdtype, off, V, T, seed, b, t,
+                                                      cand + static_cast<int64_t>(t - 1) * K,
+                                                      q + static_cast<int64_t>(t - 1) * K, K,
+                                                      gum_margin));
+    *accept_len = t;
+    *acc_margin = am;
+    return 0;
+  }
+  const int64_t off = static_cast<int64_t>(L - 1) * V;
+  out[L - 1] = static_cast<int32_t>(
+      redraw_residual(Z, zdtype, off, V, T, seed, b, L, nullptr, nullptr, 0, gum_margin));
+  *accept_len = L;
+  *acc_margin = am;
+  return 0;
+}
+
+/* The sampled traversal and its verification run once per seed in [seed0, seed0 + n) on
+ * a fixed lattice (S [P][K][K], ids [P][K]) and target rows Z [L][V], for the distribution
+ * tests: paths [n][P], out [n][L], accept_len [n]. */
+int orc_sample_verify_many(int zdtype, const void* Z, int L, int64_t V, const double* S,
+                           const int32_t* ids, int K, double T, uint64_t seed0, int64_t n,
+                           int64_t b, int nthreads, int32_t* paths, int32_t* out,
+                           int32_t* accept_len) {
+  if (L < 2 || V < 2 || K < 1 || !(T > 0.0) || n < 0) return -1;
+  const int P = L - 1;
+  int bad = 0;
+  if (nthreads <= 0) nthreads = 1;
+#pragma omp parallel for schedule(static) num_threads(nthreads) reduction(| : bad)
+  for (int64_t i = 0; i < n; ++i) {
+    std::vector<int32_t> pidx(P);
+    std::vector<double> q(static_cast<size_t>(P) * K);
+    double score, pm, am, gm;
+    const uint64_t seed = seed0 + static_cast<uint64_t>(i);
+    int rc = orc_path_sample(P, K, S, ids, T, seed, b, paths + i * P, pidx.data(), q.data(),
+                             &score, &pm);
+    if (rc == 0)
+      rc = orc_verify_proposal(zdtype, Z, L, V, paths + i * P, ids, q.data(), pidx.data(), K, T,
+                               seed, b, out + i * L, accept_len + i, &am, &gm);
+    bad |= (rc != 0);
+  }
+  return bad ? -1 : 0;
+}
+
 /* Raw Philox4x64-10 block, exposed for the library pin. */
 void orc_philox4x64(const uint64_t* ctr, const uint64_t* key, uint64_t* out) {
   philox4x64_10(ctr, key, out);
@@ -486,8 +654,9 @@ void orc_philox4x64(const uint64_t* ctr, const uint64_t* key, uint64_t* out) {
  * stages above in the pages' order: logits -> keep top-K -> gate -> pair
  * scores -> path -> verify. Inputs: h [B][L][d], W [d][V], Wg [r][d],
  * A and Bt [V][r], x0 [B], Z [B][L][V]. Outputs are indexed by list position
- * q = 0..nreq-1. path_mode 0 = greedy traversal, 1 = Viterbi; T <= 0 selects
- * greedy verification. */
+ * q = 0..nreq-1. path_mode 0 = greedy traversal, 1 = Viterbi, 2 = sampled traversal
+ * (verified against its own proposal); T <= 0 selects greedy verification (and, for
+ * path_mode 2, the greedy traversal). */
 int orc_select_verify(int dtype, int zdtype, const void* h, const void* W, const void* Wg,
                       const void* A, const void* Bt, const int32_t* x0, const void* Z,
                       int64_t B, int L, int64_t V, int64_t d, int64_t r, int K, int path_mode,
@@ -512,16 +681,27 @@ int orc_select_verify(int dtype, int zdtype, const void* h, const void* W, const
     if (rc == 0) rc = orc_topk(u.data(), P, V, K, ids, U, topk_gap + q * P);
     if (rc == 0) rc = orc_gate(dtype, h, Wg, d, r, rows.data(), P, g);
     if (rc == 0) rc = orc_pair_scores(dtype, A, Bt, r, P, K, ids, U, g, x0[b], Sq);
-    if (rc == 0)
-      rc = (path_mode == 1)
-               ? orc_path_viterbi(P, K, Sq, ids, path + q * P, pidx.data(), path_score + q, path_margin + q)
-               : orc_path_greedy(P, K, Sq, ids, path + q * P, pidx.data(), path_score + q, path_margin + q);
+    const bool sampled = path_mode == 2 && T > 0.0;
+    std::vector<double> qprop(static_cast<size_t>(P) * K);
+    if (rc == 0) {
+      if (sampled)
+        rc = orc_path_sample(P, K, Sq, ids, T, seed, b, path + q * P, pidx.data(), qprop.data(),
+                             path_score + q, path_margin + q);
+      else if (path_mode == 1)
+        rc = orc_path_viterbi(P, K, Sq, ids, path + q * P, pidx.data(), path_score + q, path_margin + q);
+      else
+        rc = orc_path_greedy(P, K, Sq, ids, path + q * P, pidx.data(), path_score + q, path_margin + q);
+    }
     if (rc != 0) return rc;
     const char* zb = static_cast<const char*>(Z) +
                      b * static_cast<int64_t>(L) * V * (zdtype == ORC_BF16 ? 2 : 4);
     acc_margin[q] = kInf;
     gum_margin[q] = kInf;
-    if (T > 0.0)
+    if (sampled)
+      rc = orc_verify_proposal(zdtype, zb, L, V, path + q * P, ids, qprop.data(), pidx.data(), K,
+                               T, seed, b, out + q * L, accept_len + q, acc_margin + q,
+                               gum_margin + q);
+    else if (T > 0.0)
       rc = orc_verify_sampling(zdtype, zb, L, V, path + q * P, T, seed, b, out + q * L,
                                accept_len + q, acc_margin + q, gum_margin + q);
     else
