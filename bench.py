@@ -185,15 +185,16 @@ def run_ours(args):
     mode = binding.DFS_PATH_GREEDY if args.path_mode == "greedy" else binding.DFS_PATH_VITERBI
     stream = torch.cuda.current_stream()
 
-    def step(i, T, h=None, Z=None, x0=None):
+    def step(i, T, h=None, Z=None, x0=None, path_mode=None):
         binding.dfs_select_verify(dims, hs[i % nrot] if h is None else h, data["W"], data["Wg"],
                                   data["A"], data["Bt"], data["x0"] if x0 is None else x0,
-                                  Zs[i % nrot] if Z is None else Z, mode, T, spec.seed + i, ws,
+                                  Zs[i % nrot] if Z is None else Z,
+                                  mode if path_mode is None else path_mode, T, spec.seed + i, ws,
                                   outputs=outs, stream=stream)
 
-    def timed(T, K, W, trace=False, clocks=None):
+    def timed(T, K, W, trace=False, clocks=None, path_mode=None):
         for i in range(W):
-            step(i, T)
+            step(i, T, path_mode=path_mode)
         torch.cuda.synchronize()
         replicas.barrier()
         torch.cuda.synchronize()
@@ -211,7 +212,7 @@ def run_ours(args):
         for i in range(K):
             if trace:
                 binding.dfs_set_trace_events(*tr[i])
-            step(W + i, T)
+            step(W + i, T, path_mode=path_mode)
         e1.record(stream)
         n1 = binding.dfs_launch_count()
         torch.cuda.synchronize()
@@ -239,6 +240,11 @@ def run_ours(args):
     accept = outs[2].float().mean().item()
     ms_samp, _, _ = timed(args.sampling_temperature, max(10, args.steps // 2), args.warmup)
     accept_samp = outs[2].float().mean().item()
+    # the sampled traversal (each successor drawn from the scores) verified against its own
+    # proposal
+    ms_prop, _, _ = timed(args.sampling_temperature, max(10, args.steps // 2), args.warmup,
+                          path_mode=binding.DFS_PATH_SAMPLE)
+    accept_prop = outs[2].float().mean().item()
 
     # end to end through the public API: every step copies its inputs (h, Z, x0) from pinned
     # host memory and reads its results back to pinned host memory. As a serving loop would,
@@ -307,6 +313,7 @@ def run_ours(args):
     value = replicas.job_throughput(spec.B * args.steps, ms_greedy * args.steps / 1e3)
     ms_max = replicas.max_over_ranks(ms_greedy)
     value_samp = replicas.job_throughput(spec.B, ms_samp / 1e3)
+    value_prop = replicas.job_throughput(spec.B, ms_prop / 1e3)
     value_e2e = replicas.job_throughput(spec.B, ms_e2e / 1e3)
     lm_max = replicas.max_over_ranks(lm_ms)
 
@@ -358,7 +365,11 @@ def run_ours(args):
                     "overlap": "step i+1's inputs copied on two copy streams during step i"},
             "sampling": {"temperature": args.sampling_temperature, "value": round(value_samp, 1),
                          "unit": UNIT, "ms_per_step": round(ms_samp, 4),
-                         "mean_accept_len": round(accept_samp, 3)},
+                         "mean_accept_len": round(accept_samp, 3),
+                         "path": args.path_mode,
+                         "sampled_path": {"value": round(value_prop, 1), "unit": UNIT,
+                                          "ms_per_step": round(ms_prop, 4),
+                                          "mean_accept_len": round(accept_prop, 3)}},
             "mean_accept_len": round(accept, 3),
             "gpu_launches": launches,
             "clocks": clk,

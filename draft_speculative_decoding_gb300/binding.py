@@ -18,7 +18,7 @@ from . import build as _build
 DFS_OK, DFS_ERR_INVALID, DFS_ERR_UNSUPPORTED, DFS_ERR_WORKSPACE, DFS_ERR_CUDA, DFS_ERR_TIMEOUT = \
     0, -1, -2, -3, -4, -5
 DFS_BF16, DFS_FP32 = 0, 1
-DFS_PATH_GREEDY, DFS_PATH_VITERBI = 0, 1
+DFS_PATH_GREEDY, DFS_PATH_VITERBI, DFS_PATH_SAMPLE = 0, 1, 2
 K = 16
 
 # Every symbol include/dfs.h declares, with its ctypes signature.

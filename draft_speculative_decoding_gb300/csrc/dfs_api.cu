@@ -438,7 +438,9 @@ int dfs_select_verify(const dfs_dims* dims, const void* hidden, const void* W_vo
   Layout L;
   int rc = prepare(dims, ws, ws_bytes, &L);
   if (rc != DFS_OK) return rc;
-  if (path_mode != DFS_PATH_GREEDY && path_mode != DFS_PATH_VITERBI) return DFS_ERR_INVALID;
+  if (path_mode != DFS_PATH_GREEDY && path_mode != DFS_PATH_VITERBI &&
+      path_mode != DFS_PATH_SAMPLE)
+    return DFS_ERR_INVALID;
   if (!(temperature >= 0.f) || temperature != temperature) return DFS_ERR_INVALID;
   if ((rc = check_ptrs({hidden, W_vocab, W_g, A, Btab, last_verified, target_logits, path,
                         out_tokens, accept_len},

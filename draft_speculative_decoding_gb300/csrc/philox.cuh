@@ -50,4 +50,12 @@ __device__ __forceinline__ float uniform_chunk(uint64_t seed, int b, int t) {
   return u01_from_word(c[0]);
 }
 
+// Path-draw uniform of the sampled traversal at draft position t of request b: counter
+// (0, t, b, 3), word 0.
+__device__ __forceinline__ float uniform_path(uint64_t seed, int b, int t) {
+  uint64_t c[4] = {0ull, static_cast<uint64_t>(t), static_cast<uint64_t>(b), 3ull};
+  philox4x64_10(c, seed, 0ull);
+  return u01_from_word(c[0]);
+}
+
 }  // namespace dfs

@@ -342,6 +342,52 @@ __device__ float pair_scores_block(const TailLaunch& a, float* P, float* Q, cons
 }
 
 // ------------------------------------------------------------------ path
+// Sampled traversal (mode 2), one warp: from the last verified token, x_t is drawn from
+// q_t(c) = softmax_c(S_t(x_{t-1}, c) * inv_T) over the 16 candidates by one uniform (Philox
+// stream 3) against the cumulative q in candidate order; if rounding leaves no candidate
+// above it, the last one with mass. Writes path_tok[P], pidx[P] (the drawn candidate
+// indices) and q[P][16] (each position's distribution given the drawn predecessor), all in
+// shared memory; returns the summed scores of the drawn path in every lane.
+__device__ float path_sample_warp(const float* S, const int* ids, int P, float inv_T,
+                                  uint64_t seed, int b, int* path_tok, int* pidx, float* q) {
+  const int lane = threadIdx.x & 31;
+  const bool act = lane < kK;
+  int a = 0;
+  float total = 0.f;
+#pragma unroll 1
+  for (int p = 0; p < P; ++p) {
+    const float s = act ? S[(p * kK + a) * kK + lane] : -INFINITY;
+    const float v = s * inv_T;
+    float m = v;
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const float e = act ? expf(v - m) : 0.f;
+    float z = e;
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    const float qc = e / z;
+    float cum = qc;  // inclusive prefix sum over lanes 0..15
+#pragma unroll
+    for (int off = 1; off < kK; off <<= 1) {
+      const float o = __shfl_up_sync(0xffffffffu, cum, off);
+      if (lane >= off) cum += o;
+    }
+    const float u = uniform_path(seed, b, p + 1);
+    const unsigned above = __ballot_sync(0xffffffffu, act && cum > u);
+    const unsigned mass = __ballot_sync(0xffffffffu, act && qc > 0.f);
+    const int c = above ? __ffs(above) - 1 : (mass ? 31 - __clz(mass) : 0);
+    if (act) q[p * kK + lane] = qc;
+    total += __shfl_sync(0xffffffffu, s, c);
+    if (lane == 0) {
+      path_tok[p] = ids[p * kK + c];
+      pidx[p] = c;
+    }
+    a = c;
+  }
+  __syncwarp();
+  return total;
+}
+
 // One warp; S [P][16][16], ids [P][16] and delta [16] in shared memory. Writes
 // path_tok[P] (shared) and returns the path score in every lane.
 __device__ float path_warp(const float* S, const int* ids, int P, int mode, int* path_tok,
@@ -413,13 +459,24 @@ struct VerifySmem {
   int info[4];
   float mass[kMaxZChunks];
   unsigned long long gk[kTailThreads / 32];
+  // sampled proposals: the rejected position's candidates in the chosen chunk
+  uint32_t inchunk[kZChunk / 32];  // bit j: token lo + j is a candidate
+  int cand[kK];                    // candidate ids
+  float cadj[kK];                  // log(max(0, 1 - q/p)) added to the candidate's key
 };
 
 // Verification of request b given its path (shared memory), by the whole block: row
 // statistics (one warp per row), the acceptance tests of all positions in parallel (one lane
 // each), then for T > 0 the redraw: a chunk of the row chosen by its residual mass, and the
 // Gumbel-max inside it.
-__device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, VerifySmem& vs) {
+// With a sampled proposal (prop_q != nullptr: q[P][16] over the candidates cand[P][16], the
+// drawn one at pidx[t-1]) a draft is accepted when U < p(x_t) / q(x_t), and the redraw is
+// from the residual max(0, p - q): a chunk's mass loses min(p, q) of each candidate in it,
+// and a candidate's Gumbel key gains log(max(0, 1 - q/p)). Without one the proposal is the
+// path itself (q = 1 on x_t).
+__device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, VerifySmem& vs,
+                             const float* prop_q = nullptr, const int* prop_cand = nullptr,
+                             const int* prop_pidx = nullptr) {
   const int L = a.L, P = L - 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool soft = a.T > 0.f;
@@ -447,7 +504,8 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
                                  : -INFINITY;
         vs.zx[lane] = z;
         const float p = expf((z - vs.rm[lane]) * inv_T - vs.rl[lane]);
-        ok = uniform_accept(a.seed, b, lane + 1) < p;
+        const float qx = prop_q ? prop_q[lane * kK + prop_pidx[lane]] : 1.0f;
+        ok = uniform_accept(a.seed, b, lane + 1) < p / qx;
       }
     }
     const unsigned fail = __ballot_sync(0xffffffffu, lane < P && !ok);
@@ -464,17 +522,48 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
   // redraw from row n (the rejected position's row, or the bonus row L-1 when n = P), with
   // the rejected proposal removed; the draw's counter position is n + 1
   const int n = vs.info[0];
-  const int excl = n < P ? path_tok[n] : -1;
+  const bool sampled = prop_q != nullptr && n < P;  // residual against a sampled proposal
+  const int excl = (n < P && !sampled) ? path_tok[n] : -1;
   const size_t grow = static_cast<size_t>(b) * L + n;
   if (warp == 0) {
     const float M = vs.rm[n];
     const bool ex_in = excl >= 0 && excl < a.V;
     const float ex_mass = ex_in ? expf((vs.zx[n] - M) * inv_T) : 0.f;
+    // sampled: mass each candidate takes out of its chunk, min(p, q) on the chunk scale
+    // (unnormalised exp((z - M)/T), whose row total is exp(rl)); lane k holds candidate k
+    int ck = -1;
+    float take = 0.f, cadj = 0.f;
+    if (sampled && lane < kK) {
+      ck = prop_cand[n * kK + lane];
+      const float qk = prop_q[n * kK + lane];
+      if (ck >= 0 && ck < a.V) {
+        const float zk = load1(a.Z, is_bf16, grow * a.V + ck);
+        const float pk = expf((zk - M) * inv_T - vs.rl[n]);
+        take = fminf(pk, qk) * expf(vs.rl[n]);
+        cadj = qk < pk ? log1pf(-qk / pk) : -INFINITY;
+      } else {
+        ck = -1;  // an id outside the vocabulary carries no target mass
+      }
+      vs.cand[lane] = ck;
+      vs.cadj[lane] = cadj;
+    }
     for (int c = lane; c < a.nchunk; c += 32) {
       const size_t o = grow * a.nchunk + c;
       float m = __ldcg(a.zsum + o) * expf((__ldcg(a.zmax + o) - M) * inv_T);
       if (ex_in && c == excl / kZChunk) m = fmaxf(m - ex_mass, 0.f);
       vs.mass[c] = m;
+    }
+    __syncwarp();
+    if (sampled) {
+      // subtract the candidates' mass lane by lane (at most 16 small updates, in order)
+      for (int k = 0; k < kK; ++k) {
+        const int cidk = __shfl_sync(0xffffffffu, ck, k);
+        const float tk = __shfl_sync(0xffffffffu, take, k);
+        if (lane == 0 && cidk >= 0) {
+          const int c = cidk / kZChunk;
+          vs.mass[c] = fmaxf(vs.mass[c] - tk, 0.f);
+        }
+      }
     }
     __syncwarp();
     if (lane == 0) {
@@ -494,6 +583,15 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
   __syncthreads();
   const int lo = vs.info[1] * kZChunk;
   const int hi = min(a.V, lo + kZChunk);
+  if (sampled) {
+    if (threadIdx.x < kZChunk / 32) vs.inchunk[threadIdx.x] = 0u;
+    __syncthreads();
+    if (threadIdx.x < kK) {
+      const int ck = vs.cand[threadIdx.x];
+      if (ck >= lo && ck < hi) atomicOr(&vs.inchunk[(ck - lo) >> 5], 1u << ((ck - lo) & 31));
+    }
+    __syncthreads();
+  }
   const int v0 = lo + threadIdx.x * 16;  // kZChunk = 16 tokens x 256 threads
   unsigned long long best = 0ull;
   if (v0 < hi) {
@@ -511,7 +609,13 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
       for (int w = 0; w < 4; ++w) {
         const int v = vq + w;
         if (v == excl) continue;
-        const float key = x[q >> 1][(q & 1) * 4 + w] * inv_T - logf(-logf(u01_from_word(c[w])));
+        float adj = 0.f;
+        if (sampled && (vs.inchunk[(v - lo) >> 5] >> ((v - lo) & 31) & 1u)) {
+          for (int k = 0; k < kK; ++k)
+            if (vs.cand[k] == v) adj = vs.cadj[k];
+          if (adj == -INFINITY) continue;  // q >= p: no residual mass
+        }
+        const float key = x[q >> 1][(q & 1) * 4 + w] * inv_T + adj - logf(-logf(u01_from_word(c[w])));
         const unsigned long long k = pack_key(key, v);
         best = k > best ? k : best;
       }
@@ -542,6 +646,8 @@ struct TailSmem {
   int* path_tok;                 // [16]
   int* flag;
   VerifySmem* vs;
+  float* qprop;                  // sampled traversal: [P][16] proposal distributions
+  int* pidx;                     // [16] drawn candidate indices
 };
 
 __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
@@ -553,6 +659,7 @@ __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
   n += static_cast<size_t>(kMaxL) * kK * kK * 4 + kMaxL * kK * 4 + 32;
   n += kMaxL * kK + 16 + 80 + 80 + 16;
   n += sizeof(VerifySmem) + 16;
+  n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
   return n + 256;
 }
 
@@ -584,6 +691,8 @@ __device__ TailSmem carve(uint8_t* base, int G, int r) {
   s.path_tok = reinterpret_cast<int*>(take(64));
   s.flag = reinterpret_cast<int*>(take(16));
   s.vs = reinterpret_cast<VerifySmem*>(take(sizeof(VerifySmem)));
+  s.qprop = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
+  s.pidx = reinterpret_cast<int*>(take(kMaxL * 4));
   return s;
 }
 
@@ -598,13 +707,23 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
        reinterpret_cast<uint4*>(sm.ids_all), P * kK / 4}};
   staged_copy<5, 2>(seg);
   __syncthreads();
+  // path mode 2 at T > 0: the sampled traversal, verified against its own proposal; at
+  // T = 0 it is the greedy traversal
+  const bool sampled = a.path_mode == 2 && a.T > 0.f;
   if (threadIdx.x < 32) {
-    const float score = path_warp(sm.S_all, sm.ids_all, P, a.path_mode, sm.path_tok, sm.bp, sm.delta);
+    const float score =
+        sampled ? path_sample_warp(sm.S_all, sm.ids_all, P, 1.0f / a.T, a.seed, b, sm.path_tok,
+                                   sm.pidx, sm.qprop)
+                : path_warp(sm.S_all, sm.ids_all, P, a.path_mode == 1 ? 1 : 0, sm.path_tok,
+                            sm.bp, sm.delta);
     if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
     if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
   }
   __syncthreads();
-  verify_block(a, b, sm.path_tok, *sm.vs);
+  if (sampled)
+    verify_block(a, b, sm.path_tok, *sm.vs, sm.qprop, sm.ids_all, sm.pidx);
+  else
+    verify_block(a, b, sm.path_tok, *sm.vs);
 }
 
 // ------------------------------------------------------------------ kernels

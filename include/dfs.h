@@ -64,7 +64,9 @@ typedef enum {
  * CUDA cores (exact fp32 products, for small checkable cases). */
 typedef enum { DFS_BF16 = 0, DFS_FP32 = 1 } dfs_dtype;
 
-typedef enum { DFS_PATH_GREEDY = 0, DFS_PATH_VITERBI = 1 } dfs_path_mode;
+/* DFS_PATH_SAMPLE ("A lightweight path selector": sampling draws from the same scores)
+ * is the fused call's sampled traversal; see dfs_select_verify. */
+typedef enum { DFS_PATH_GREEDY = 0, DFS_PATH_VITERBI = 1, DFS_PATH_SAMPLE = 2 } dfs_path_mode;
 
 typedef struct {
   int B;      /* requests in the batch, >= 1                                 */
@@ -187,7 +189,15 @@ int dfs_verify_noalloc(const dfs_dims* dims, const int32_t* path, const void* ta
 
 /* The whole step, a1..a6, fused: the LM head, gate, pair scores, path and
  * verification above in one enqueue, with the same inputs and outputs.
- * cand_ids_opt, cand_U_opt, S_opt and path_score_opt may be NULL. */
+ * cand_ids_opt, cand_U_opt, S_opt and path_score_opt may be NULL.
+ * path_mode DFS_PATH_SAMPLE with temperature > 0: the traversal draws each successor,
+ *   x_t ~ q_t(c) = softmax_c(S_t(x_{t-1}, c) / T) over position t's 16 candidates (Philox
+ *   counter (0, t, b, 3), word 0, against the cumulative q in candidate order), and the
+ *   verification is speculative sampling against that proposal: accept x_t when
+ *   U < p_{t-1}(x_t) / q_t(x_t); on the first rejection emit a draw from the residual
+ *   max(0, p_{t-1} - q_t) renormalised; when all are accepted a bonus draw from p_{L-1}.
+ *   path_score_opt is then the summed scores of the drawn path. With temperature 0 the
+ *   mode is DFS_PATH_GREEDY. (dfs_path_select does not take it: it has no seed.) */
 int dfs_select_verify(const dfs_dims* dims, const void* hidden, const void* W_vocab,
                       const void* W_g, const void* A, const void* Btab,
                       const int32_t* last_verified, const void* target_logits, int path_mode,

@@ -110,7 +110,8 @@ def _invariants(g, spec, npd, T):
 
 
 @pytest.mark.parametrize("spec", SMALL, ids=lambda s: s.name)
-@pytest.mark.parametrize("mode", [binding.DFS_PATH_GREEDY, binding.DFS_PATH_VITERBI])
+@pytest.mark.parametrize("mode", [binding.DFS_PATH_GREEDY, binding.DFS_PATH_VITERBI,
+                                  binding.DFS_PATH_SAMPLE])
 @pytest.mark.parametrize("T", [0.0, 0.8])
 def test_fused_small(lib, orc, spec, mode, T):
     data = wl.generate(spec, "cuda")
@@ -170,3 +171,21 @@ def test_fused_full_size(lib, orc, spec, reqs):
                                   reqs=reqs)
             diverged = _compare(g, o, spec, reqs, T)
             assert diverged <= max(1, len(reqs) // 2), f"{diverged} of {len(reqs)} diverged"
+
+
+@pytest.mark.parametrize("spec,reqs,T", [(wl.THROUGHPUT, [0, 13, 31], 0.6),
+                                         (wl.SMALL_BATCH, [0, 5], 1.0)],
+                         ids=lambda x: getattr(x, "name", str(x)))
+def test_fused_full_size_sampled(lib, orc, spec, reqs, T):
+    """The sampled traversal and its speculative-sampling verification at full size, on the
+    launch configuration the benchmark times."""
+    data = wl.generate(spec, "cuda")
+    npd = np_inputs(data)
+    for seed in (spec.seed, spec.seed + 17):
+        g = _run(data, spec, binding.DFS_PATH_SAMPLE, T, seed=seed)
+        _invariants(g, spec, npd, T)
+        o = orc.select_verify(npd["h"], npd["W"], npd["Wg"], npd["A"], npd["Bt"], npd["x0"],
+                              npd["Z"], path_mode=binding.DFS_PATH_SAMPLE, temperature=T,
+                              seed=seed, reqs=reqs)
+        diverged = _compare(g, o, spec, reqs, T)
+        assert diverged <= max(1, len(reqs) // 2), f"{diverged} of {len(reqs)} diverged"
