@@ -246,6 +246,37 @@ def run_ours(args):
                           path_mode=binding.DFS_PATH_SAMPLE)
     accept_prop = outs[2].float().mean().item()
 
+    # the greedy step replayed from a CUDA graph (how a decode loop would issue it): 30 steps
+    # over the rotating buffers recorded once, the recording replayed for the timed steps
+    n_rec = 30
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for i in range(n_rec):
+            step(i, 0.0)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cap = torch.cuda.current_stream()
+        for i in range(n_rec):
+            binding.dfs_select_verify(dims, hs[i % nrot], data["W"], data["Wg"], data["A"],
+                                      data["Bt"], data["x0"], Zs[i % nrot], mode, 0.0,
+                                      spec.seed + i, ws, outputs=outs, stream=cap)
+    for _ in range(max(1, args.warmup // n_rec + 1)):
+        graph.replay()
+    torch.cuda.synchronize()
+    replicas.barrier()
+    n_rep = max(1, args.steps // n_rec)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(n_rep):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    ms_graph = g0.elapsed_time(g1) / (n_rep * n_rec)
+    assert binding.dfs_get_device_error(ws) == binding.DFS_OK
+
     # end to end through the public API: every step copies its inputs (h, Z, x0) from pinned
     # host memory and reads its results back to pinned host memory. As a serving loop would,
     # step i+1's inputs are copied while step i runs: two device input sets, two copy streams
@@ -314,6 +345,7 @@ def run_ours(args):
     ms_max = replicas.max_over_ranks(ms_greedy)
     value_samp = replicas.job_throughput(spec.B, ms_samp / 1e3)
     value_prop = replicas.job_throughput(spec.B, ms_prop / 1e3)
+    value_graph = replicas.job_throughput(spec.B, ms_graph / 1e3)
     value_e2e = replicas.job_throughput(spec.B, ms_e2e / 1e3)
     lm_max = replicas.max_over_ranks(lm_ms)
 
@@ -370,6 +402,9 @@ def run_ours(args):
                          "sampled_path": {"value": round(value_prop, 1), "unit": UNIT,
                                           "ms_per_step": round(ms_prop, 4),
                                           "mean_accept_len": round(accept_prop, 3)}},
+            "graph": {"value": round(value_graph, 1), "unit": UNIT,
+                      "ms_per_step": round(ms_graph, 4),
+                      "note": "greedy steps replayed from a CUDA graph of 30 recorded steps"},
             "mean_accept_len": round(accept, 3),
             "gpu_launches": launches,
             "clocks": clk,

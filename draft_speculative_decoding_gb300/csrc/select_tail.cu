@@ -868,10 +868,15 @@ cudaError_t counted(cudaError_t e) {
   return e;
 }
 
-template <typename K>
-cudaError_t set_smem(K kern, size_t bytes) {
-  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(bytes));
+// A tail kernel may need up to tail_smem_bytes(kMaxLists, kMaxRank) of dynamic shared
+// memory. The limit is raised once per kernel, on its first launch, so later launches
+// (including ones recorded into a CUDA graph) make no other runtime call.
+template <auto Kern>
+cudaError_t allow_smem() {
+  static const cudaError_t status = cudaFuncSetAttribute(
+      Kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      static_cast<int>(tail_smem_bytes(kMaxLists, kMaxRank)));
+  return status;
 }
 
 }  // namespace
@@ -889,14 +894,14 @@ cudaError_t launch_zreduce(const ZReduceLaunch& a, cudaStream_t s) {
 
 cudaError_t launch_tail_fused(const TailLaunch& a, cudaStream_t s) {
   const size_t bytes = tail_smem_bytes(a.G, a.r);
-  cudaError_t e = set_smem(k_tail_fused, bytes);
+  cudaError_t e = allow_smem<k_tail_fused>();
   if (e != cudaSuccess) return e;
   return launch_dependent(k_tail_fused, dim3(a.L - 1, a.B), dim3(kTailThreads), bytes, s, a);
 }
 
 cudaError_t launch_merge(const TailLaunch& a, cudaStream_t s) {
   const size_t bytes = tail_smem_bytes(a.G, a.r);
-  cudaError_t e = set_smem(k_merge, bytes);
+  cudaError_t e = allow_smem<k_merge>();
   if (e != cudaSuccess) return e;
   k_merge<<<dim3(a.L - 1, a.B), kTailThreads, bytes, s>>>(a);
   return counted(cudaGetLastError());
@@ -904,7 +909,7 @@ cudaError_t launch_merge(const TailLaunch& a, cudaStream_t s) {
 
 cudaError_t launch_pair(const TailLaunch& a, cudaStream_t s) {
   const size_t bytes = tail_smem_bytes(1, a.r);
-  cudaError_t e = set_smem(k_pair, bytes);
+  cudaError_t e = allow_smem<k_pair>();
   if (e != cudaSuccess) return e;
   k_pair<<<dim3(a.L - 1, a.B), kTailThreads, bytes, s>>>(a);
   return counted(cudaGetLastError());
