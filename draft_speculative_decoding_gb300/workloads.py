@@ -52,6 +52,9 @@ class WorkloadSpec:
     # target agreement: ("top1", rate) | ("recall16", rate) | ("top1_linear", first, last)
     agreement: tuple = ("top1", 0.85)
     zipf: bool = False
+    # "e4m3": the LM head is also given quantised, Wq [V, d] E4M3 bytes with one power-of-two
+    # scale per vocabulary entry, drawn from the same W
+    lmhead: str = "bf16"
     path_modes: tuple = ("viterbi",)
     temperatures: tuple = (0.0,)
 
@@ -184,8 +187,26 @@ def generate(spec: WorkloadSpec, device="cpu", *, calib_reps: int | None = None)
     meta = {"sigma": sig, "agreement_metric": metric, "agreement_target": list(spec.agreement),
             "agreement_realised_per_position": per_pos,
             "agreement_realised": float(sum(per_pos) / len(per_pos)), "device": str(device)}
-    return {"h": h, "W": W, "Wg": Wg, "A": A, "Bt": Bt, "x0": x0.to(torch.int32), "Z": Z,
-            "meta": meta, "spec": spec}
+    out = {"h": h, "W": W, "Wg": Wg, "A": A, "Bt": Bt, "x0": x0.to(torch.int32), "Z": Z,
+           "meta": meta, "spec": spec}
+    if spec.lmhead == "e4m3":
+        out["Wq"], out["w_scale"] = quantize_lmhead_e4m3(W)
+    return out
+
+
+def quantize_lmhead_e4m3(W: torch.Tensor):
+    """Input synthesis for the E4M3 LM head: W [d, V] -> (Wq [V, d] uint8 E4M3 bytes,
+    w_scale [V] fp32), per vocabulary entry the smallest power-of-two scale 2^e with
+    max|W[:, v]| <= 448 * 2^e (1 for an all-zero column), Wq = E4M3(W / scale) rounded to
+    nearest even by torch's float8 cast."""
+    Wt = W.float().t().contiguous()
+    amax = Wt.abs().amax(dim=1)
+    m, e = torch.frexp(amax)
+    e = e - 9 + (m > 0.875).to(e.dtype)
+    scale = torch.where(amax >= 2.0 ** -100, torch.ldexp(torch.ones_like(amax), e),
+                        torch.ones_like(amax))
+    Wq = (Wt / scale[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+    return Wq, scale.float().contiguous()
 
 
 def fresh_targets(data: dict, seed: int) -> torch.Tensor:

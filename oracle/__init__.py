@@ -69,7 +69,11 @@ def _load():
                                             P, P, P], i32),
                 "orc_philox4x64": ([P, P, P], None),
                 "orc_select_verify": ([i32, i32, P, P, P, P, P, P, P, i64, i32, i64, i64, i64,
-                                       i32, i32, f64, u64, P, i64, i32] + [P] * 12, i32),
+                                       i32, i32, f64, u64, P, i64, i32] + [P] * 14, i32),
+                "orc_e4m3_decode": ([P, i64, P], None),
+                "orc_e4m3_encode": ([P, i64, P], None),
+                "orc_quantize_rows_e4m3": ([i32, P, i64, P, i64, P, P], i32),
+                "orc_logits_e4m3": ([P, P, P, P, i64, i64, i64, P, i32], i32),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -287,9 +291,52 @@ def philox4x64(ctr, key) -> np.ndarray:
     return o
 
 
+def e4m3_decode(b) -> np.ndarray:
+    """E4M3 bytes -> float64 (OCP OFP8)."""
+    b = _c(b, np.uint8).reshape(-1)
+    out = np.empty(b.size, np.float64)
+    _load().orc_e4m3_decode(_ptr(b), b.size, _ptr(out))
+    return out
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """float64 values (|x| <= 448) -> E4M3 bytes, round to nearest even."""
+    x = _c(x, np.float64).reshape(-1)
+    out = np.empty(x.size, np.uint8)
+    _load().orc_e4m3_encode(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def quantize_rows_e4m3(h, rows):
+    """h viewed as [-1, d]; (q [n, d] uint8, scale [n] float64)."""
+    h = _c(h)
+    d = h.shape[-1]
+    h2 = h.reshape(-1, d)
+    rows = _c(rows, np.int64).reshape(-1)
+    q = np.empty((rows.size, d), np.uint8)
+    sc = np.empty(rows.size, np.float64)
+    _check(_load().orc_quantize_rows_e4m3(_dtype_code(h2), _ptr(h2), d, _ptr(rows), rows.size,
+                                          _ptr(q), _ptr(sc)), "quantize_rows_e4m3")
+    return q, sc
+
+
+def logits_e4m3(q, h_scale, Wq, w_scale, nthreads: int | None = None) -> np.ndarray:
+    """u [n, V] from quantised rows q [n, d] (scales h_scale [n]) and the E4M3 LM head
+    Wq [V, d] (scales w_scale [V])."""
+    q = _c(q, np.uint8)
+    n, d = q.shape
+    Wq = _c(Wq, np.uint8)
+    V = Wq.shape[0]
+    u = np.empty((n, V), np.float64)
+    _check(_load().orc_logits_e4m3(_ptr(q), _ptr(_c(h_scale, np.float64)), _ptr(Wq),
+                                   _ptr(_c(w_scale, np.float32)), d, V, n, _ptr(u),
+                                   nthreads or default_threads()), "logits_e4m3")
+    return u
+
+
 def select_verify(h, W, Wg, A, Bt, x0, Z, *, K: int = 16, path_mode: int = 0,
                   temperature: float = 0.0, seed: int = 0, reqs=None,
-                  nthreads: int | None = None) -> dict:
+                  nthreads: int | None = None, Wq=None, w_scale=None) -> dict:
     """The whole step for the listed requests (default: all).
 
     h [B, L, d], W [d, V], Wg [r, d], A/Bt [V, r] share one dtype (uint16 = bf16 bits,
@@ -327,10 +374,14 @@ def select_verify(h, W, Wg, A, Bt, x0, Z, *, K: int = 16, path_mode: int = 0,
     }
     order = ["cand_ids", "cand_U", "gate", "S", "path", "path_score", "out_tokens", "accept_len",
              "topk_gap", "path_margin", "acc_margin", "gumbel_margin"]
+    if Wq is not None:
+        Wq = _c(Wq, np.uint8)
+        w_scale = _c(w_scale, np.float32)
     rc = _load().orc_select_verify(
         dt, _dtype_code(Z), _ptr(h), _ptr(W), _ptr(Wg), _ptr(A), _ptr(Bt), _ptr(x0), _ptr(Z),
         B, L, V, d, r, K, int(path_mode), float(temperature), ctypes.c_uint64(seed & (2**64 - 1)),
-        _ptr(reqs), n, nthreads or default_threads(), *[_ptr(res[k]) for k in order])
+        _ptr(reqs), n, nthreads or default_threads(), *[_ptr(res[k]) for k in order],
+        None if Wq is None else _ptr(Wq), None if w_scale is None else _ptr(w_scale))
     _check(rc, "select_verify")
     res["reqs"] = reqs
     return res

@@ -257,11 +257,107 @@ int64_t redraw_residual(const void* Z, int zdtype, int64_t off, int64_t V, doubl
   return best;
 }
 
+/* ---- E4M3, the OCP 8-bit floating-point format ("OCP 8-bit Floating Point
+ * Specification (OFP8)", 2023): 1 sign, 4 exponent (bias 7) and 3 mantissa bits; normals
+ * (8 + m) 2^(e - 10) for e = 1..15 up to 448 = 1.75 * 2^8, subnormals m 2^-9, no
+ * infinities, S.1111.111 is NaN. */
+double e4m3_value(uint8_t b) {
+  const int sgn = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  if (e == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
+  const double v = (e == 0) ? std::ldexp(static_cast<double>(m), -9)
+                            : std::ldexp(static_cast<double>(8 + m), e - 10);
+  return sgn ? -v : v;
+}
+
+/* x (|x| <= 448) rounded to E4M3, to nearest with ties to even: the grid spacing is
+ * 2^(E - 3) in the binade [2^E, 2^(E+1)) for E >= -6 and 2^-9 below. */
+uint8_t e4m3_round(double x) {
+  const uint8_t sgn = std::signbit(x) ? 0x80 : 0x00;
+  const double a = std::fabs(x);
+  int E = -6;
+  if (a >= std::ldexp(1.0, -6)) {
+    int ex;
+    std::frexp(a, &ex);  // a = f 2^ex, f in [0.5, 1)
+    E = ex - 1;
+  }
+  const double q = std::ldexp(1.0, E - 3);
+  const double v = std::nearbyint(a / q) * q;  // a / q is exact (a power of two)
+  if (v == 0.0) return sgn;
+  if (v < std::ldexp(1.0, -6))
+    return static_cast<uint8_t>(sgn | static_cast<int>(v / std::ldexp(1.0, -9)));
+  int ex;
+  std::frexp(v, &ex);
+  const int e = ex - 1 + 7;                                             // biased exponent
+  const int m = static_cast<int>(v / std::ldexp(1.0, ex - 1 - 3)) - 8;  // 3 mantissa bits
+  return static_cast<uint8_t>(sgn | (e << 3) | m);
+}
+
+/* The power-of-two scale of a row quantised to E4M3: the smallest 2^e with
+ * amax <= 448 * 2^e (448 is E4M3's largest value); 1 when amax is 0 or below 2^-100. */
+double e4m3_row_scale(double amax) {
+  if (!(amax >= std::ldexp(1.0, -100))) return 1.0;
+  int E;
+  const double f = std::frexp(amax, &E);  // amax = f 2^E, f in [0.5, 1); 448 = 0.875 2^9
+  return std::ldexp(1.0, E - 9 + (f > 0.875 ? 1 : 0));
+}
+
 }  // namespace
 
 extern "C" {
 
 int orc_abi_version() { return 1; }
+
+/* E4M3 bytes to double, and doubles (|x| <= 448) to E4M3 bytes, for the format pins. */
+void orc_e4m3_decode(const uint8_t* b, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_value(b[i]);
+}
+void orc_e4m3_encode(const double* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_round(x[i]);
+}
+
+/* Rows of the hidden states quantised for the E4M3 LM head: per row a power-of-two
+ * scale s (e4m3_row_scale of the row's largest magnitude) and q[k] = E4M3(h[k] / s).
+ * h [*, d] of dtype; rows [n]; q [n][d] bytes; scale [n]. */
+int orc_quantize_rows_e4m3(int dtype, const void* h, int64_t d, const int64_t* rows, int64_t n,
+                           uint8_t* q, double* scale) {
+  if (d <= 0 || n < 0 || (dtype != ORC_BF16 && dtype != ORC_FP32)) return -1;
+  for (int64_t i = 0; i < n; ++i) {
+    double amax = 0.0;
+    for (int64_t k = 0; k < d; ++k)
+      amax = std::max(amax, std::fabs(widen(h, dtype, rows[i] * d + k)));
+    const double s = e4m3_row_scale(amax);
+    scale[i] = s;
+    for (int64_t k = 0; k < d; ++k) q[i * d + k] = e4m3_round(widen(h, dtype, rows[i] * d + k) / s);
+  }
+  return 0;
+}
+
+/* Draft logits of the E4M3 LM head: W stored [V][d] as E4M3 bytes with one scale per
+ * vocabulary entry, the rows quantised as above:
+ * u[i][v] = s_h[i] s_w[v] sum_k E4M3(q[i][k]) E4M3(Wq[v][k]), in double. */
+int orc_logits_e4m3(const uint8_t* q, const double* h_scale, const uint8_t* Wq,
+                    const float* w_scale, int64_t d, int64_t V, int64_t n, double* u,
+                    int nthreads) {
+  if (d <= 0 || V <= 0 || n < 0) return -1;
+  std::vector<double> hd(static_cast<size_t>(n) * d);
+  for (int64_t i = 0; i < n; ++i)
+    for (int64_t k = 0; k < d; ++k) hd[i * d + k] = e4m3_value(q[i * d + k]);
+  if (nthreads <= 0) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+  {
+    std::vector<double> w(d);
+#pragma omp for schedule(dynamic, 64)
+    for (int64_t v = 0; v < V; ++v) {
+      for (int64_t k = 0; k < d; ++k) w[k] = e4m3_value(Wq[v * d + k]);
+      for (int64_t i = 0; i < n; ++i) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < d; ++k) acc += hd[i * d + k] * w[k];
+        u[i * V + v] = acc * h_scale[i] * static_cast<double>(w_scale[v]);
+      }
+    }
+  }
+  return 0;
+}
 
 /* Draft logits, [Blog] §"A lightweight path selector": U_t(b) is the drafter's
  * own logit for b, i.e. the shared LM head applied to the position's hidden
@@ -654,7 +750,8 @@ void orc_philox4x64(const uint64_t* ctr, const uint64_t* key, uint64_t* out) {
  * stages above in the pages' order: logits -> keep top-K -> gate -> pair
  * scores -> path -> verify. Inputs: h [B][L][d], W [d][V], Wg [r][d],
  * A and Bt [V][r], x0 [B], Z [B][L][V]. Outputs are indexed by list position
- * q = 0..nreq-1. path_mode 0 = greedy traversal, 1 = Viterbi, 2 = sampled traversal
+ * q = 0..nreq-1. Wq / w_scale non-null: the LM head is E4M3 (orc_logits_e4m3) instead of W.
+ * path_mode 0 = greedy traversal, 1 = Viterbi, 2 = sampled traversal
  * (verified against its own proposal); T <= 0 selects greedy verification (and, for
  * path_mode 2, the greedy traversal). */
 int orc_select_verify(int dtype, int zdtype, const void* h, const void* W, const void* Wg,
@@ -663,7 +760,8 @@ int orc_select_verify(int dtype, int zdtype, const void* h, const void* W, const
                       double T, uint64_t seed, const int64_t* reqs, int64_t nreq, int nthreads,
                       int32_t* cand_ids, double* cand_U, double* gate, double* S, int32_t* path,
                       double* path_score, int32_t* out, int32_t* accept_len, double* topk_gap,
-                      double* path_margin, double* acc_margin, double* gum_margin) {
+                      double* path_margin, double* acc_margin, double* gum_margin,
+                      const uint8_t* Wq, const float* w_scale) {
   if (L < 2 || K < 1 || V < K || B < 1) return -1;
   const int P = L - 1;
   std::vector<int64_t> rows(P);
@@ -677,7 +775,16 @@ int orc_select_verify(int dtype, int zdtype, const void* h, const void* W, const
     double* U = cand_U + q * P * K;
     double* g = gate + q * P * r;
     double* Sq = S + q * P * K * K;
-    int rc = orc_logits(dtype, h, W, d, V, rows.data(), P, u.data(), nthreads);
+    int rc;
+    if (Wq != nullptr) {  // E4M3 LM head: rows quantised, then the E4M3 product
+      std::vector<uint8_t> hq(static_cast<size_t>(P) * d);
+      std::vector<double> hs(P);
+      rc = orc_quantize_rows_e4m3(dtype, h, d, rows.data(), P, hq.data(), hs.data());
+      if (rc == 0)
+        rc = orc_logits_e4m3(hq.data(), hs.data(), Wq, w_scale, d, V, P, u.data(), nthreads);
+    } else {
+      rc = orc_logits(dtype, h, W, d, V, rows.data(), P, u.data(), nthreads);
+    }
     if (rc == 0) rc = orc_topk(u.data(), P, V, K, ids, U, topk_gap + q * P);
     if (rc == 0) rc = orc_gate(dtype, h, Wg, d, r, rows.data(), P, g);
     if (rc == 0) rc = orc_pair_scores(dtype, A, Bt, r, P, K, ids, U, g, x0[b], Sq);
