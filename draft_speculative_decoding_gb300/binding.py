@@ -48,6 +48,11 @@ SIGNATURES = {
     "dfs_verify_noalloc": ([_DP, _P, _P, ctypes.c_float, ctypes.c_uint64, _P, _P, _P], _I),
     "dfs_select_verify": ([_DP, _P, _P, _P, _P, _P, _P, _P, _I, ctypes.c_float, ctypes.c_uint64,
                            _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
+    "dfs_quantize_rows_e4m3": ([_DP, _P, _P, _P, _P], _I),
+    "dfs_lmhead_topk_e4m3": ([_DP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
+    "dfs_select_verify_e4m3": ([_DP, _P, _P, _P, _P, _P, _P, _P, _P, _I, ctypes.c_float,
+                                ctypes.c_uint64, _P, _P, _P, _P, _P, _P, _P, _P,
+                                ctypes.c_size_t, _P], _I),
 }
 
 _lock = threading.Lock()
@@ -226,6 +231,55 @@ def dfs_select_verify(dims: Dims, hidden, W_vocab, W_g, A, Btab, last_verified, 
     _check("dfs_select_verify", load().dfs_select_verify(
         ctypes.byref(dims), _ptr(hidden), _ptr(W_vocab), _ptr(W_g), _ptr(A), _ptr(Btab),
         _ptr(last_verified), _ptr(target_logits), int(path_mode), float(temperature),
+        int(seed) & (2**64 - 1), _ptr(path), _ptr(out), _ptr(acc), _ptr(ids), _ptr(U), _ptr(S),
+        _ptr(score), _ptr(ws), ws.numel(), _stream(stream)))
+    res = {"path": path, "out_tokens": out, "accept_len": acc}
+    if want_intermediates:
+        res.update(cand_ids=ids, cand_U=U, S=S, path_score=score)
+    return res
+
+
+# ---- E4M3 LM head
+def dfs_quantize_rows_e4m3(dims: Dims, hidden, stream=None):
+    """hidden [B, L, d] bf16 -> (q [B*L, d] uint8 E4M3 bytes, scale [B*L] fp32)."""
+    rows = dims.B * dims.L
+    q = torch.empty(rows, dims.d, dtype=torch.uint8, device=hidden.device)
+    sc = torch.empty(rows, dtype=torch.float32, device=hidden.device)
+    _check("dfs_quantize_rows_e4m3", load().dfs_quantize_rows_e4m3(
+        ctypes.byref(dims), _ptr(hidden), _ptr(q), _ptr(sc), _stream(stream)))
+    return q, sc
+
+
+def dfs_lmhead_topk_e4m3(dims: Dims, hidden, Wq, w_scale, ws, stream=None):
+    P = dims.L - 1
+    ids = torch.empty(dims.B, P, K, dtype=torch.int32, device=hidden.device)
+    U = torch.empty(dims.B, P, K, dtype=torch.float32, device=hidden.device)
+    _check("dfs_lmhead_topk_e4m3", load().dfs_lmhead_topk_e4m3(
+        ctypes.byref(dims), _ptr(hidden), _ptr(Wq), _ptr(w_scale), _ptr(ids), _ptr(U), _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return ids, U
+
+
+def dfs_select_verify_e4m3(dims: Dims, hidden, Wq, w_scale, W_g, A, Btab, last_verified,
+                           target_logits, path_mode: int, temperature: float, seed: int, ws, *,
+                           outputs=None, want_intermediates: bool = False, stream=None):
+    """The fused step with the E4M3 LM head; as dfs_select_verify."""
+    P = dims.L - 1
+    dev = hidden.device
+    if outputs is None:
+        outputs = (torch.empty(dims.B, P, dtype=torch.int32, device=dev),
+                   torch.empty(dims.B, dims.L, dtype=torch.int32, device=dev),
+                   torch.empty(dims.B, dtype=torch.int32, device=dev))
+    path, out, acc = outputs
+    ids = U = S = score = None
+    if want_intermediates:
+        ids = torch.empty(dims.B, P, K, dtype=torch.int32, device=dev)
+        U = torch.empty(dims.B, P, K, dtype=torch.float32, device=dev)
+        S = torch.empty(dims.B, P, K, K, dtype=torch.float32, device=dev)
+        score = torch.empty(dims.B, dtype=torch.float32, device=dev)
+    _check("dfs_select_verify_e4m3", load().dfs_select_verify_e4m3(
+        ctypes.byref(dims), _ptr(hidden), _ptr(Wq), _ptr(w_scale), _ptr(W_g), _ptr(A),
+        _ptr(Btab), _ptr(last_verified), _ptr(target_logits), int(path_mode), float(temperature),
         int(seed) & (2**64 - 1), _ptr(path), _ptr(out), _ptr(acc), _ptr(ids), _ptr(U), _ptr(S),
         _ptr(score), _ptr(ws), ws.numel(), _stream(stream)))
     res = {"path": path, "out_tokens": out, "accept_len": acc}

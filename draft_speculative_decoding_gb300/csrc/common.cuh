@@ -252,6 +252,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int n, bool b_mn_major, in
          | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4 with E4M3 A and B (both K-major) and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int n, int m) {
+  return (1u << 4)                           // D format: f32
+         | (0u << 7)                         // A format: E4M3
+         | (0u << 10)                        // B format: E4M3
+         | (static_cast<uint32_t>(n >> 3) << 17)
+         | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
 // ---------------------------------------------------------------- CTA pairs
 // A CTA pair is the two CTAs of a cluster whose ranks differ in bit 0; an MMA issued with
 // cta_group::2 by the even one (the leader) computes M = 256 rows, 128 in each CTA's tensor
@@ -303,6 +312,18 @@ __device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_des
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Pair MMA on 8-bit operands (kind::f8f6f4, K = 32 per instruction), issued by one thread
+// of the leader CTA.
+__device__ __forceinline__ void tc_mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

@@ -47,6 +47,7 @@ struct Layout {
   size_t zmax, zarg, zsum;
   size_t cand_ids, cand_U, S, path;
   size_t logits;
+  size_t hq, h_scale;  // E4M3 LM head: quantised rows and their scales
   size_t total;
   int G, nchunk;
 };
@@ -92,6 +93,8 @@ bool make_layout(const dfs_dims& d, Layout* L) {
   L->S = take(4 * d.B * P * kK * kK);
   L->path = take(4 * d.B * P);
   L->logits = take(d.dtype == DFS_FP32 ? 4 * rows * d.V : 0);
+  L->hq = take(d.dtype == DFS_BF16 ? rows * static_cast<size_t>(d.d) : 0);
+  L->h_scale = take(4 * rows);
   L->total = off;
   return true;
 }
@@ -130,6 +133,8 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? DFS_OK : DFS_ERR_CUDA; }
 
 thread_local cudaEvent_t g_trace_start = nullptr;
 thread_local cudaEvent_t g_trace_stop = nullptr;
+cudaEvent_t vocab_trace_start() { return g_trace_start; }
+cudaEvent_t vocab_trace_stop() { return g_trace_stop; }
 
 dfs::TailLaunch tail_args(const dfs_dims& d, const Layout& L, void* ws) {
   dfs::TailLaunch t{};
@@ -452,6 +457,145 @@ int dfs_select_verify(const dfs_dims* dims, const void* hidden, const void* W_vo
     return DFS_ERR_CUDA;
   dfs::TailLaunch t = tail_args(*dims, L, ws);
   t.G = lists_per_row(*dims, L);
+  t.A = A;
+  t.Bt = Btab;
+  t.x0 = last_verified;
+  t.Z = target_logits;
+  t.T = temperature;
+  t.seed = seed;
+  t.path_mode = path_mode;
+  if (cand_ids_opt) t.cand_ids = cand_ids_opt;
+  if (cand_U_opt) t.cand_U = cand_U_opt;
+  if (S_opt) t.S = S_opt;
+  t.path = path;
+  t.path_score = path_score_opt;
+  t.out_tokens = out_tokens;
+  t.accept_len = accept_len;
+  if (dfs::launch_tail_fused(t, s) != cudaSuccess) return DFS_ERR_CUDA;
+  return DFS_OK;
+}
+
+int dfs_quantize_rows_e4m3(const dfs_dims* dims, const void* hidden, void* q, float* scale,
+                           void* stream) {
+  if (dims == nullptr || dims->B < 1 || dims->L < 1 || dims->d < 8) return DFS_ERR_INVALID;
+  if (dims->dtype != DFS_BF16 || dims->d % 8 != 0 ||
+      static_cast<long long>(dims->B) * dims->L > (1LL << 30))
+    return DFS_ERR_UNSUPPORTED;
+  int rc = check_ptrs({hidden, q, scale}, {});
+  if (rc != DFS_OK) return rc;
+  return cuda_rc(dfs::launch_quantize_rows_e4m3(hidden, dims->B * dims->L, dims->d, q, scale,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shape and pointer checks of the E4M3 LM head: bf16 hidden states (quantised per row by
+// the call), d a multiple of 128 (one stage is 128 bytes of k), Wq [V, d] E4M3 and w_scale
+// [V] fp32, 16-byte aligned.
+int check_e4m3(const dfs_dims* dims, const void* Wq, const float* w_scale) {
+  if (dims->dtype != DFS_BF16 || dims->d % 128 != 0) return DFS_ERR_UNSUPPORTED;
+  return check_ptrs({Wq, w_scale}, {});
+}
+
+// Quantise the rows, then the E4M3 vocabulary tiles with the bf16 gate tiles when W_g is
+// given (and the target-row statistics when Z is given), one kernel launched as a
+// programmatic dependent of the quantisation.
+cudaError_t run_lmhead_e4m3(const dfs_dims& d, const Layout& L, void* ws, const void* hidden,
+                            const void* Wq, const float* w_scale, const void* Wg, cudaStream_t s,
+                            const void* Z = nullptr, float T = 0.f) {
+  const int rows = d.B * d.L;
+  cudaError_t e = dfs::launch_quantize_rows_e4m3(hidden, rows, d.d, at<uint8_t>(ws, L.hq),
+                                                 at<float>(ws, L.h_scale), s);
+  if (e != cudaSuccess) return e;
+  dfs::LmheadLaunch a{};
+  a.hidden = hidden;
+  a.Wg = Wg;
+  a.gate = Wg != nullptr;  // gate tiles (bf16) in the same kernel
+  a.rows_total = rows;
+  a.L = d.L;
+  a.V = d.V;
+  a.d = d.d;
+  a.r = d.r;
+  a.G = L.G;
+  a.part_val = at<float>(ws, L.part_val);
+  a.part_idx = at<int>(ws, L.part_idx);
+  a.gate_out = at<float>(ws, L.gate);
+  a.err = at<int>(ws, L.err);
+  a.wait_limit_ns = debug_wait_limit_ns();
+  a.stall_mma = debug_stall_mma();
+  a.hq = at<uint8_t>(ws, L.hq);
+  a.h_scale = at<float>(ws, L.h_scale);
+  a.Wq = Wq;
+  a.w_scale = w_scale;
+  a.zero_ptr = at<int>(ws, L.counters);
+  a.zero_count = static_cast<int>((L.part_val - L.counters) / 4);
+  if (Z != nullptr) {
+    a.Z = Z;
+    a.zdtype = d.zdtype;
+    a.z_rows = rows;
+    a.z_nchunk = L.nchunk;
+    a.z_inv_T = T > 0.f ? 1.0f / T : 0.f;
+    a.zmax = at<float>(ws, L.zmax);
+    a.zarg = at<int>(ws, L.zarg);
+    a.zsum = at<float>(ws, L.zsum);
+  }
+  if (vocab_trace_start() != nullptr && cudaEventRecord(vocab_trace_start(), s) != cudaSuccess)
+    return cudaErrorInvalidResourceHandle;
+  e = dfs::launch_lmhead_e4m3(a, s);
+  if (e == cudaSuccess && vocab_trace_stop() != nullptr) e = cudaEventRecord(vocab_trace_stop(), s);
+  return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dfs_lmhead_topk_e4m3(const dfs_dims* dims, const void* hidden, const void* Wq,
+                         const float* w_scale, int32_t* cand_ids, float* cand_U, void* ws,
+                         size_t ws_bytes, void* stream) {
+  Layout L;
+  int rc = prepare(dims, ws, ws_bytes, &L);
+  if (rc != DFS_OK) return rc;
+  if ((rc = check_e4m3(dims, Wq, w_scale)) != DFS_OK) return rc;
+  if ((rc = check_ptrs({hidden, cand_ids, cand_U}, {})) != DFS_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (run_lmhead_e4m3(*dims, L, ws, hidden, Wq, w_scale, nullptr, s) != cudaSuccess)
+    return DFS_ERR_CUDA;
+  dfs::TailLaunch t = tail_args(*dims, L, ws);
+  t.G = L.G / 2;
+  t.cand_ids = cand_ids;
+  t.cand_U = cand_U;
+  return cuda_rc(dfs::launch_merge(t, s));
+}
+
+int dfs_select_verify_e4m3(const dfs_dims* dims, const void* hidden, const void* Wq,
+                           const float* w_scale, const void* W_g, const void* A,
+                           const void* Btab, const int32_t* last_verified,
+                           const void* target_logits, int path_mode, float temperature,
+                           uint64_t seed, int32_t* path, int32_t* out_tokens,
+                           int32_t* accept_len, int32_t* cand_ids_opt, float* cand_U_opt,
+                           float* S_opt, float* path_score_opt, void* ws, size_t ws_bytes,
+                           void* stream) {
+  Layout L;
+  int rc = prepare(dims, ws, ws_bytes, &L);
+  if (rc != DFS_OK) return rc;
+  if ((rc = check_e4m3(dims, Wq, w_scale)) != DFS_OK) return rc;
+  if (path_mode != DFS_PATH_GREEDY && path_mode != DFS_PATH_VITERBI &&
+      path_mode != DFS_PATH_SAMPLE)
+    return DFS_ERR_INVALID;
+  if (!(temperature >= 0.f) || temperature != temperature) return DFS_ERR_INVALID;
+  if ((rc = check_ptrs({hidden, W_g, A, Btab, last_verified, target_logits, path, out_tokens,
+                        accept_len},
+                       {cand_ids_opt, cand_U_opt, S_opt, path_score_opt})) != DFS_OK)
+    return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (run_lmhead_e4m3(*dims, L, ws, hidden, Wq, w_scale, W_g, s, target_logits, temperature) !=
+      cudaSuccess)
+    return DFS_ERR_CUDA;
+  dfs::TailLaunch t = tail_args(*dims, L, ws);
+  t.G = L.G / 2;
   t.A = A;
   t.Bt = Btab;
   t.x0 = last_verified;

@@ -36,6 +36,12 @@ struct LmheadLaunch {
   // MMA issuer idle so that the other roles' waits run out and report DFS_ERR_TIMEOUT.
   unsigned long long wait_limit_ns;
   int stall_mma;
+  // E4M3 LM head (launch_lmhead_e4m3): rows quantised by launch_quantize_rows_e4m3 and the
+  // head given as E4M3 bytes [V, d] with one fp32 scale per vocabulary entry
+  const void* hq;        // [rows_total, d] E4M3
+  const float* h_scale;  // [rows_total]
+  const void* Wq;        // [V, d] E4M3
+  const float* w_scale;  // [V]
   // Target-logit row statistics computed by the kernel's spare warps (z_rows = 0: none).
   const void* Z;       // [z_rows, V]
   int zdtype, z_rows, z_nchunk;
@@ -51,6 +57,14 @@ struct LmheadLaunch {
 void note_launches(int n);
 
 cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s);
+// The E4M3 LM head on CTA pairs: vocabulary tiles with kind::f8f6f4 pair MMAs on the
+// quantised rows, gate tiles (when gate) in bf16 from hidden and Wg, the target-row
+// statistics; launched as a programmatic dependent of launch_quantize_rows_e4m3. Partial
+// lists: one per CTA pair (G / 2 per row).
+cudaError_t launch_lmhead_e4m3(const LmheadLaunch& a, cudaStream_t s);
+// Rows of h [rows, d] bf16 quantised to E4M3 with per-row power-of-two scales.
+cudaError_t launch_quantize_rows_e4m3(const void* h, int rows, int d, void* q, float* scale,
+                                      cudaStream_t s);
 // Whether a call with these rows runs on CTA pairs that split the rows (then each row gets
 // G / 2 partial lists, one per pair, instead of G).
 bool lmhead_row_split(int rows_total, int variant, int G);

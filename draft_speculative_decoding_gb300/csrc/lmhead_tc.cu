@@ -37,6 +37,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cuda_fp8.h>
+
 #include <cstring>
 
 #include "common.cuh"
@@ -48,6 +50,7 @@ namespace dfs {
 static_assert(kZChunk == 16 * 256, "zchunk_stat_warp covers a chunk as 16 loads x 32 lanes x 8");
 
 struct LmheadParams {
+  CUtensorMap tm_hq;  // E4M3 head: quantised rows [rows_total, d] bytes, box 128 x 128
   CUtensorMap tm_h;  // hidden [rows_total, d], box 64 (k) x 128 (rows)
   CUtensorMap tm_w;  // W_vocab [d, V], box 64 (vocab) x 64 (k)
   CUtensorMap tm_g;  // W_g [r, d], box 64 (k) x NT (rows of W_g)
@@ -69,6 +72,8 @@ struct LmheadParams {
   int zero_count;
   unsigned long long wait_limit_ns;  // every bounded wait gives up after this long
   int stall_mma;                     // test hook: the MMA issuer stays idle
+  const float* w_scale;              // E4M3 head: per-vocabulary scale [V]
+  const float* h_scale;              // E4M3 head: per-row scale [rows_total]
 };
 
 template <int MT, int NT, int NBUF, int SW, int SH, int CL, int RS>
@@ -550,7 +555,10 @@ struct PairCfg {
   static_assert(kAccCols * kNBuf <= kTmemCols, "TMEM");
 };
 
-template <int S>
+// kE4M3: the operands are E4M3 (the quantised rows and the quantised head Wq [V, d], both
+// K-major 128-byte rows, 128 k per stage, kind::f8f6f4 with K = 32 per instruction), and
+// the epilogue scales column v by w_scale[v] and the row by h_scale (no gate tiles).
+template <int S, bool kE4M3>
 __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
     k_lmhead_pair(const __grid_constant__ LmheadParams p) {
   using Cfg = PairCfg<S>;
@@ -600,7 +608,9 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
   const int n_tiles = p.n_vocab_tiles + p.n_gate_tiles;
   const int cid = blockIdx.x >> 1;
   const int ncl = gridDim.x >> 1;
-  const int KB = p.d / 64;
+  // k-blocks of a tile: 64 bf16 or 128 E4M3 elements (both 128 bytes per row)
+  const int KB_bf16 = p.d / 64;
+  const int KB_e4m3 = p.d / 128;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -611,10 +621,13 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      if (kE4M3) grid_dependency_wait();  // the quantised rows (launched as a dependent)
       for (int tile = cid; ok && tile < n_tiles; tile += ncl) {
         const PairTile pt = pair_tile(tile, ncl, p.n_gate_tiles, n_tiles);
         const bool is_vocab = pt.vocab;
+        const bool q8 = kE4M3 && is_vocab;  // E4M3 operands (gate tiles stay bf16)
         const int n0 = pt.n0 + static_cast<int>(rank) * 128;
+        const int KB = q8 ? KB_e4m3 : KB_bf16;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) {
             ok = false;
@@ -623,14 +636,20 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
           if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * Cfg::kStage);
           const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
           const uint32_t sw = smem_u32(ring + size_t(stage) * Cfg::kStage);
-          if (is_vocab) {
-            tma_load_2d_pair(sw, &p.tm_w, fb, n0, kb * 64, pol_stream);
-            tma_load_2d_pair(sw + 8192, &p.tm_w, fb, n0 + 64, kb * 64, pol_stream);
+          if (q8) {  // 128 vocabulary rows x 128 k bytes (K-major), and the quantised rows
+            tma_load_2d_pair(sw, &p.tm_w, fb, kb * 128, n0, pol_stream);
+            tma_load_2d_pair(sw + Cfg::kHalfBytes, &p.tm_hq, fb, kb * 128,
+                             p.row0 + static_cast<int>(rank) * 128, pol_keep);
           } else {
-            tma_load_2d_pair(sw, &p.tm_g, fb, kb * 64, n0, pol_keep);
+            if (is_vocab) {
+              tma_load_2d_pair(sw, &p.tm_w, fb, n0, kb * 64, pol_stream);
+              tma_load_2d_pair(sw + 8192, &p.tm_w, fb, n0 + 64, kb * 64, pol_stream);
+            } else {
+              tma_load_2d_pair(sw, &p.tm_g, fb, kb * 64, n0, pol_keep);
+            }
+            tma_load_2d_pair(sw + Cfg::kHalfBytes, &p.tm_h, fb, kb * 64,
+                             p.row0 + static_cast<int>(rank) * 128, pol_keep);
           }
-          tma_load_2d_pair(sw + Cfg::kHalfBytes, &p.tm_h, fb, kb * 64,
-                           p.row0 + static_cast<int>(rank) * 128, pol_keep);
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
@@ -661,6 +680,8 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
       bool ok = true;
       for (int tile = cid; ok && tile < n_tiles; tile += ncl) {
         const bool is_vocab = pair_tile(tile, ncl, p.n_gate_tiles, n_tiles).vocab;
+        const bool q8 = kE4M3 && is_vocab;
+        const int KB = q8 ? KB_e4m3 : KB_bf16;
         if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
@@ -673,12 +694,17 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
           const uint32_t sw = smem_u32(ring + size_t(stage) * Cfg::kStage);
           const uint32_t sh = sw + Cfg::kHalfBytes;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bdesc = is_vocab ? smem_desc_sw128(sw + kk * 2048, 8192, 1024)
-                                            : smem_desc_sw128(sw + kk * 32, 0, 1024);
+          for (int kk = 0; kk < 4; ++kk) {  // K = 16 (bf16) or 32 (E4M3): 32 bytes per step
             const uint64_t adesc = smem_desc_sw128(sh + kk * 32, 0, 1024);
-            tc_mma_bf16_pair(d0, adesc, bdesc, is_vocab ? kIdescVocab : kIdescGate,
-                             (kb | kk) != 0);
+            if (q8) {
+              tc_mma_e4m3_pair(d0, adesc, smem_desc_sw128(sw + kk * 32, 0, 1024),
+                               idesc_e4m3_f32(256, 256), (kb | kk) != 0);
+            } else {
+              const uint64_t bdesc = is_vocab ? smem_desc_sw128(sw + kk * 2048, 8192, 1024)
+                                              : smem_desc_sw128(sw + kk * 32, 0, 1024);
+              tc_mma_bf16_pair(d0, adesc, bdesc, is_vocab ? kIdescVocab : kIdescGate,
+                               (kb | kk) != 0);
+            }
           }
           tc_commit_pair_multicast(smem_u32(&empty[stage]), 0x3);
           if (++stage == S) {
@@ -719,6 +745,8 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
     const int grow = p.row0 + row;
     const bool valid = row < p.rows && (grow % p.L) != 0;  // skip each block's verified slot
     const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
+    if (kE4M3) grid_dependency_wait();  // h_scale comes from the quantisation kernel
+    const float hs = (kE4M3 && valid) ? p.h_scale[grow] : 1.f;
     Top16 top;
     top16_init(top);
     int acc = 0;
@@ -738,6 +766,17 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
         tmem_ld_wait();
         if (!valid) continue;
         const int cbase = n0 + c * 32;
+        if (kE4M3 && is_vocab) {  // u = acc * w_scale[v] * h_scale (past V: scale 0, not offered)
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (cbase + j < p.V) w4 = __ldg(reinterpret_cast<const float4*>(p.w_scale + cbase + j));
+            rr[j] = __float_as_uint(__uint_as_float(rr[j]) * w4.x * hs);
+            rr[j + 1] = __float_as_uint(__uint_as_float(rr[j + 1]) * w4.y * hs);
+            rr[j + 2] = __float_as_uint(__uint_as_float(rr[j + 2]) * w4.z * hs);
+            rr[j + 3] = __float_as_uint(__uint_as_float(rr[j + 3]) * w4.w * hs);
+          }
+        }
         if (is_vocab) {
           top16_offer32(top, rr, cbase, p.V - cbase);  // columns past V are not tokens
         } else {
@@ -776,6 +815,59 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
   cluster_sync();  // neither CTA leaves while its peer may still use the pair's resources
 }
 
+// ------------------------------------------------------------------ row quantisation
+// One block per row of h [rows, d] bf16 (d a multiple of 8): the row's largest magnitude,
+// its power-of-two scale (the smallest 2^e with amax <= 448 * 2^e, from the exponent and
+// mantissa bits of amax; 1 when amax < 2^-100), then q = E4M3(h * 2^-e) rounded to nearest
+// even (h * 2^-e is exact).
+__global__ void __launch_bounds__(256) k_quantize_rows_e4m3(const uint16_t* __restrict__ h, int d,
+                                                          uint8_t* __restrict__ q,
+                                                          float* __restrict__ scale) {
+  __shared__ float wmax[8];
+  grid_dependents_launch();  // the LM-head kernel may set up while the rows are quantised
+  const size_t base = static_cast<size_t>(blockIdx.x) * d;
+  const int nch = d / 8;
+  float amax = 0.f;
+  for (int c = threadIdx.x; c < nch; c += blockDim.x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(h + base) + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[j] & 0xFFFFu)),
+                               fabsf(bf16_bits_to_float(w[j] >> 16))));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = wmax[0];
+  for (int i = 1; i < (blockDim.x >> 5); ++i) amax = fmaxf(amax, wmax[i]);
+  // amax = 1.M 2^(Eb - 127) = f 2^E with f = 1.M / 2, E = Eb - 126; 448 = 0.875 2^9:
+  // e = E - 9 + (f > 0.875) = Eb - 135 + (M > 0x600000)
+  const uint32_t bits = __float_as_uint(amax);
+  const int Eb = static_cast<int>(bits >> 23) & 0xFF;
+  int e = 0;
+  if (Eb >= 27) e = Eb - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);  // amax >= 2^-100
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
+  if (threadIdx.x == 0) scale[blockIdx.x] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+  for (int c = threadIdx.x; c < nch; c += blockDim.x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(h + base) + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int j = 0; j < 4; j += 2) {
+      const float2 a = make_float2(bf16_bits_to_float(w[j] & 0xFFFFu) * inv,
+                                   bf16_bits_to_float(w[j] >> 16) * inv);
+      const float2 b = make_float2(bf16_bits_to_float(w[j + 1] & 0xFFFFu) * inv,
+                                   bf16_bits_to_float(w[j + 1] >> 16) * inv);
+      const uint32_t lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+      const uint32_t hi = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
+      out[j >> 1] = lo | (hi << 16);
+    }
+    reinterpret_cast<uint2*>(q + base)[c] = make_uint2(out[0], out[1]);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 namespace {
 
@@ -810,6 +902,21 @@ bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t o
   return r == CUDA_SUCCESS;
 }
 
+// Row-major byte matrix [outer, inner] (E4M3), box inner_box x outer_box, 128-byte swizzle.
+bool encode_u8_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                  uint32_t inner_box, uint32_t outer_box) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {inner_box, outer_box};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int MT, int NT, int NBUF, int SW, int SH, int CL, int RS = 0>
 cudaError_t launch_cfg(const LmheadParams& prm, int grid, cudaStream_t s) {
   using Cfg = LmCfg<MT, NT, NBUF, SW, SH, CL, RS>;
@@ -838,10 +945,10 @@ cudaError_t launch_cfg(const LmheadParams& prm, int grid, cudaStream_t s) {
   return e;
 }
 
-template <int S>
-cudaError_t launch_pair(const LmheadParams& prm, int grid, cudaStream_t s) {
+template <int S, bool kE4M3 = false>
+cudaError_t launch_pair(const LmheadParams& prm, int grid, cudaStream_t s, bool dependent = false) {
   using Cfg = PairCfg<S>;
-  auto kern = k_lmhead_pair<S>;
+  auto kern = k_lmhead_pair<S, kE4M3>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -854,13 +961,15 @@ cudaError_t launch_pair(const LmheadParams& prm, int grid, cudaStream_t s) {
   cfg.blockDim = dim3(Cfg::kThreads);
   cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = dependent ? 2 : 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
   if (e == cudaSuccess) note_launches(1);
   return e;
@@ -936,11 +1045,67 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
     // runs without.
     const int cl = a.vocab ? a.cluster : 1;
     if (variant == 5)
-      e = launch_pair<7>(prm, grid, s);
+      e = launch_pair<7, false>(prm, grid, s);
     else if (variant == 4)
       e = launch_cfg<1, 256, 2, 5, 4, 2, 1>(prm, grid, s);
     else
       e = launch_cluster<1, 256, 2, 5, 4>(prm, grid, cl, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_quantize_rows_e4m3(const void* h, int rows, int d, void* q, float* scale,
+                                      cudaStream_t s) {
+  k_quantize_rows_e4m3<<<rows, 256, 0, s>>>(static_cast<const uint16_t*>(h), d,
+                                             static_cast<uint8_t*>(q), scale);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launches(1);
+  return e;
+}
+
+cudaError_t launch_lmhead_e4m3(const LmheadLaunch& a, cudaStream_t s) {
+  LmheadParams prm;
+  memset(&prm, 0, sizeof(prm));
+  if (!encode_u8_2d(&prm.tm_hq, a.hq, a.d, a.rows_total, 128, 128)) return cudaErrorInvalidValue;
+  if (!encode_u8_2d(&prm.tm_w, a.Wq, a.d, a.V, 128, 128)) return cudaErrorInvalidValue;
+  // gate tiles stay bf16: the bf16 rows and W_g (128 W_g rows per CTA of a pair)
+  if (!encode_bf16_2d(&prm.tm_h, a.hidden, a.d, a.rows_total, 64, 128)) return cudaErrorInvalidValue;
+  if (!encode_bf16_2d(&prm.tm_g, a.gate ? a.Wg : a.hidden, a.d, a.gate ? a.r : a.rows_total, 64,
+                      128))
+    return cudaErrorInvalidValue;
+  prm.L = a.L;
+  prm.V = a.V;
+  prm.d = a.d;
+  prm.r = a.r;
+  prm.G = a.G / 2;  // one partial list per CTA pair
+  prm.part_val = a.part_val;
+  prm.part_idx = a.part_idx;
+  prm.gate_out = a.gate_out;
+  prm.err = a.err;
+  prm.wait_limit_ns = a.wait_limit_ns > 0 ? a.wait_limit_ns : kWaitLimitNs;
+  prm.stall_mma = a.stall_mma;
+  prm.w_scale = a.w_scale;
+  prm.h_scale = a.h_scale;
+  prm.n_vocab_tiles = (a.V + 255) / 256;
+  prm.n_gate_tiles = a.gate ? (a.r + 255) / 256 : 0;
+  prm.write_partials = 1;
+  for (int row0 = 0; row0 < a.rows_total; row0 += 256) {
+    const bool first = row0 == 0;
+    prm.row0 = row0;
+    prm.rows = a.rows_total - row0 < 256 ? a.rows_total - row0 : 256;
+    prm.Z = a.Z;
+    prm.zdtype = a.zdtype;
+    prm.z_rows = first ? a.z_rows : 0;
+    prm.z_nchunk = a.z_nchunk;
+    prm.z_inv_T = a.z_inv_T;
+    prm.zmax = a.zmax;
+    prm.zarg = a.zarg;
+    prm.zsum = a.zsum;
+    prm.zero_ptr = first ? a.zero_ptr : nullptr;
+    prm.zero_count = first ? a.zero_count : 0;
+    // the first group is a programmatic dependent of the row quantisation
+    const cudaError_t e = launch_pair<7, true>(prm, a.G, s, first);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -206,6 +206,40 @@ int dfs_select_verify(const dfs_dims* dims, const void* hidden, const void* W_vo
                       float* S_opt, float* path_score_opt, void* ws, size_t ws_bytes,
                       void* stream);
 
+/* ---- The LM head given quantised: E4M3 (OCP 8-bit floating point) -------------------
+ * The pages run top-k candidate selection through a quantised lm_head when its weights are
+ * not FP16/BF16/FP32 (the RTX 5090 NVFP4 compatibility path). Here the head is E4M3 with
+ * one fp32 scale per vocabulary entry, and the draft rows are quantised per row to E4M3 with
+ * a power-of-two scale (exact to apply), so the product runs on the 8-bit tensor cores:
+ *   u_t[v] = s_h[t] * w_scale[v] * sum_k E4M3(hq[t][k]) * E4M3(Wq[v][k])
+ * Everything after the LM head (gate, pair scores, path, verification) is the bf16 step's.
+ *   Wq      [V, d] E4M3 bytes (vocabulary-major: each entry's d weights contiguous)
+ *   w_scale [V] fp32
+ *   dims: dtype DFS_BF16 (hidden states, W_g, A, B), d a multiple of 128; Wq and w_scale
+ *   16-byte aligned, else DFS_ERR_UNSUPPORTED / DFS_ERR_INVALID. */
+
+/* The row quantisation alone: hidden [B, L, d] bf16 -> q [B*L, d] E4M3 bytes and
+ * scale [B*L] fp32, per row the smallest power of two 2^e with max|h| <= 448 * 2^e (448 is
+ * E4M3's largest value; 1 when max|h| < 2^-100), q = E4M3(h / 2^e) rounded to nearest
+ * even. d a multiple of 8. */
+int dfs_quantize_rows_e4m3(const dfs_dims* dims, const void* hidden, void* q, float* scale,
+                           void* stream);
+
+/* dfs_lmhead_topk with the E4M3 head: cand_ids / cand_U as dfs_lmhead_topk, from u above. */
+int dfs_lmhead_topk_e4m3(const dfs_dims* dims, const void* hidden, const void* Wq,
+                         const float* w_scale, int32_t* cand_ids, float* cand_U, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* dfs_select_verify with the E4M3 head (W_vocab replaced by Wq, w_scale); same outputs. */
+int dfs_select_verify_e4m3(const dfs_dims* dims, const void* hidden, const void* Wq,
+                           const float* w_scale, const void* W_g, const void* A,
+                           const void* Btab, const int32_t* last_verified,
+                           const void* target_logits, int path_mode, float temperature,
+                           uint64_t seed, int32_t* path, int32_t* out_tokens,
+                           int32_t* accept_len, int32_t* cand_ids_opt, float* cand_U_opt,
+                           float* S_opt, float* path_score_opt, void* ws, size_t ws_bytes,
+                           void* stream);
+
 #ifdef __cplusplus
 }
 #endif

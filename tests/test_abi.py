@@ -14,7 +14,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dfs_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(dfs_[a-z0-9_]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
