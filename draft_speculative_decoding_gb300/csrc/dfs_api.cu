@@ -48,6 +48,7 @@ struct Layout {
   size_t cand_ids, cand_U, S, path;
   size_t logits;
   size_t hq, h_scale;  // E4M3 LM head: quantised rows and their scales
+  size_t rstat;        // fused tail: target-row statistics [B*L][4]
   size_t total;
   int G, nchunk;
 };
@@ -95,6 +96,7 @@ bool make_layout(const dfs_dims& d, Layout* L) {
   L->logits = take(d.dtype == DFS_FP32 ? 4 * rows * d.V : 0);
   L->hq = take(d.dtype == DFS_BF16 ? rows * static_cast<size_t>(d.d) : 0);
   L->h_scale = take(4 * rows);
+  L->rstat = take(16 * rows);
   L->total = off;
   return true;
 }
@@ -158,6 +160,7 @@ dfs::TailLaunch tail_args(const dfs_dims& d, const Layout& L, void* ws) {
   t.path = at<int>(ws, L.path);
   t.counters = at<int>(ws, L.counters);
   t.err = at<int>(ws, L.err);
+  t.rstat = at<float>(ws, L.rstat);
   return t;
 }
 

@@ -125,6 +125,8 @@ struct TailLaunch {
   int* accept_len;           // [B]
   int* counters;             // [B]
   int* err;
+  float* rstat;              // fused tail: [B*L][4] target-row statistics (max, argmax bits,
+                             // log-sum-exp), published by the position blocks
 };
 // Fused tail for dfs_select_verify: (L-1) x B blocks; the last block of each request
 // selects its path and verifies it.

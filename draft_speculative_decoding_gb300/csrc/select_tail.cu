@@ -211,13 +211,14 @@ __device__ __forceinline__ int warp_best_lane(bool has, float v, int id) {
 // watches the heads of lists l, l+32, ...; each of the 16 rounds takes the warp's best lane
 // head, and only the winning lane advances its list and rescans its heads. Ids are unique
 // across lists (the vocabulary tiles partition V), so (value, id) orders them totally.
-__device__ void merge_lists_warp(const float* sv, const int* si, int nl, float* outv, int* outi) {
+template <int NS>
+__device__ void merge_lists_warp_ns(const float* sv, const int* si, int nl, float* outv, int* outi) {
   const int lane = threadIdx.x & 31;
-  int head[8];
-  float hv[8];
-  int hi[8];
+  int head[NS];
+  float hv[NS];
+  int hi[NS];
 #pragma unroll
-  for (int s = 0; s < 8; ++s) {
+  for (int s = 0; s < NS; ++s) {
     const int l = lane + 32 * s;
     head[s] = 0;
     hv[s] = l < nl ? sv[l * kK] : -INFINITY;
@@ -227,7 +228,7 @@ __device__ void merge_lists_warp(const float* sv, const int* si, int nl, float* 
   float bv = -INFINITY;
   int bi = kIntMax, bs = -1;
 #pragma unroll
-  for (int s = 0; s < 8; ++s)
+  for (int s = 0; s < NS; ++s)
     if (lane + 32 * s < nl && (bs < 0 || ranks_before(hv[s], hi[s], bv, bi))) {
       bv = hv[s];
       bi = hi[s];
@@ -247,7 +248,7 @@ __device__ void merge_lists_warp(const float* sv, const int* si, int nl, float* 
       outv[k] = bv;
       outi[k] = bi;
 #pragma unroll
-      for (int s = 0; s < 8; ++s)
+      for (int s = 0; s < NS; ++s)
         if (s == bs) {
           const int l = lane + 32 * s;
           ++head[s];
@@ -260,7 +261,7 @@ __device__ void merge_lists_warp(const float* sv, const int* si, int nl, float* 
       bv = -INFINITY;
       bi = kIntMax;
 #pragma unroll
-      for (int s = 0; s < 8; ++s)
+      for (int s = 0; s < NS; ++s)
         if (lane + 32 * s < nl && head[s] < kK && (bs < 0 || ranks_before(hv[s], hi[s], bv, bi))) {
           bv = hv[s];
           bi = hi[s];
@@ -269,6 +270,15 @@ __device__ void merge_lists_warp(const float* sv, const int* si, int nl, float* 
     }
   }
   __syncwarp();
+}
+
+// The merge with as many list slots per lane as nl needs (rescans are shorter).
+__device__ void merge_lists_warp(const float* sv, const int* si, int nl, float* outv, int* outi) {
+  if (nl <= 32) return merge_lists_warp_ns<1>(sv, si, nl, outv, outi);
+  if (nl <= 64) return merge_lists_warp_ns<2>(sv, si, nl, outv, outi);
+  if (nl <= 96) return merge_lists_warp_ns<3>(sv, si, nl, outv, outi);
+  if (nl <= 160) return merge_lists_warp_ns<5>(sv, si, nl, outv, outi);
+  return merge_lists_warp_ns<8>(sv, si, nl, outv, outi);
 }
 
 // ------------------------------------------------------------------ pair scores
@@ -474,20 +484,40 @@ struct VerifySmem {
 // from the residual max(0, p - q): a chunk's mass loses min(p, q) of each candidate in it,
 // and a candidate's Gumbel key gains log(max(0, 1 - q/p)). Without one the proposal is the
 // path itself (q = 1 on x_t).
+// Statistics of target row `row` (max, argmax, log of the sum of exp), by one warp.
+__device__ void row_stat_publish(const TailLaunch& a, int row, float* dst) {
+  const RowStat st = row_stat_warp(a, row);
+  if ((threadIdx.x & 31) == 0) {
+    dst[0] = st.m;
+    dst[1] = __int_as_float(st.i);
+    dst[2] = a.T > 0.f ? logf(st.s) : 0.f;
+  }
+}
+
+// stats != nullptr: the request's L row statistics were published (rstat layout) and staged
+// into shared memory already; otherwise they are computed here.
 __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, VerifySmem& vs,
                              const float* prop_q = nullptr, const int* prop_cand = nullptr,
-                             const int* prop_pidx = nullptr) {
+                             const int* prop_pidx = nullptr, const float* stats = nullptr) {
   const int L = a.L, P = L - 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool soft = a.T > 0.f;
   const float inv_T = soft ? 1.0f / a.T : 0.f;
   const int is_bf16 = a.zdtype == 0;
-  for (int i = warp; i < L; i += blockDim.x >> 5) {
-    const RowStat st = row_stat_warp(a, b * L + i);
-    if (lane == 0) {
-      vs.rm[i] = st.m;
-      vs.ry[i] = st.i;
-      vs.rl[i] = soft ? logf(st.s) : 0.f;
+  if (stats != nullptr) {
+    if (threadIdx.x < L) {
+      vs.rm[threadIdx.x] = stats[threadIdx.x * 4];
+      vs.ry[threadIdx.x] = __float_as_int(stats[threadIdx.x * 4 + 1]);
+      vs.rl[threadIdx.x] = stats[threadIdx.x * 4 + 2];
+    }
+  } else {
+    for (int i = warp; i < L; i += blockDim.x >> 5) {
+      const RowStat st = row_stat_warp(a, b * L + i);
+      if (lane == 0) {
+        vs.rm[i] = st.m;
+        vs.ry[i] = st.i;
+        vs.rl[i] = soft ? logf(st.s) : 0.f;
+      }
     }
   }
   __syncthreads();
@@ -648,6 +678,7 @@ struct TailSmem {
   VerifySmem* vs;
   float* qprop;                  // sampled traversal: [P][16] proposal distributions
   int* pidx;                     // [16] drawn candidate indices
+  float* rstat;                  // [L][4] the request's published row statistics
 };
 
 __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
@@ -660,6 +691,7 @@ __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
   n += kMaxL * kK + 16 + 80 + 80 + 16;
   n += sizeof(VerifySmem) + 16;
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
+  n += kMaxL * 16 + 16;
   return n + 256;
 }
 
@@ -693,6 +725,7 @@ __device__ TailSmem carve(uint8_t* base, int G, int r) {
   s.vs = reinterpret_cast<VerifySmem*>(take(sizeof(VerifySmem)));
   s.qprop = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
   s.pidx = reinterpret_cast<int*>(take(kMaxL * 4));
+  s.rstat = reinterpret_cast<float*>(take(kMaxL * 16));
   return s;
 }
 
@@ -700,12 +733,14 @@ __device__ TailSmem carve(uint8_t* base, int G, int r) {
 // candidates of every position are read back from global memory in one round trip.
 __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
   const int P = a.L - 1;
-  const Seg seg[2] = {
+  const Seg seg[3] = {
       {reinterpret_cast<const uint4*>(a.S + static_cast<size_t>(b) * P * kK * kK),
        reinterpret_cast<uint4*>(sm.S_all), P * kK * kK / 4},
       {reinterpret_cast<const uint4*>(a.cand_ids + static_cast<size_t>(b) * P * kK),
-       reinterpret_cast<uint4*>(sm.ids_all), P * kK / 4}};
-  staged_copy<5, 2>(seg);
+       reinterpret_cast<uint4*>(sm.ids_all), P * kK / 4},
+      {reinterpret_cast<const uint4*>(a.rstat + static_cast<size_t>(b) * a.L * 4),
+       reinterpret_cast<uint4*>(sm.rstat), a.L}};
+  staged_copy<5, 3>(seg);
   __syncthreads();
   // path mode 2 at T > 0: the sampled traversal, verified against its own proposal; at
   // T = 0 it is the greedy traversal
@@ -721,9 +756,9 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
   }
   __syncthreads();
   if (sampled)
-    verify_block(a, b, sm.path_tok, *sm.vs, sm.qprop, sm.ids_all, sm.pidx);
+    verify_block(a, b, sm.path_tok, *sm.vs, sm.qprop, sm.ids_all, sm.pidx, sm.rstat);
   else
-    verify_block(a, b, sm.path_tok, *sm.vs);
+    verify_block(a, b, sm.path_tok, *sm.vs, nullptr, nullptr, nullptr, sm.rstat);
 }
 
 // ------------------------------------------------------------------ kernels
@@ -750,6 +785,10 @@ __global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_consta
   __syncthreads();
   if (warp == 0) merge_lists_warp(sm.lv_cur, sm.li_cur, a.G, sm.cand_U, sm.cand_id);
   if (warp == 1 && t >= 2) merge_lists_warp(sm.lv_prev, sm.li_prev, a.G, sm.prev_U, sm.prev_id);
+  // meanwhile: the statistics of target row t-1 (and of the bonus row L-1 for the last
+  // position), published for the request's last block
+  if (warp == 2) row_stat_publish(a, b * L + t - 1, a.rstat + (static_cast<size_t>(b) * L + t - 1) * 4);
+  if (warp == 3 && t == P) row_stat_publish(a, b * L + L - 1, a.rstat + (static_cast<size_t>(b) * L + L - 1) * 4);
   __syncthreads();
   if (threadIdx.x < kK) {
     sm.prev_tok[threadIdx.x] = t >= 2 ? sm.prev_id[threadIdx.x] : a.x0[b];
