@@ -207,148 +207,232 @@ __device__ __forceinline__ int warp_best_lane(bool has, float v, int id) {
   return __ffs(w) - 1;
 }
 
-// One warp merges nl <= 256 sorted lists of 16 into the top 16 (value desc, id asc): lane l
-// watches the heads of lists l, l+32, ...; each of the 16 rounds takes the warp's best lane
-// head, and only the winning lane advances its list and rescans its heads. Ids are unique
-// across lists (the vocabulary tiles partition V), so (value, id) orders them totally.
-template <int NS>
-__device__ void merge_lists_warp_ns(const float* sv, const int* si, int nl, float* outv, int* outi) {
-  const int lane = threadIdx.x & 31;
-  int head[NS];
-  float hv[NS];
-  int hi[NS];
-#pragma unroll
-  for (int s = 0; s < NS; ++s) {
-    const int l = lane + 32 * s;
-    head[s] = 0;
-    hv[s] = l < nl ? sv[l * kK] : -INFINITY;
-    hi[s] = l < nl ? si[l * kK] : kIntMax;
+// Block-wide top 16 (value desc, id asc) of nm <= 2 sets of G <= 256 sorted lists of 16.
+// Ids are unique across lists (the vocabulary tiles partition V) and the only repeated
+// entries are the (-inf, INT_MAX) fillers, so the packed key orders them totally.
+// 1. The 16 lists with the best heads: no entry of any other list can be in the top 16,
+//    since each of those 16 heads ranks before that list's head, which ranks before the
+//    rest of its list. Heads are ranked by counting (ties of filler heads by list index).
+// 2. A merge tree over those 16 lists: a half-warp merges two sorted lists into their top
+//    16 (the elementwise better of A[l] and B[15-l] is bitonic, four half-cleaner steps sort
+//    it), 16 -> 8 -> 4 -> 2 -> 1 lists per set.
+struct MergeSmem {
+  unsigned long long hk[2][kMaxLists];  // head keys
+  int sel[2][kK];                       // lists by head rank
+  float v1[16][kK];                     // tree levels: 16, 4 lists (both sets)
+  int i1[16][kK];
+  float v2[8][kK];                      // 8 lists
+  int i2[8][kK];
+};
+
+__device__ __forceinline__ void bar_sync_warps0to3() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Two sorted lists (element l16 of A and of B in lane l16 of this half-warp) merged into
+// their top 16, sorted, in (av, ai). All 32 lanes of the warp call it.
+__device__ __forceinline__ void merge2_halfwarp(float& av, int& ai, float bv, int bi) {
+  const int l16 = threadIdx.x & 15;
+  const float rv = __shfl_xor_sync(0xffffffffu, bv, 15);  // B[15 - l16]
+  const int ri = __shfl_xor_sync(0xffffffffu, bi, 15);
+  if (pack_key(rv, ri) > pack_key(av, ai)) {
+    av = rv;
+    ai = ri;
   }
-  // this lane's best head (slot bs), kept across rounds until the lane wins
-  float bv = -INFINITY;
-  int bi = kIntMax, bs = -1;
 #pragma unroll
-  for (int s = 0; s < NS; ++s)
-    if (lane + 32 * s < nl && (bs < 0 || ranks_before(hv[s], hi[s], bv, bi))) {
-      bv = hv[s];
-      bi = hi[s];
-      bs = s;
-    }
-#pragma unroll 1
-  for (int k = 0; k < kK; ++k) {
-    const int wl = warp_best_lane(bs >= 0, bv, bi);
-    if (wl < 0) {  // fewer than 16 candidates in all (e.g. NaN logits): sentinel
-      if (lane == 0) {
-        outv[k] = -INFINITY;
-        outi[k] = -1;
-      }
-      continue;
-    }
-    if (lane == wl) {
-      outv[k] = bv;
-      outi[k] = bi;
-#pragma unroll
-      for (int s = 0; s < NS; ++s)
-        if (s == bs) {
-          const int l = lane + 32 * s;
-          ++head[s];
-          const bool more = head[s] < kK;
-          hv[s] = more ? sv[l * kK + head[s]] : -INFINITY;
-          hi[s] = more ? si[l * kK + head[s]] : kIntMax;
-          if (!more) head[s] = kK + 1;  // exhausted
-        }
-      bs = -1;
-      bv = -INFINITY;
-      bi = kIntMax;
-#pragma unroll
-      for (int s = 0; s < NS; ++s)
-        if (lane + 32 * s < nl && head[s] < kK && (bs < 0 || ranks_before(hv[s], hi[s], bv, bi))) {
-          bv = hv[s];
-          bi = hi[s];
-          bs = s;
-        }
+  for (int d = 8; d > 0; d >>= 1) {
+    const float pv = __shfl_xor_sync(0xffffffffu, av, d);
+    const int pi = __shfl_xor_sync(0xffffffffu, ai, d);
+    const bool lower = (l16 & d) == 0;  // the lower index keeps the better one
+    if ((pack_key(pv, pi) > pack_key(av, ai)) == lower) {
+      av = pv;
+      ai = pi;
     }
   }
-  __syncwarp();
 }
 
-// The merge with as many list slots per lane as nl needs (rescans are shorter).
-__device__ void merge_lists_warp(const float* sv, const int* si, int nl, float* outv, int* outi) {
-  if (nl <= 32) return merge_lists_warp_ns<1>(sv, si, nl, outv, outi);
-  if (nl <= 64) return merge_lists_warp_ns<2>(sv, si, nl, outv, outi);
-  if (nl <= 96) return merge_lists_warp_ns<3>(sv, si, nl, outv, outi);
-  if (nl <= 160) return merge_lists_warp_ns<5>(sv, si, nl, outv, outi);
-  return merge_lists_warp_ns<8>(sv, si, nl, outv, outi);
+// Steps 1 and the first tree level, by the whole block; ends with the level's lists in
+// ms.v1/ms.i1 (set m's list p at m * 8 + p) and a block barrier.
+__device__ void merge_begin(const float* sv0, const int* si0, const float* sv1, const int* si1,
+                            int nm, int G, MergeSmem& ms) {
+  const int n = nm * G;
+  for (int x = threadIdx.x; x < n; x += kTailThreads) {
+    const int m = x >= G, j = x - m * G;
+    ms.hk[m][j] = pack_key((m ? sv1 : sv0)[j * kK], (m ? si1 : si0)[j * kK]);
+  }
+  if (threadIdx.x < 2 * kK) ms.sel[threadIdx.x >> 4][threadIdx.x & 15] = -1;
+  __syncthreads();
+  for (int x = threadIdx.x; x < n; x += kTailThreads) {
+    const int m = x >= G, j = x - m * G;
+    const unsigned long long k = ms.hk[m][j];
+    int rank = 0;
+    for (int i = 0; i < G; ++i) {
+      const unsigned long long o = ms.hk[m][i];
+      rank += (o > k) || (o == k && i < j);
+    }
+    if (rank < kK) ms.sel[m][rank] = j;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, l16 = lane & 15;
+  const int q = warp * 2 + (lane >> 4);  // merge q of 16: set q >> 3, lists 2p, 2p+1
+  const int m = q >> 3, p = q & 7;
+  const float* sv = m ? sv1 : sv0;
+  const int* si = m ? si1 : si0;
+  const int la = m < nm ? ms.sel[m][2 * p] : -1, lb = m < nm ? ms.sel[m][2 * p + 1] : -1;
+  float av = la >= 0 ? sv[la * kK + l16] : -INFINITY;
+  int ai = la >= 0 ? si[la * kK + l16] : kIntMax;
+  const float bv = lb >= 0 ? sv[lb * kK + l16] : -INFINITY;
+  const int bi = lb >= 0 ? si[lb * kK + l16] : kIntMax;
+  merge2_halfwarp(av, ai, bv, bi);
+  ms.v1[q][l16] = av;
+  ms.i1[q][l16] = ai;
+  __syncthreads();
+}
+
+// The remaining tree levels, by warps 0..3 only (they sync among themselves); the top 16
+// of set m go to outv[m]/outi[m]. The caller joins all warps with a block barrier after.
+__device__ void merge_finish(int nm, MergeSmem& ms, float* outv0, int* outi0, float* outv1,
+                             int* outi1) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, l16 = lane & 15;
+  const int h = lane >> 4;
+  {  // 16 -> 8 lists: merge q = 2 warp + h (q < 8), set q >> 2
+    const int q = warp * 2 + h, m = q >> 2, p = q & 3;
+    float av = ms.v1[m * 8 + 2 * p][l16];
+    int ai = ms.i1[m * 8 + 2 * p][l16];
+    merge2_halfwarp(av, ai, ms.v1[m * 8 + 2 * p + 1][l16], ms.i1[m * 8 + 2 * p + 1][l16]);
+    ms.v2[q][l16] = av;
+    ms.i2[q][l16] = ai;
+  }
+  bar_sync_warps0to3();
+  if (warp < 2) {  // 8 -> 4 lists: merge q = 2 warp + h (q < 4), set q >> 1
+    const int q = warp * 2 + h, m = q >> 1, p = q & 1;
+    float av = ms.v2[m * 4 + 2 * p][l16];
+    int ai = ms.i2[m * 4 + 2 * p][l16];
+    merge2_halfwarp(av, ai, ms.v2[m * 4 + 2 * p + 1][l16], ms.i2[m * 4 + 2 * p + 1][l16]);
+    ms.v1[q][l16] = av;  // level 1's lists are all consumed
+    ms.i1[q][l16] = ai;
+  }
+  bar_sync_warps0to3();
+  if (warp == 0) {  // 4 -> 2 lists: half h is set h
+    float av = ms.v1[2 * h][l16];
+    int ai = ms.i1[2 * h][l16];
+    merge2_halfwarp(av, ai, ms.v1[2 * h + 1][l16], ms.i1[2 * h + 1][l16]);
+    if (h < nm) {
+      (h ? outv1 : outv0)[l16] = av;
+      (h ? outi1 : outi0)[l16] = ai;
+    }
+  }
 }
 
 // ------------------------------------------------------------------ pair scores
 // S_t(a, c) = U_t(c) + sum_j A(a)_j g_j B(c)_j for the 16 x 16 pairs of one position.
 // prev_tok[a] is the a-th predecessor token (all x0 for position 1); cur_tok/cur_U the
-// position's candidates; g (the gate row, shared memory) is already in place. Thread
-// (a = tid/16, c = tid%16) returns its score. P and Q are [16][r+4] fp32 scratch rows.
+// position's candidates; g (the gate row, shared memory) is already in place. P and Q are
+// [16][r+4] fp32 scratch rows. Warp w gathers table rows 4w..4w+3 (0..15: A rows of the
+// predecessors, scaled by g; 16..31: B rows of the candidates), one 16-byte chunk per lane
+// per step. Then thread (blk = tid / 16, ks = tid % 16) accumulates a 4 x 4 block of pairs
+// (a in 4 (blk / 4) + 0..3, c in 4 (blk % 4) + 0..3) over the float4 chunks ks, ks + 16, ...
+// of the rank, and the 16 lanes of each half-warp reduce-scatter the block so that lane ks
+// ends with pair (4 (blk / 4) + ks / 4, 4 (blk % 4) + ks % 4). Returns that pair's score and
+// its index a * 16 + c in `pair`.
 __device__ float pair_scores_block(const TailLaunch& a, float* P, float* Q, const float* g,
-                                   const int* prev_tok, const int* cur_tok, const float* cur_U) {
+                                   const int* prev_tok, const int* cur_tok, const float* cur_U,
+                                   int& pair) {
   const int r = a.r, rs = r + 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int is_bf16 = a.dtype == 0;
-  const int per_row = r * (is_bf16 ? 2 : 4) / 16;  // 16-byte chunks per table row
-  const int total = 32 * per_row;
-  constexpr int kMaxPer = 16;                      // r <= 512, fp32: 32 * 128 / 256
-  uint4 raw[kMaxPer];
+  const int per_row = r * (is_bf16 ? 2 : 4) / 16;  // 16-byte chunks per row: <= 128
+  const size_t row_bytes = static_cast<size_t>(r) * (is_bf16 ? 2 : 4);
+  uint4 raw[4][4];
 #pragma unroll
-  for (int k = 0; k < kMaxPer; ++k) {
-    const int i = threadIdx.x + k * kTailThreads;
-    if (i < total) {
-      const int row = i / per_row, ch = i - row * per_row;
-      const bool isP = row < 16;
-      const int tok = isP ? prev_tok[row] : cur_tok[row - 16];
-      if (tok >= 0 && tok < a.V) {
-        const char* base = static_cast<const char*>(isP ? a.A : a.Bt) +
-                           static_cast<size_t>(tok) * r * (is_bf16 ? 2 : 4);
-        raw[k] = __ldg(reinterpret_cast<const uint4*>(base) + ch);
-      } else {  // an id outside the vocabulary (bad input) scores as a zero embedding
-        raw[k] = make_uint4(0u, 0u, 0u, 0u);
-      }
+  for (int rr = 0; rr < 4; ++rr) {
+    const int row = warp * 4 + rr;
+    const int tok = row < 16 ? prev_tok[row] : cur_tok[row - 16];
+    const bool ok = tok >= 0 && tok < a.V;  // an id outside the vocabulary: zero embedding
+    const uint4* base = reinterpret_cast<const uint4*>(static_cast<const char*>(row < 16 ? a.A : a.Bt) +
+                                                       static_cast<size_t>(ok ? tok : 0) * row_bytes);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int ch = lane + 32 * c;
+      raw[rr][c] = (ok && ch < per_row) ? __ldg(base + ch) : make_uint4(0u, 0u, 0u, 0u);
     }
   }
 #pragma unroll
-  for (int k = 0; k < kMaxPer; ++k) {
-    const int i = threadIdx.x + k * kTailThreads;
-    if (i < total) {
-      const int row = i / per_row, ch = i - row * per_row;
-      const bool isP = row < 16;
-      float* dst = (isP ? P + row * rs : Q + (row - 16) * rs);
-      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+  for (int rr = 0; rr < 4; ++rr) {
+    const int row = warp * 4 + rr;
+    const bool isP = row < 16;
+    float* dst = isP ? P + row * rs : Q + (row - 16) * rs;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int ch = lane + 32 * c;
+      if (ch >= per_row) continue;
+      const uint32_t w[4] = {raw[rr][c].x, raw[rr][c].y, raw[rr][c].z, raw[rr][c].w};
       if (is_bf16) {
         const int e0 = ch * 8;
+        float x[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float lo = bf16_bits_to_float(w[j] & 0xFFFFu), hi = bf16_bits_to_float(w[j] >> 16);
-          dst[e0 + 2 * j] = isP ? lo * g[e0 + 2 * j] : lo;
-          dst[e0 + 2 * j + 1] = isP ? hi * g[e0 + 2 * j + 1] : hi;
+          x[2 * j] = bf16_bits_to_float(w[j] & 0xFFFFu);
+          x[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
         }
+        if (isP) {
+          const float4 g0 = *reinterpret_cast<const float4*>(g + e0);
+          const float4 g1 = *reinterpret_cast<const float4*>(g + e0 + 4);
+          x[0] *= g0.x; x[1] *= g0.y; x[2] *= g0.z; x[3] *= g0.w;
+          x[4] *= g1.x; x[5] *= g1.y; x[6] *= g1.z; x[7] *= g1.w;
+        }
+        *reinterpret_cast<float4*>(dst + e0) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(dst + e0 + 4) = make_float4(x[4], x[5], x[6], x[7]);
       } else {
         const int e0 = ch * 4;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float x = __uint_as_float(w[j]);
-          dst[e0 + j] = isP ? x * g[e0 + j] : x;
+        float4 x = make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]),
+                               __uint_as_float(w[3]));
+        if (isP) {
+          const float4 gg = *reinterpret_cast<const float4*>(g + e0);
+          x.x *= gg.x; x.y *= gg.y; x.z *= gg.z; x.w *= gg.w;
         }
+        *reinterpret_cast<float4*>(dst + e0) = x;
       }
     }
   }
   __syncthreads();
-  const int ai = threadIdx.x >> 4, ci = threadIdx.x & 15;
-  const float4* pr = reinterpret_cast<const float4*>(P + ai * rs);
-  const float4* qr = reinterpret_cast<const float4*>(Q + ci * rs);
-  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-  for (int j = 0; j < r / 4; ++j) {
-    const float4 p = pr[j], q = qr[j];
-    s0 = fmaf(p.x, q.x, s0);
-    s1 = fmaf(p.y, q.y, s1);
-    s2 = fmaf(p.z, q.z, s2);
-    s3 = fmaf(p.w, q.w, s3);
+  const int ks = threadIdx.x & 15, blk = threadIdx.x >> 4;
+  const int a0 = 4 * (blk >> 2), c0 = 4 * (blk & 3);
+  float acc[16];
+#pragma unroll
+  for (int o = 0; o < 16; ++o) acc[o] = 0.f;
+  for (int kc = ks; kc < r / 4; kc += 16) {
+    float4 pv[4], qv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      pv[i] = reinterpret_cast<const float4*>(P + (a0 + i) * rs)[kc];
+      qv[i] = reinterpret_cast<const float4*>(Q + (c0 + i) * rs)[kc];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float t = acc[i * 4 + j];
+        t = fmaf(pv[i].x, qv[j].x, t);
+        t = fmaf(pv[i].y, qv[j].y, t);
+        t = fmaf(pv[i].z, qv[j].z, t);
+        t = fmaf(pv[i].w, qv[j].w, t);
+        acc[i * 4 + j] = t;
+      }
   }
-  return cur_U[ci] + ((s0 + s1) + (s2 + s3));
+  // reduce-scatter over the 16 lanes: at step d the lane keeps the half of its outputs
+  // selected by bit d of ks and adds its partner's copy of that half
+#pragma unroll
+  for (int d = 8, n = 16; d > 0; d >>= 1, n >>= 1) {
+    const bool upper = (ks & d) != 0;
+#pragma unroll
+    for (int o = 0; o < n / 2; ++o) {
+      const float send = upper ? acc[o] : acc[o + n / 2];
+      const float keep = upper ? acc[o + n / 2] : acc[o];
+      acc[o] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+    }
+  }
+  const int ai = a0 + (ks >> 2), ci = c0 + (ks & 3);
+  pair = ai * kK + ci;
+  return cur_U[ci] + acc[0];
 }
 
 // ------------------------------------------------------------------ path
@@ -362,6 +446,7 @@ __device__ float path_sample_warp(const float* S, const int* ids, int P, float i
                                   uint64_t seed, int b, int* path_tok, int* pidx, float* q) {
   const int lane = threadIdx.x & 31;
   const bool act = lane < kK;
+  const float u_lane = lane < P ? uniform_path(seed, b, lane + 1) : 0.f;  // lane p: position p+1
   int a = 0;
   float total = 0.f;
 #pragma unroll 1
@@ -382,7 +467,7 @@ __device__ float path_sample_warp(const float* S, const int* ids, int P, float i
       const float o = __shfl_up_sync(0xffffffffu, cum, off);
       if (lane >= off) cum += o;
     }
-    const float u = uniform_path(seed, b, p + 1);
+    const float u = __shfl_sync(0xffffffffu, u_lane, p);
     const unsigned above = __ballot_sync(0xffffffffu, act && cum > u);
     const unsigned mass = __ballot_sync(0xffffffffu, act && qc > 0.f);
     const int c = above ? __ffs(above) - 1 : (mass ? 31 - __clz(mass) : 0);
@@ -467,12 +552,14 @@ struct VerifySmem {
   float rm[kMaxL], rl[kMaxL], zx[kMaxL];
   int ry[kMaxL];
   int info[4];
-  float mass[kMaxZChunks];
+  float uc[kMaxL];                 // chunk-choice uniform of each possible redraw row
+  float mass[kMaxZChunks];         // cumulative residual mass over chunks
   unsigned long long gk[kTailThreads / 32];
   // sampled proposals: the rejected position's candidates in the chosen chunk
   uint32_t inchunk[kZChunk / 32];  // bit j: token lo + j is a candidate
   int cand[kK];                    // candidate ids
   float cadj[kK];                  // log(max(0, 1 - q/p)) added to the candidate's key
+  float take[kK];                  // min(p, q) of each candidate on the chunk-mass scale
 };
 
 // Verification of request b given its path (shared memory), by the whole block: row
@@ -538,6 +625,7 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
         ok = uniform_accept(a.seed, b, lane + 1) < p / qx;
       }
     }
+    if (soft && lane < L) vs.uc[lane] = uniform_chunk(a.seed, b, lane + 1);
     const unsigned fail = __ballot_sync(0xffffffffu, lane < P && !ok);
     const int n = fail ? __ffs(fail) - 1 : P;  // accepted drafts
     if (lane < L && (lane != n || !soft))
@@ -576,39 +664,52 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
       }
       vs.cand[lane] = ck;
       vs.cadj[lane] = cadj;
-    }
-    for (int c = lane; c < a.nchunk; c += 32) {
-      const size_t o = grow * a.nchunk + c;
-      float m = __ldcg(a.zsum + o) * expf((__ldcg(a.zmax + o) - M) * inv_T);
-      if (ex_in && c == excl / kZChunk) m = fmaxf(m - ex_mass, 0.f);
-      vs.mass[c] = m;
+      vs.take[lane] = take;
     }
     __syncwarp();
-    if (sampled) {
-      // subtract the candidates' mass lane by lane (at most 16 small updates, in order)
-      for (int k = 0; k < kK; ++k) {
-        const int cidk = __shfl_sync(0xffffffffu, ck, k);
-        const float tk = __shfl_sync(0xffffffffu, take, k);
-        if (lane == 0 && cidk >= 0) {
-          const int c = cidk / kZChunk;
-          vs.mass[c] = fmaxf(vs.mass[c] - tk, 0.f);
+    // chunk masses, lane-parallel; the cumulative sum by warp scans in chunk order (its last
+    // value is the total, so the pick below always finds a chunk when target < total)
+    const int exc = ex_in ? excl / kZChunk : -1;
+    float run = 0.f;
+    int last_nonzero = 0;
+    for (int c0 = 0; c0 < a.nchunk; c0 += 32) {
+      const int c = c0 + lane;
+      float m = 0.f;
+      if (c < a.nchunk) {
+        const size_t o = grow * a.nchunk + c;
+        m = __ldcg(a.zsum + o) * expf((__ldcg(a.zmax + o) - M) * inv_T);
+        if (c == exc) m = fmaxf(m - ex_mass, 0.f);
+        if (sampled) {  // the candidates' mass, removed in candidate order
+          bool hit = false;
+          for (int k = 0; k < kK; ++k)
+            if (vs.cand[k] >= 0 && vs.cand[k] / kZChunk == c) {
+              m -= vs.take[k];
+              hit = true;
+            }
+          if (hit) m = fmaxf(m, 0.f);
         }
       }
+      const unsigned nz = __ballot_sync(0xffffffffu, m > 0.f);
+      if (nz) last_nonzero = c0 + 31 - __clz(nz);
+      float cum = m;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, cum, off);
+        if (lane >= off) cum += o;
+      }
+      cum += run;
+      if (c < a.nchunk) vs.mass[c] = cum;
+      run = __shfl_sync(0xffffffffu, cum, 31);
     }
     __syncwarp();
-    if (lane == 0) {
-      float total = 0.f;
-      for (int c = 0; c < a.nchunk; ++c) total += vs.mass[c];
-      const float target = uniform_chunk(a.seed, b, n + 1) * total;
-      int pick = -1, last_nonzero = 0;
-      float cum = 0.f;
-      for (int c = 0; c < a.nchunk; ++c) {
-        cum += vs.mass[c];
-        if (vs.mass[c] > 0.f) last_nonzero = c;
-        if (pick < 0 && cum > target) pick = c;
-      }
-      vs.info[1] = pick < 0 ? last_nonzero : pick;
+    const float target = vs.uc[n] * run;
+    int pick = -1;
+    for (int c0 = 0; c0 < a.nchunk && pick < 0; c0 += 32) {
+      const int c = c0 + lane;
+      const unsigned above = __ballot_sync(0xffffffffu, c < a.nchunk && vs.mass[c] > target);
+      if (above) pick = c0 + __ffs(above) - 1;
     }
+    if (lane == 0) vs.info[1] = pick < 0 ? last_nonzero : pick;
   }
   __syncthreads();
   const int lo = vs.info[1] * kZChunk;
@@ -625,31 +726,34 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
   const int v0 = lo + threadIdx.x * 16;  // kZChunk = 16 tokens x 256 threads
   unsigned long long best = 0ull;
   if (v0 < hi) {
-    float x[2][8];
+    float x[2][8] = {};
     load8(a.Z, is_bf16, grow * a.V + v0, x[0]);
     if (v0 + 8 < hi) load8(a.Z, is_bf16, grow * a.V + v0 + 8, x[1]);
+    uint64_t c[4][4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const int vq = v0 + 4 * q;
-      if (vq >= hi) break;
-      uint64_t c[4] = {static_cast<uint64_t>(vq >> 2), static_cast<uint64_t>(n + 1),
-                       static_cast<uint64_t>(b), 1ull};
-      philox4x64_10(c, a.seed, 0ull);
+      c[q][0] = static_cast<uint64_t>((v0 >> 2) + q);
+      c[q][1] = static_cast<uint64_t>(n + 1);
+      c[q][2] = static_cast<uint64_t>(b);
+      c[q][3] = 1ull;
+    }
+    philox4x64_10_n<4>(c, a.seed, 0ull);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
-        const int v = vq + w;
-        if (v == excl) continue;
+        const int v = v0 + 4 * q + w;
+        bool skip = v >= hi || v == excl;
         float adj = 0.f;
-        if (sampled && (vs.inchunk[(v - lo) >> 5] >> ((v - lo) & 31) & 1u)) {
+        if (sampled && !skip && (vs.inchunk[(v - lo) >> 5] >> ((v - lo) & 31) & 1u)) {
           for (int k = 0; k < kK; ++k)
             if (vs.cand[k] == v) adj = vs.cadj[k];
-          if (adj == -INFINITY) continue;  // q >= p: no residual mass
+          skip = adj == -INFINITY;  // q >= p: no residual mass
         }
-        const float key = x[q >> 1][(q & 1) * 4 + w] * inv_T + adj - logf(-logf(u01_from_word(c[w])));
+        const float key = x[q >> 1][(q & 1) * 4 + w] * inv_T + adj - logf(-logf(u01_from_word(c[q][w])));
         const unsigned long long k = pack_key(key, v);
-        best = k > best ? k : best;
+        if (!skip && k > best) best = k;
       }
-    }
   }
   best = warp_max_u64(best);
   if (lane == 0) vs.gk[warp] = best;
@@ -679,6 +783,7 @@ struct TailSmem {
   float* qprop;                  // sampled traversal: [P][16] proposal distributions
   int* pidx;                     // [16] drawn candidate indices
   float* rstat;                  // [L][4] the request's published row statistics
+  MergeSmem* ms;                 // top-16 merge scratch
 };
 
 __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
@@ -692,6 +797,7 @@ __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
   n += sizeof(VerifySmem) + 16;
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
   n += kMaxL * 16 + 16;
+  n += sizeof(MergeSmem) + 16;
   return n + 256;
 }
 
@@ -726,6 +832,7 @@ __device__ TailSmem carve(uint8_t* base, int G, int r) {
   s.qprop = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
   s.pidx = reinterpret_cast<int*>(take(kMaxL * 4));
   s.rstat = reinterpret_cast<float*>(take(kMaxL * 16));
+  s.ms = reinterpret_cast<MergeSmem*>(take(sizeof(MergeSmem)));
   return s;
 }
 
@@ -783,12 +890,17 @@ __global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_consta
        t >= 2 ? n4 : 0}};
   staged_copy<17, 5>(seg);  // G <= 256, r <= 512: 4 * 1024 + 128 chunks over 256 threads
   __syncthreads();
-  if (warp == 0) merge_lists_warp(sm.lv_cur, sm.li_cur, a.G, sm.cand_U, sm.cand_id);
-  if (warp == 1 && t >= 2) merge_lists_warp(sm.lv_prev, sm.li_prev, a.G, sm.prev_U, sm.prev_id);
-  // meanwhile: the statistics of target row t-1 (and of the bonus row L-1 for the last
-  // position), published for the request's last block
-  if (warp == 2) row_stat_publish(a, b * L + t - 1, a.rstat + (static_cast<size_t>(b) * L + t - 1) * 4);
-  if (warp == 3 && t == P) row_stat_publish(a, b * L + L - 1, a.rstat + (static_cast<size_t>(b) * L + L - 1) * 4);
+  // the candidates of position t (and of t-1, the predecessors), merged by the block
+  const int nm = t >= 2 ? 2 : 1;
+  merge_begin(sm.lv_cur, sm.li_cur, sm.lv_prev, sm.li_prev, nm, a.G, *sm.ms);
+  if (warp < 4) {
+    merge_finish(nm, *sm.ms, sm.cand_U, sm.cand_id, sm.prev_U, sm.prev_id);
+  } else {
+    // meanwhile: the statistics of target row t-1 (and of the bonus row L-1 for the last
+    // position), published for the request's last block
+    if (warp == 4) row_stat_publish(a, b * L + t - 1, a.rstat + (static_cast<size_t>(b) * L + t - 1) * 4);
+    if (warp == 5 && t == P) row_stat_publish(a, b * L + L - 1, a.rstat + (static_cast<size_t>(b) * L + L - 1) * 4);
+  }
   __syncthreads();
   if (threadIdx.x < kK) {
     sm.prev_tok[threadIdx.x] = t >= 2 ? sm.prev_id[threadIdx.x] : a.x0[b];
@@ -797,8 +909,9 @@ __global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_consta
     a.cand_U[o] = sm.cand_U[threadIdx.x];
   }
   __syncthreads();
-  const float s = pair_scores_block(a, sm.P, sm.Q, sm.g, sm.prev_tok, sm.cand_id, sm.cand_U);
-  a.S[(static_cast<size_t>(b) * P + (t - 1)) * kK * kK + threadIdx.x] = s;
+  int pair;
+  const float s = pair_scores_block(a, sm.P, sm.Q, sm.g, sm.prev_tok, sm.cand_id, sm.cand_U, pair);
+  a.S[(static_cast<size_t>(b) * P + (t - 1)) * kK * kK + pair] = s;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) *sm.flag = (atomicAdd(a.counters + b, 1) == P - 1);
@@ -821,7 +934,8 @@ __global__ void __launch_bounds__(kTailThreads) k_merge(const __grid_constant__ 
       {reinterpret_cast<const uint4*>(a.part_idx + rc * lst), reinterpret_cast<uint4*>(sm.li_cur), a.G * kK / 4}};
   staged_copy<8, 2>(seg);
   __syncthreads();
-  if (threadIdx.x < 32) merge_lists_warp(sm.lv_cur, sm.li_cur, a.G, sm.cand_U, sm.cand_id);
+  merge_begin(sm.lv_cur, sm.li_cur, nullptr, nullptr, 1, a.G, *sm.ms);
+  if (threadIdx.x < 128) merge_finish(1, *sm.ms, sm.cand_U, sm.cand_id, nullptr, nullptr);
   __syncthreads();
   if (threadIdx.x < kK) {
     const size_t o = (static_cast<size_t>(b) * P + (t - 1)) * kK + threadIdx.x;
@@ -845,8 +959,9 @@ __global__ void __launch_bounds__(kTailThreads) k_pair(const __grid_constant__ T
     sm.prev_tok[threadIdx.x] = t >= 2 ? a.cand_ids[o - kK] : a.x0[b];
   }
   __syncthreads();
-  const float s = pair_scores_block(a, sm.P, sm.Q, sm.g, sm.prev_tok, sm.cand_id, sm.cand_U);
-  a.S[(static_cast<size_t>(b) * P + (t - 1)) * kK * kK + threadIdx.x] = s;
+  int pair;
+  const float s = pair_scores_block(a, sm.P, sm.Q, sm.g, sm.prev_tok, sm.cand_id, sm.cand_U, pair);
+  a.S[(static_cast<size_t>(b) * P + (t - 1)) * kK * kK + pair] = s;
 }
 
 // dfs_path_select: one block per request; four warps stage the scores, one selects.
