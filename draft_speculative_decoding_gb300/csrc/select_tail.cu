@@ -784,6 +784,8 @@ struct TailSmem {
   int* pidx;                     // [16] drawn candidate indices
   float* rstat;                  // [L][4] the request's published row statistics
   MergeSmem* ms;                 // top-16 merge scratch
+  uint64_t* bar;                 // bulk-copy completion of the staged lists
+  int* abort;                    // set when a bounded wait gave up
 };
 
 __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
@@ -798,6 +800,7 @@ __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
   n += kMaxL * 16 + 16;
   n += sizeof(MergeSmem) + 16;
+  n += 32;
   return n + 256;
 }
 
@@ -833,6 +836,8 @@ __device__ TailSmem carve(uint8_t* base, int G, int r) {
   s.pidx = reinterpret_cast<int*>(take(kMaxL * 4));
   s.rstat = reinterpret_cast<float*>(take(kMaxL * 16));
   s.ms = reinterpret_cast<MergeSmem*>(take(sizeof(MergeSmem)));
+  s.bar = reinterpret_cast<uint64_t*>(take(16));
+  s.abort = reinterpret_cast<int*>(take(16));
   return s;
 }
 
@@ -873,23 +878,34 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
 // 16 x 16 pairs of position t, and the last block of request b runs path + verification.
 __global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_constant__ TailLaunch a) {
   extern __shared__ __align__(16) uint8_t tail_smem[];
-  grid_dependency_wait();  // the LM-head kernel's results (launched as its dependent)
   const int t = blockIdx.x + 1, b = blockIdx.y, L = a.L, P = L - 1;
   TailSmem sm = carve(tail_smem, a.G, a.r);
   const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(sm.bar), 1);
+    *sm.abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  grid_dependency_wait();  // the LM-head kernel's results (launched as its dependent)
+  // the gate row and the partial top-16 lists of positions t and t-1: bulk copies
   const size_t lst = static_cast<size_t>(a.G) * kK;
   const size_t rc = static_cast<size_t>(b) * L + t;
-  const int n4 = a.G * kK / 4;
-  const Seg seg[5] = {
-      {reinterpret_cast<const uint4*>(a.gate + rc * a.r), reinterpret_cast<uint4*>(sm.g), a.r / 4},
-      {reinterpret_cast<const uint4*>(a.part_val + rc * lst), reinterpret_cast<uint4*>(sm.lv_cur), n4},
-      {reinterpret_cast<const uint4*>(a.part_idx + rc * lst), reinterpret_cast<uint4*>(sm.li_cur), n4},
-      {reinterpret_cast<const uint4*>(a.part_val + (rc - 1) * lst), reinterpret_cast<uint4*>(sm.lv_prev),
-       t >= 2 ? n4 : 0},
-      {reinterpret_cast<const uint4*>(a.part_idx + (rc - 1) * lst), reinterpret_cast<uint4*>(sm.li_prev),
-       t >= 2 ? n4 : 0}};
-  staged_copy<17, 5>(seg);  // G <= 256, r <= 512: 4 * 1024 + 128 chunks over 256 threads
-  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t bar = smem_u32(sm.bar);
+    const uint32_t lb = static_cast<uint32_t>(lst * 4);
+    mbar_arrive_expect_tx(bar, a.r * 4 + (t >= 2 ? 4 : 2) * lb);
+    bulk_load(smem_u32(sm.g), a.gate + rc * a.r, a.r * 4, bar);
+    bulk_load(smem_u32(sm.lv_cur), a.part_val + rc * lst, lb, bar);
+    bulk_load(smem_u32(sm.li_cur), a.part_idx + rc * lst, lb, bar);
+    if (t >= 2) {
+      bulk_load(smem_u32(sm.lv_prev), a.part_val + (rc - 1) * lst, lb, bar);
+      bulk_load(smem_u32(sm.li_prev), a.part_idx + (rc - 1) * lst, lb, bar);
+    }
+  }
+  // a wait that runs out leaves the error word set; the block runs on (every later index is
+  // bounds-checked) and the host reads DFS_ERR_TIMEOUT
+  mbar_wait_bounded(smem_u32(sm.bar), 0, a.err, sm.abort);
   // the candidates of position t (and of t-1, the predecessors), merged by the block
   const int nm = t >= 2 ? 2 : 1;
   merge_begin(sm.lv_cur, sm.li_cur, sm.lv_prev, sm.li_prev, nm, a.G, *sm.ms);
