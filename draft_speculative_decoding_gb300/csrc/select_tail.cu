@@ -264,6 +264,7 @@ __device__ void merge_begin(const float* sv0, const int* si0, const float* sv1, 
     const int m = x >= G, j = x - m * G;
     const unsigned long long k = ms.hk[m][j];
     int rank = 0;
+#pragma unroll 8
     for (int i = 0; i < G; ++i) {
       const unsigned long long o = ms.hk[m][i];
       rank += (o > k) || (o == k && i < j);
@@ -436,50 +437,109 @@ __device__ float pair_scores_block(const TailLaunch& a, float* P, float* Q, cons
 }
 
 // ------------------------------------------------------------------ path
-// Sampled traversal (mode 2), one warp: from the last verified token, x_t is drawn from
-// q_t(c) = softmax_c(S_t(x_{t-1}, c) * inv_T) over the 16 candidates by one uniform (Philox
+// Sampled traversal (mode 2) by the whole block: from the last verified token, x_t is drawn
+// from q_t(c) = softmax_c(S_t(x_{t-1}, c) / T) over the 16 candidates by one uniform (Philox
 // stream 3) against the cumulative q in candidate order; if rounding leaves no candidate
-// above it, the last one with mass. Writes path_tok[P], pidx[P] (the drawn candidate
-// indices) and q[P][16] (each position's distribution given the drawn predecessor), all in
-// shared memory; returns the summed scores of the drawn path in every lane.
-__device__ float path_sample_warp(const float* S, const int* ids, int P, float inv_T,
-                                  uint64_t seed, int b, int* path_tok, int* pidx, float* q) {
-  const int lane = threadIdx.x & 31;
-  const bool act = lane < kK;
-  const float u_lane = lane < P ? uniform_path(seed, b, lane + 1) : 0.f;  // lane p: position p+1
-  int a = 0;
-  float total = 0.f;
-#pragma unroll 1
-  for (int p = 0; p < P; ++p) {
-    const float s = act ? S[(p * kK + a) * kK + lane] : -INFINITY;
-    const float v = s * inv_T;
-    float m = v;
+// above it, the last one with mass. Every (position p, predecessor a) row's q and draw are
+// computed first, one row per thread, the row's q kept in place of its scores; then thread 0 walks
+// from predecessor 0 and the drawn rows' q are copied out. Writes path_tok[P], pidx[P] and
+// q[P][16]; returns the path score in thread 0. Contains block barriers.
+__device__ float path_sample_block(float* S, const int* ids, int P, float inv_T, uint64_t seed,
+                                   int b, int* path_tok, int* pidx, float* q, float* sdraw,
+                                   float* upath, unsigned char* draw) {
+  if (threadIdx.x < P) upath[threadIdx.x] = uniform_path(seed, b, threadIdx.x + 1);
+  __syncthreads();
+  for (int x = threadIdx.x; x < P * kK; x += blockDim.x) {
+    float* row = S + x * kK;
+    float v[kK];
+    float m = -INFINITY;
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    const float e = act ? expf(v - m) : 0.f;
-    float z = e;
-#pragma unroll
-    for (int off = 8; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-    const float qc = e / z;
-    float cum = qc;  // inclusive prefix sum over lanes 0..15
-#pragma unroll
-    for (int off = 1; off < kK; off <<= 1) {
-      const float o = __shfl_up_sync(0xffffffffu, cum, off);
-      if (lane >= off) cum += o;
+    for (int c = 0; c < kK; ++c) {
+      v[c] = row[c];
+      m = fmaxf(m, v[c] * inv_T);
     }
-    const float u = __shfl_sync(0xffffffffu, u_lane, p);
-    const unsigned above = __ballot_sync(0xffffffffu, act && cum > u);
-    const unsigned mass = __ballot_sync(0xffffffffu, act && qc > 0.f);
-    const int c = above ? __ffs(above) - 1 : (mass ? 31 - __clz(mass) : 0);
-    if (act) q[p * kK + lane] = qc;
-    total += __shfl_sync(0xffffffffu, s, c);
-    if (lane == 0) {
+    float z = 0.f;
+    float e[kK];
+#pragma unroll
+    for (int c = 0; c < kK; ++c) {
+      e[c] = expf(v[c] * inv_T - m);
+      z += e[c];
+    }
+    const float u = upath[x >> 4];
+    float cum = 0.f, v_pick = v[0], v_last = v[0];
+    int pick = -1, last = 0;
+#pragma unroll
+    for (int c = 0; c < kK; ++c) {
+      const float qc = e[c] / z;
+      cum += qc;
+      if (qc > 0.f) {
+        last = c;
+        v_last = v[c];
+      }
+      if (pick < 0 && cum > u) {
+        pick = c;
+        v_pick = v[c];
+      }
+      row[c] = qc;
+    }
+    draw[x] = static_cast<unsigned char>(pick < 0 ? last : pick);
+    sdraw[x] = pick < 0 ? v_last : v_pick;
+  }
+  __syncthreads();
+  float total = 0.f;
+  if (threadIdx.x == 0) {
+    int a = 0;
+    for (int p = 0; p < P; ++p) {
+      const int c = draw[p * kK + a];
+      total += sdraw[p * kK + a];
       path_tok[p] = ids[p * kK + c];
       pidx[p] = c;
+      a = c;
     }
-    a = c;
   }
-  __syncwarp();
+  __syncthreads();
+  for (int x = threadIdx.x; x < P * kK; x += blockDim.x) {
+    const int p = x >> 4, a = p == 0 ? 0 : pidx[p - 1];
+    q[x] = S[(p * kK + a) * kK + (x & 15)];
+  }
+  __syncthreads();
+  return total;
+}
+
+// Greedy traversal by the whole block: the best successor of every (position, predecessor)
+// pair, best[p][a] = argmax_c S_p(a, c) (value desc, id asc; candidate 0 when no score is
+// orderable), one pair per thread into `best`, then thread 0 walks x_t = best[t][x_{t-1}]
+// from the last verified token (predecessor 0). Writes path_tok[P] (shared); returns the
+// path score in thread 0. Contains block barriers.
+__device__ float path_greedy_block(const float* S, const int* ids, int P, int* path_tok,
+                                   unsigned char* best) {
+  for (int x = threadIdx.x; x < P * kK; x += blockDim.x) {
+    const int p = x >> 4;
+    const float* row = S + x * kK;  // S_p(a, .), a = x % 16
+    unsigned long long bk = 0ull;
+    int bc = 0;
+#pragma unroll
+    for (int c = 0; c < kK; ++c) {
+      const unsigned long long k = pack_key(row[c], ids[p * kK + c]);
+      if (k > bk) {
+        bk = k;
+        bc = c;
+      }
+    }
+    best[x] = static_cast<unsigned char>((bk >> 32) == 0ull ? 0 : bc);
+  }
+  __syncthreads();
+  float total = 0.f;
+  if (threadIdx.x == 0) {
+    int a = 0;
+    for (int p = 0; p < P; ++p) {
+      const int c = best[p * kK + a];
+      total += S[(p * kK + a) * kK + c];
+      path_tok[p] = ids[p * kK + c];
+      a = c;
+    }
+  }
+  __syncthreads();
   return total;
 }
 
@@ -781,6 +841,8 @@ struct TailSmem {
   int* flag;
   VerifySmem* vs;
   float* qprop;                  // sampled traversal: [P][16] proposal distributions
+  float* sdraw;                  // [P][16] score of the drawn successor of each (p, a)
+  float* upath;                  // [P] path-draw uniforms
   int* pidx;                     // [16] drawn candidate indices
   float* rstat;                  // [L][4] the request's published row statistics
   MergeSmem* ms;                 // top-16 merge scratch
@@ -797,6 +859,7 @@ __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
   n += static_cast<size_t>(kMaxL) * kK * kK * 4 + kMaxL * kK * 4 + 32;
   n += kMaxL * kK + 16 + 80 + 80 + 16;
   n += sizeof(VerifySmem) + 16;
+  n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
   n += kMaxL * 16 + 16;
   n += sizeof(MergeSmem) + 16;
@@ -834,6 +897,8 @@ __device__ TailSmem carve(uint8_t* base, int G, int r) {
   s.vs = reinterpret_cast<VerifySmem*>(take(sizeof(VerifySmem)));
   s.qprop = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
   s.pidx = reinterpret_cast<int*>(take(kMaxL * 4));
+  s.sdraw = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
+  s.upath = reinterpret_cast<float*>(take(kMaxL * 4));
   s.rstat = reinterpret_cast<float*>(take(kMaxL * 16));
   s.ms = reinterpret_cast<MergeSmem*>(take(sizeof(MergeSmem)));
   s.bar = reinterpret_cast<uint64_t*>(take(16));
@@ -857,12 +922,17 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
   // path mode 2 at T > 0: the sampled traversal, verified against its own proposal; at
   // T = 0 it is the greedy traversal
   const bool sampled = a.path_mode == 2 && a.T > 0.f;
-  if (threadIdx.x < 32) {
-    const float score =
-        sampled ? path_sample_warp(sm.S_all, sm.ids_all, P, 1.0f / a.T, a.seed, b, sm.path_tok,
-                                   sm.pidx, sm.qprop)
-                : path_warp(sm.S_all, sm.ids_all, P, a.path_mode == 1 ? 1 : 0, sm.path_tok,
-                            sm.bp, sm.delta);
+  if (!sampled && a.path_mode != 1) {  // greedy (mode 2 at T = 0 included)
+    const float score = path_greedy_block(sm.S_all, sm.ids_all, P, sm.path_tok, sm.bp);
+    if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
+    if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
+  } else if (sampled) {
+    const float score = path_sample_block(sm.S_all, sm.ids_all, P, 1.0f / a.T, a.seed, b,
+                                          sm.path_tok, sm.pidx, sm.qprop, sm.sdraw, sm.upath, sm.bp);
+    if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
+    if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
+  } else if (threadIdx.x < 32) {
+    const float score = path_warp(sm.S_all, sm.ids_all, P, 1, sm.path_tok, sm.bp, sm.delta);
     if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
     if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
   }
