@@ -56,6 +56,7 @@ def _load():
                 "orc_logits": ([i32, P, P, i64, i64, P, i64, P, i32], i32),
                 "orc_topk": ([P, i64, i64, i32, P, P, P], i32),
                 "orc_gate": ([i32, P, P, i64, i64, P, i64, P], i32),
+                "orc_conv2tap": ([i32, P, P, i32, P, i64, i64, i64, P], i32),
                 "orc_pair_scores": ([i32, P, P, i64, i32, i32, P, P, P, ctypes.c_int32, P], i32),
                 "orc_path_greedy": ([i32, i32, P, P, P, P, P, P], i32),
                 "orc_path_viterbi": ([i32, i32, P, P, P, P, P, P], i32),
@@ -143,6 +144,21 @@ def gate(h, Wg, rows) -> np.ndarray:
     _check(_load().orc_gate(_dtype_code(Wg), _ptr(h), _ptr(Wg), d, r, _ptr(rows), rows.size,
                             _ptr(g)), "gate")
     return g
+
+
+def conv2tap(x, base, Wc) -> np.ndarray:
+    """Two-tap dynamic depthwise convolution of x [B, L, d] (bf16 bits or fp32) with the base
+    kernel base [2, d] (fp32) and the correction map Wc [d/8, d] (bf16 bits or fp32):
+    out[b, t] = (base[0] + corr0) * x[b, t] + (base[1] + corr1) * x[b, t-1], x[b, -1] = 0,
+    corr = Wc x[b, t] with one value per 16 channels and tap. float64 [B, L, d]."""
+    x = _c(x)
+    B, L, d = x.shape
+    base = _c(base, np.float32).reshape(2, d)
+    Wc = _c(Wc).reshape(d // 8, d)
+    out = np.empty((B, L, d), np.float64)
+    _check(_load().orc_conv2tap(_dtype_code(x), _ptr(x), _ptr(base), _dtype_code(Wc), _ptr(Wc),
+                                B, L, d, _ptr(out)), "conv2tap")
+    return out
 
 
 def pair_scores(A, Bt, ids, U, g, x0: int) -> np.ndarray:

@@ -30,6 +30,9 @@
  *   orc_philox4x64 ........... numpy.random.Philox raw output
  *   accept length ............ closed form that reproduces the [Blog] Table 1
  *                              verify lengths 4.27 / 6.79
+ *   orc_conv2tap ............. identity and shift kernels (zero correction), one
+ *                              correction group at a time, the correction read from
+ *                              the position's own row, and the [Blog]'s parameter count
  *
  * Tie rule everywhere: among equal values the lower token id wins.
  */
@@ -815,6 +818,42 @@ int orc_select_verify(int dtype, int zdtype, const void* h, const void* W, const
       rc = orc_verify_greedy(zdtype, zb, L, V, path + q * P, out + q * L, accept_len + q);
     if (rc != 0) return rc;
   }
+  return 0;
+}
+
+/* Two-tap dynamic depthwise convolution, [Blog] §"A lightweight local convolution" (its
+ * equation and Fig. 4): Conv_k(x)_t = k_{t,0} (.) x_t + k_{t,1} (.) x_{t-1} over the L
+ * positions of each block, elementwise over the d channels. The pages give each coefficient
+ * as a learned base kernel plus a small correction computed from the current hidden state,
+ * one correction shared by every 16 channels, and say the first position reads the last
+ * verified token. Readings taken (the correction's form is not printed):
+ *   k_{t,j}[c] = base[j][c] + corr_t[j * (d/16) + c / 16],  corr_t = Wc x_t  (Wc: [d/8][d]),
+ *   a linear map of the position's own hidden state: 2 d + 2 (d/16) d parameters per
+ *   convolution, which over the 20 convolutions of a five-layer drafter of width 2560 (one
+ *   before and after each attention and MLP sublayer) is the 16.5M the [Blog] reports;
+ *   row 0 of a block is the last verified token, whose predecessor is outside the block;
+ *   the convolution is block-local and stateless, so x_{-1} = 0 there.
+ * x [nb][L][d] (xdtype), base [2][d] fp32, Wc [d/8][d] (wdtype); out [nb][L][d]. */
+int orc_conv2tap(int xdtype, const void* x, const float* base, int wdtype, const void* Wc,
+                 int64_t nb, int64_t L, int64_t d, double* out) {
+  if (nb < 0 || L < 1 || d < 16 || d % 16 != 0) return -1;
+  const int64_t G = d / 16;
+  std::vector<double> corr(2 * G);
+  for (int64_t b = 0; b < nb; ++b)
+    for (int64_t t = 0; t < L; ++t) {
+      const int64_t row = b * L + t;
+      for (int64_t n = 0; n < 2 * G; ++n) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < d; ++k) acc += widen(Wc, wdtype, n * d + k) * widen(x, xdtype, row * d + k);
+        corr[n] = acc;
+      }
+      for (int64_t c = 0; c < d; ++c) {
+        const double k0 = static_cast<double>(base[c]) + corr[c / 16];
+        const double k1 = static_cast<double>(base[d + c]) + corr[G + c / 16];
+        const double prev = t > 0 ? widen(x, xdtype, (row - 1) * d + c) : 0.0;
+        out[row * d + c] = k0 * widen(x, xdtype, row * d + c) + k1 * prev;
+      }
+    }
   return 0;
 }
 
