@@ -53,6 +53,8 @@ SIGNATURES = {
     "dfs_select_verify_e4m3": ([_DP, _P, _P, _P, _P, _P, _P, _P, _P, _I, ctypes.c_float,
                                 ctypes.c_uint64, _P, _P, _P, _P, _P, _P, _P, _P,
                                 ctypes.c_size_t, _P], _I),
+    "dfs_conv2tap_workspace_size": ([_I, _I, _I], ctypes.c_size_t),
+    "dfs_conv2tap": ([_I, _I, _I, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
 }
 
 _lock = threading.Lock()
@@ -248,6 +250,27 @@ def dfs_quantize_rows_e4m3(dims: Dims, hidden, stream=None):
     _check("dfs_quantize_rows_e4m3", load().dfs_quantize_rows_e4m3(
         ctypes.byref(dims), _ptr(hidden), _ptr(q), _ptr(sc), _stream(stream)))
     return q, sc
+
+
+def alloc_conv_workspace(B: int, L: int, d: int, device=None, stream=None) -> torch.Tensor:
+    """A zero-initialised workspace for dfs_conv2tap on [B, L, d] inputs."""
+    n = load().dfs_conv2tap_workspace_size(B, L, d)
+    if n == 0:
+        raise DfsError("dfs_conv2tap_workspace_size", DFS_ERR_UNSUPPORTED)
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    _check("dfs_workspace_init", load().dfs_workspace_init(_ptr(ws), n, _stream(stream)))
+    return ws
+
+
+def dfs_conv2tap(x, base, Wc, ws, out=None, stream=None):
+    """Two-tap dynamic depthwise convolution: x [B, L, d] bf16, base [2, d] fp32, Wc [d/8, d]
+    bf16 -> out [B, L, d] bf16 (written into `out` when given)."""
+    B, L, d = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _check("dfs_conv2tap", load().dfs_conv2tap(B, L, d, _ptr(x), _ptr(base), _ptr(Wc), _ptr(out),
+                                               _ptr(ws), ws.numel(), _stream(stream)))
+    return out
 
 
 def dfs_lmhead_topk_e4m3(dims: Dims, hidden, Wq, w_scale, ws, stream=None):

@@ -618,3 +618,52 @@ int dfs_select_verify_e4m3(const dfs_dims* dims, const void* hidden, const void*
 }
 
 }  // extern "C"
+
+// ---- two-tap dynamic depthwise convolution ----
+namespace {
+
+int check_conv(int B, int L, int d) {
+  if (B < 1 || L < 1 || d < 64) return DFS_ERR_INVALID;
+  if (d % 64 != 0 || d > 16384 || static_cast<long long>(B) * L > (1LL << 24)) return DFS_ERR_UNSUPPORTED;
+  return DFS_OK;
+}
+
+// The error word, then the correction GEMM's per-split partial sums.
+size_t conv_ws_bytes(int B, int L, int d) { return kAlign + align_up(dfs::conv2tap_partial_bytes(B, L, d)); }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dfs_conv2tap_workspace_size(int B, int L, int d) {
+  return check_conv(B, L, d) == DFS_OK ? conv_ws_bytes(B, L, d) : 0;
+}
+
+int dfs_conv2tap(int B, int L, int d, const void* x, const float* base, const void* Wc, void* out,
+                 void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_conv(B, L, d);
+  if (rc != DFS_OK) return rc;
+  if ((rc = check_ptrs({x, base, Wc, out, ws}, {})) != DFS_OK) return rc;
+  const size_t xbytes = 2 * static_cast<size_t>(B) * L * d;
+  if (overlaps(x, xbytes, out, xbytes)) return DFS_ERR_INVALID;
+  if (ws_bytes < conv_ws_bytes(B, L, d)) return DFS_ERR_WORKSPACE;
+  dfs::ConvLaunch a{};
+  a.x = x;
+  a.base = base;
+  a.Wc = Wc;
+  a.out = out;
+  a.err = at<int>(ws, 0);
+  a.partial = at<float>(ws, kAlign);
+  a.B = B;
+  a.L = L;
+  a.d = d;
+  a.wait_limit_ns = debug_wait_limit_ns();
+  return cuda_rc(dfs::launch_conv2tap(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

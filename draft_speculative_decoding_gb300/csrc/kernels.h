@@ -2,6 +2,7 @@
 // include/dfs.h validates arguments and lays out the workspace, then calls these.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -52,6 +53,30 @@ struct LmheadLaunch {
   int* zero_ptr;       // counters cleared for the later kernels of the call
   int zero_count;
 };
+// ---- two-tap dynamic depthwise convolution (drafter side) ----
+struct ConvLaunch {
+  const void* x;       // [B*L, d] bf16
+  const float* base;   // [2][d]
+  const void* Wc;      // [d/8, d] bf16
+  void* out;           // [B*L, d] bf16
+  float* partial;      // [n_split][B*L][d/8] fp32 (conv2tap_partial_bytes)
+  int* err;
+  int B, L, d;
+  unsigned long long wait_limit_ns;  // 0: the default
+};
+// How the correction GEMM splits K = d: n_kb blocks of 64, kb_per_split per CTA, n_split
+// splits (at most 8, none empty).
+struct ConvSplit {
+  int n_kb, kb_per_split, n_split;
+};
+ConvSplit conv2tap_split(int d);
+size_t conv2tap_partial_bytes(int B, int L, int d);
+cudaError_t launch_conv2tap(const ConvLaunch& a, cudaStream_t s);
+// Row-major bf16 matrix [outer, inner] as a TMA tensor map with an inner_box x outer_box box,
+// 128-byte swizzle, zero fill outside the matrix (the LM-head kernels' encoding).
+bool encode_bf16_2d_tile(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                         uint32_t inner_box, uint32_t outer_box);
+
 // Adds n to the process-wide count of kernels this library has launched. Every launch site
 // calls it once the runtime has accepted the launch; dfs_launch_count reads the total.
 void note_launches(int n);

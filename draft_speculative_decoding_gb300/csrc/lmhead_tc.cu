@@ -1111,4 +1111,9 @@ cudaError_t launch_lmhead_e4m3(const LmheadLaunch& a, cudaStream_t s) {
   return cudaSuccess;
 }
 
+bool encode_bf16_2d_tile(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                         uint32_t inner_box, uint32_t outer_box) {
+  return encode_bf16_2d(m, base, inner, outer, inner_box, outer_box);
+}
+
 }  // namespace dfs

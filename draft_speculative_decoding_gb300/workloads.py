@@ -220,6 +220,38 @@ def fresh_targets(data: dict, seed: int) -> torch.Tensor:
     return (data["Z"].float() + 0.25 * scale * noise).to(torch_dtype(spec)).contiguous()
 
 
+@dataclasses.dataclass(frozen=True)
+class ConvSpec:
+    """Two-tap dynamic depthwise convolution inputs: x [B, L, d] (block row 0 the verified
+    slot), one convolution's base kernels and correction map."""
+    name: str
+    B: int
+    L: int
+    d: int
+    seed: int = 0
+
+    def with_(self, **kw) -> "ConvSpec":
+        return dataclasses.replace(self, **kw)
+
+
+# the drafter width and block of the serving workload (B = 32 blocks of 8)
+CONV_THROUGHPUT = ConvSpec("conv_B32_L8_d5120", B=32, L=8, d=5120, seed=11)
+CONV_SMALL = ConvSpec("conv_B3_L5_d640", B=3, L=5, d=640, seed=12)
+
+
+def conv_inputs(spec: ConvSpec, device="cpu") -> dict:
+    """x ~ N(0, 1) in bf16; base kernels near a learned mix, base[0] ~ 1 + 0.1 N(0, 1) and
+    base[1] ~ 0.5 + 0.1 N(0, 1) (fp32); the correction map Wc ~ N(0, 0.01 / d) in bf16, so
+    each correction (one per 16 channels and tap) is about 0.1: small next to the base, as
+    the pages describe it."""
+    g = torch.Generator().manual_seed(spec.seed)
+    d = spec.d
+    x = torch.randn(spec.B, spec.L, d, generator=g).to(torch.bfloat16)
+    base = torch.stack([1.0 + 0.1 * torch.randn(d, generator=g), 0.5 + 0.1 * torch.randn(d, generator=g)])
+    Wc = (torch.randn(d // 8, d, generator=g) * (0.1 / math.sqrt(d))).to(torch.bfloat16)
+    return {"x": x.to(device), "base": base.float().contiguous().to(device), "Wc": Wc.to(device)}
+
+
 def to_numpy_bits(t: torch.Tensor):
     """Host numpy view of a tensor as the oracle takes it: bf16 -> uint16 bits, fp32 as is,
     integers as int32/int64."""

@@ -240,6 +240,26 @@ int dfs_select_verify_e4m3(const dfs_dims* dims, const void* hidden, const void*
                            float* S_opt, float* path_score_opt, void* ws, size_t ws_bytes,
                            void* stream);
 
+/* ---- Two-tap dynamic depthwise convolution (drafter side) ----
+ * "DFlash 2: Keep Drafting Parallel" §"A lightweight local convolution" (equation, Fig. 4):
+ * inserted before and after each attention and MLP sublayer of the drafter, it mixes every
+ * block position with its predecessor. For block b (B blocks of L rows) and position t:
+ *   out[b][t][c] = k0 * x[b][t][c] + k1 * x[b][t-1][c]        (x[b][-1] = 0: row 0 is the
+ *                                                             last verified token)
+ *   kj = base[j][c] + corr[b][t][j * (d/16) + c / 16]         (one correction per 16 channels)
+ *   corr[b][t][n] = sum_k Wc[n][k] * x[b][t][k]               (n < d/8; a linear map of the
+ *                                                             position's own hidden state)
+ * x: [B][L][d] bf16; base: [2][d] fp32; Wc: [d/8][d] bf16; out: [B][L][d] bf16, all device
+ * memory owned by the caller, 16-byte aligned; out must not overlap x. Correction sums are
+ * fp32 (tensor cores, summed over K splits in a fixed order: results repeat bit for bit);
+ * the output is rounded to bf16 once. d a multiple of 64, at most 16384; L >= 1.
+ * ws: dfs_conv2tap_workspace_size(B, L, d) bytes (the error word and fp32 partial sums),
+ * 16-byte aligned, initialised once with dfs_workspace_init; dfs_get_device_error reads its
+ * error word. Asynchronous on `stream`: two kernels, the second a programmatic dependent. */
+size_t dfs_conv2tap_workspace_size(int B, int L, int d);
+int dfs_conv2tap(int B, int L, int d, const void* x, const float* base, const void* Wc, void* out,
+                 void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
