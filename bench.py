@@ -301,6 +301,57 @@ def run_ours(args):
     ms_graph = g0.elapsed_time(g1) / (n_rep * n_rec)
     assert binding.dfs_get_device_error(ws) == binding.DFS_OK
 
+    # the drafter-side two-tap convolution (dfs_conv2tap) at the workload's block shape: 16
+    # rotating input sets (x and W_c: 147 MB, more than L2), 48 calls recorded into a CUDA
+    # graph and replayed (the per-call host work is not the kernels' time); eager calls too
+    cspec = wl.ConvSpec(f"conv_B{spec.B}_L{spec.L}_d{spec.d}", B=spec.B, L=spec.L, d=spec.d,
+                        seed=spec.seed + 5)
+    n_cset = 16
+    csets = [wl.conv_inputs(cspec.with_(seed=cspec.seed + k), dev) for k in range(n_cset)]
+    cws = binding.alloc_conv_workspace(cspec.B, cspec.L, cspec.d)
+    cout = torch.empty_like(csets[0]["x"])
+
+    def cstep(k, st):
+        c = csets[k % n_cset]
+        binding.dfs_conv2tap(c["x"], c["base"], c["Wc"], cws, out=cout, stream=st)
+
+    for k in range(max(3, args.warmup)):
+        cstep(k, stream)
+    torch.cuda.synchronize()
+    K_c = 200
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for k in range(K_c):
+        cstep(k, stream)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    us_conv_eager = c0.elapsed_time(c1) / K_c * 1e3
+    n_crec = 48
+    with torch.cuda.stream(side):
+        for k in range(n_crec):
+            cstep(k, side)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    cgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cgraph):
+        cap = torch.cuda.current_stream()
+        for k in range(n_crec):
+            cstep(k, cap)
+    cgraph.replay()
+    torch.cuda.synchronize()
+    n_crep = 10
+    c0.record(stream)
+    for _ in range(n_crep):
+        cgraph.replay()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    us_conv = c0.elapsed_time(c1) / (n_crep * n_crec) * 1e3
+    assert binding.dfs_get_device_error(cws) == binding.DFS_OK
+    conv_rows = cspec.B * cspec.L
+    conv_bytes = 4 * conv_rows * cspec.d + 2 * (cspec.d // 8) * cspec.d + 8 * cspec.d
+    conv_flops = 2.0 * conv_rows * cspec.d * (cspec.d // 8)
+    del csets, cgraph
+
     # end to end through the public API: every step copies its inputs (h, Z, x0) from pinned
     # host memory and reads its results back to pinned host memory. As a serving loop would,
     # step i+1's inputs are copied while step i runs: two device input sets, two copy streams
@@ -434,6 +485,18 @@ def run_ours(args):
                                                           peaks["hbm_gbs"], 4),
                           "note": "LM head as E4M3 with per-vocabulary scales "
                                   "(dfs_select_verify_e4m3); not the headline's precision"},
+            "conv2tap": {"workload": cspec.name, "us_per_call": round(us_conv, 3),
+                         "us_per_call_eager": round(us_conv_eager, 3),
+                         "roofline": {"bound": "hbm",
+                                      "achieved": round(conv_bytes / (us_conv * 1e-6) / 1e9, 1),
+                                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                      "frac": round(conv_bytes / (us_conv * 1e-6) / 1e9 /
+                                                    peaks["hbm_gbs"], 4),
+                                      "algorithmic_bytes_per_call": conv_bytes},
+                         "tensor_tflops": round(conv_flops / (us_conv * 1e-6) / 1e12, 1),
+                         "note": "drafter-side two-tap dynamic depthwise convolution "
+                                 "(dfs_conv2tap: correction GEMM + apply, two kernels), "
+                                 "48 calls per CUDA graph over 16 rotating input sets"},
             "graph": {"value": round(value_graph, 1), "unit": UNIT,
                       "ms_per_step": round(ms_graph, 4),
                       "note": "greedy steps replayed from a CUDA graph of 30 recorded steps"},
