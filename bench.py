@@ -20,6 +20,7 @@ import argparse
 import datetime
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -352,6 +353,66 @@ def run_ours(args):
     conv_flops = 2.0 * conv_rows * cspec.d * (cspec.d // 8)
     del csets, cgraph
 
+    # multi-cycle decode loops (cycles.py). Fused: per cycle the fused step and the last-token
+    # hand-off (dfs_next_tokens), the last verified tokens carried on the device, 30 cycles
+    # recorded into one CUDA graph, for B = 1, 8 and the workload's B (its first requests).
+    # Planted: at the workload's B, staged greedy cycles against targets whose argmax agrees
+    # with each drafted token with the page's Table 1 Recall@1 rates (closed form 4.27).
+    from draft_speculative_decoding_gb300 import cycles as cyc_mod
+    cyc_legs = {}
+    n_cyc = 30
+    for Bc in sorted({1, 8, spec.B}):
+        if Bc > spec.B:
+            continue
+        dims_c = binding.make_dims(Bc, spec.L, spec.V, spec.d, spec.r, binding.DFS_BF16,
+                                   binding.DFS_BF16)
+        ws_c = binding.alloc_workspace(dims_c)
+        hs_c, Zs_c = [h[:Bc] for h in hs], [Z[:Bc] for Z in Zs]
+        x0c = data["x0"][:Bc].clone()
+        P_ = spec.L - 1
+        outs_c = (torch.empty(Bc, P_, dtype=torch.int32, device=dev),
+                  torch.empty(Bc, spec.L, dtype=torch.int32, device=dev),
+                  torch.empty(Bc, dtype=torch.int32, device=dev))
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):  # warm-up, and the accept lengths of one eager pass
+            _, accs = cyc_mod.fused_cycles(dims_c, data, hs_c, Zs_c, x0c, ws_c, mode, n_cyc,
+                                           stream=side)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        mean_acc_c = torch.stack(accs).float().mean().item()
+        g_c = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_c):
+            cyc_mod.fused_cycles(dims_c, data, hs_c, Zs_c, x0c, ws_c, mode, n_cyc,
+                                 outputs=outs_c, stream=torch.cuda.current_stream())
+        g_c.replay()
+        torch.cuda.synchronize()
+        n_rep_c = 3
+        c0.record(stream)
+        for _ in range(n_rep_c):
+            g_c.replay()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        ms_cyc = c0.elapsed_time(c1) / (n_rep_c * n_cyc)
+        assert binding.dfs_get_device_error(ws_c) == binding.DFS_OK
+        cyc_legs[f"B{Bc}"] = {"ms_per_cycle": round(ms_cyc, 4),
+                              "cycles_per_s": round(1e3 / ms_cyc, 1),
+                              "blocks_per_s": round(Bc * 1e3 / ms_cyc, 1),
+                              "accepted_tokens_per_s": round(mean_acc_c * Bc * 1e3 / ms_cyc, 1),
+                              "mean_accept_len": round(mean_acc_c, 3)}
+        del g_c, ws_c
+    gen_p = torch.Generator(device=dev).manual_seed(spec.seed + 7)
+    x0p = data["x0"].clone()
+    runs = cyc_mod.planted_cycles(dims, data, hs, Zs[0], x0p, ws, cyc_mod.TABLE1_RECALL_AT_1, 40,
+                                  gen_p)
+    torch.cuda.synchronize()
+    acc_p = torch.stack([a for a, _ in runs]).float()
+    exact_p = all(torch.equal(a.long(), cyc_mod.leading_agreements(g)) for a, g in runs)
+    planted = {"cycles": 40, "requests": spec.B, "mean_accept_len": round(acc_p.mean().item(), 3),
+               "std_error": round(acc_p.std().item() / math.sqrt(acc_p.numel()), 3),
+               "closed_form": round(cyc_mod.closed_form_accept_len(cyc_mod.TABLE1_RECALL_AT_1), 3),
+               "every_accept_len_as_planted": exact_p}
+    assert binding.dfs_get_device_error(ws) == binding.DFS_OK
+
     # end to end through the public API: every step copies its inputs (h, Z, x0) from pinned
     # host memory and reads its results back to pinned host memory. As a serving loop would,
     # step i+1's inputs are copied while step i runs: two device input sets, two copy streams
@@ -497,6 +558,12 @@ def run_ours(args):
                          "note": "drafter-side two-tap dynamic depthwise convolution "
                                  "(dfs_conv2tap: correction GEMM + apply, two kernels), "
                                  "48 calls per CUDA graph over 16 rotating input sets"},
+            "cycles": {"fused_graph": cyc_legs, "planted_table1": planted,
+                       "note": "multi-cycle decode loops: fused step + last-token hand-off per "
+                               "cycle, 30 cycles per CUDA graph (B = 1, 8, 32: the workload's "
+                               "first requests); planted: staged greedy cycles against targets "
+                               "agreeing with each drafted token at the page's Table 1 Recall@1 "
+                               "rates"},
             "graph": {"value": round(value_graph, 1), "unit": UNIT,
                       "ms_per_step": round(ms_graph, 4),
                       "note": "greedy steps replayed from a CUDA graph of 30 recorded steps"},

@@ -53,6 +53,7 @@ SIGNATURES = {
     "dfs_select_verify_e4m3": ([_DP, _P, _P, _P, _P, _P, _P, _P, _P, _I, ctypes.c_float,
                                 ctypes.c_uint64, _P, _P, _P, _P, _P, _P, _P, _P,
                                 ctypes.c_size_t, _P], _I),
+    "dfs_next_tokens": ([_I, _I, _P, _P, _P, _P], _I),
     "dfs_conv2tap_workspace_size": ([_I, _I, _I], ctypes.c_size_t),
     "dfs_conv2tap": ([_I, _I, _I, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
 }
@@ -250,6 +251,17 @@ def dfs_quantize_rows_e4m3(dims: Dims, hidden, stream=None):
     _check("dfs_quantize_rows_e4m3", load().dfs_quantize_rows_e4m3(
         ctypes.byref(dims), _ptr(hidden), _ptr(q), _ptr(sc), _stream(stream)))
     return q, sc
+
+
+def dfs_next_tokens(out_tokens, accept_len, next_last_verified=None, stream=None):
+    """The last token each request emitted (out_tokens [B, L], accept_len [B]) -> [B] int32,
+    written into `next_last_verified` when given (e.g. the next cycle's x0 buffer)."""
+    B, L = out_tokens.shape
+    if next_last_verified is None:
+        next_last_verified = torch.empty(B, dtype=torch.int32, device=out_tokens.device)
+    _check("dfs_next_tokens", load().dfs_next_tokens(B, L, _ptr(out_tokens), _ptr(accept_len),
+                                                     _ptr(next_last_verified), _stream(stream)))
+    return next_last_verified
 
 
 def alloc_conv_workspace(B: int, L: int, d: int, device=None, stream=None) -> torch.Tensor:

@@ -640,6 +640,15 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 extern "C" {
 
+int dfs_next_tokens(int B, int L, const int32_t* out_tokens, const int32_t* accept_len,
+                    int32_t* next_last_verified, void* stream) {
+  if (B < 1 || L < 1 || L > dfs::kMaxL) return DFS_ERR_INVALID;
+  const int rc = check_ptrs({out_tokens, accept_len, next_last_verified}, {});
+  if (rc != DFS_OK) return rc;
+  return cuda_rc(dfs::launch_next_tokens(B, L, out_tokens, accept_len, next_last_verified,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 size_t dfs_conv2tap_workspace_size(int B, int L, int d) {
   return check_conv(B, L, d) == DFS_OK ? conv_ws_bytes(B, L, d) : 0;
 }

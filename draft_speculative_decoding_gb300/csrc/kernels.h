@@ -156,6 +156,8 @@ struct TailLaunch {
 // Fused tail for dfs_select_verify: (L-1) x B blocks; the last block of each request
 // selects its path and verifies it.
 cudaError_t launch_tail_fused(const TailLaunch& a, cudaStream_t s);
+cudaError_t launch_next_tokens(int B, int L, const int32_t* out_tokens, const int32_t* accept_len,
+                               int32_t* next, cudaStream_t s);
 // Stage launchers for the separate entry points (same device code).
 cudaError_t launch_merge(const TailLaunch& a, cudaStream_t s);    // partial lists -> cand
 cudaError_t launch_pair(const TailLaunch& a, cudaStream_t s);     // cand + gate -> S

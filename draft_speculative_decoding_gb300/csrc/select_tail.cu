@@ -1008,6 +1008,16 @@ __global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_consta
   if (threadIdx.x == 0) a.counters[b] = 0;
 }
 
+// Decode-loop hand-off: the last token request b emitted becomes the next cycle's last
+// verified token (-1 for an accept length outside 1..L).
+__global__ void k_next_tokens(int B, int L, const int32_t* __restrict__ out_tokens,
+                              const int32_t* __restrict__ accept_len, int32_t* __restrict__ next) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int n = accept_len[b];
+  next[b] = (n >= 1 && n <= L) ? out_tokens[static_cast<size_t>(b) * L + n - 1] : -1;
+}
+
 // dfs_lmhead_topk: block (t-1, b) merges the partial lists of draft row t.
 __global__ void __launch_bounds__(kTailThreads) k_merge(const __grid_constant__ TailLaunch a) {
   extern __shared__ __align__(16) uint8_t tail_smem[];
@@ -1137,6 +1147,12 @@ cudaError_t launch_tail_fused(const TailLaunch& a, cudaStream_t s) {
   cudaError_t e = allow_smem<k_tail_fused>();
   if (e != cudaSuccess) return e;
   return launch_dependent(k_tail_fused, dim3(a.L - 1, a.B), dim3(kTailThreads), bytes, s, a);
+}
+
+cudaError_t launch_next_tokens(int B, int L, const int32_t* out_tokens, const int32_t* accept_len,
+                               int32_t* next, cudaStream_t s) {
+  k_next_tokens<<<(B + 255) / 256, 256, 0, s>>>(B, L, out_tokens, accept_len, next);
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_merge(const TailLaunch& a, cudaStream_t s) {

@@ -240,6 +240,15 @@ int dfs_select_verify_e4m3(const dfs_dims* dims, const void* hidden, const void*
                            float* S_opt, float* path_score_opt, void* ws, size_t ws_bytes,
                            void* stream);
 
+/* Decode-loop hand-off ([Blog] Fig. 1, one draft-verify cycle after another): for each
+ * request b, next_last_verified[b] = out_tokens[b][accept_len[b] - 1], the last token the
+ * cycle emitted (the target's own next token), which is the next cycle's last verified token
+ * x0. out_tokens [B][L] and accept_len [B] as dfs_select_verify writes them; an accept length
+ * outside 1..L gives -1. Device pointers, 16-byte aligned; next_last_verified may be the
+ * buffer the next cycle passes as last_verified. One kernel on `stream`. */
+int dfs_next_tokens(int B, int L, const int32_t* out_tokens, const int32_t* accept_len,
+                    int32_t* next_last_verified, void* stream);
+
 /* ---- Two-tap dynamic depthwise convolution (drafter side) ----
  * "DFlash 2: Keep Drafting Parallel" §"A lightweight local convolution" (equation, Fig. 4):
  * inserted before and after each attention and MLP sublayer of the drafter, it mixes every
