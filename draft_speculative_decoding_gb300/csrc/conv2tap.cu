@@ -8,8 +8,9 @@
 //                   so that about one CTA per SM streams its share through an 8-stage TMA
 //                   ring; one thread issues tcgen05.mma (bf16 in, fp32 in tensor memory), the
 //                   four warps drain the accumulator into per-split partial sums (fp32, L2).
-//   k_conv_apply -- a programmatic dependent: sums the partials in split order, forms both
-//                   taps' kernels and writes the bf16 output, 8 channels per thread.
+//   k_conv_apply -- a programmatic dependent, one block per row and 1024 channels: sums the
+//                   partials in split order, forms both taps' kernels and writes the bf16
+//                   output, 8 channels per thread.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -28,8 +29,10 @@ constexpr int kCThreads = 128;
 constexpr uint32_t kCTmemCols = 128;
 constexpr int kMaxSplit = 8;
 constexpr size_t kCSmem = 1024 + size_t(kCStages) * kCStage + 8 * (2 * kCStages + 1) + 16;
-constexpr int kApplyThreads = 256;
+constexpr int kApplyThreads = 128;                // one block: 128 chunks of 8 channels of a row
+constexpr int kStilePitch = kCN + 1;               // fp32 staging rows: conflict-free scalar writes
 static_assert(kCStage % 1024 == 0, "stages keep the 1024-byte alignment of 128-byte swizzle");
+static_assert(size_t(kCM) * (kCN + 1) * 4 <= size_t(kCStages) * kCStage, "the staging tile fits in the ring");
 
 struct ConvParams {
   CUtensorMap tm_x;  // x as [rows, d] bf16, box 64 x 128
@@ -127,7 +130,10 @@ __global__ void __launch_bounds__(kCThreads, 1) k_conv_corr(const __grid_constan
   const bool ok = __all_sync(0xffffffffu,
                              mbar_wait_bounded(smem_u32(tfull), 0, p.err, abort_flag, p.wait_limit_ns));
   tc_fence_after();
-  const int row = m0 + warp * 32 + lane;
+  // accumulator -> shared staging tile (the ring is free: every stage has been consumed) ->
+  // coalesced rows of the per-split partials
+  float* stile = reinterpret_cast<float*>(ring);  // [128][kStilePitch]
+  __syncthreads();
   if (ok) {
     uint32_t r[3][32];
     const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
@@ -135,15 +141,20 @@ __global__ void __launch_bounds__(kCThreads, 1) k_conv_corr(const __grid_constan
     tmem_ld_32x32b_x32(taddr + 32, r[1]);
     tmem_ld_32x32b_x32(taddr + 64, r[2]);  // columns 80..95 are read and dropped
     tmem_ld_wait();
-    if (row < p.rows) {
-      float* dst = p.partial + (static_cast<size_t>(split) * p.rows + row) * p.n_out + n0;
-      const int nv = min(kCN, p.n_out - n0);  // a multiple of 8
+    float* srow = stile + (warp * 32 + lane) * kStilePitch;
 #pragma unroll
-      for (int j = 0; j < kCN; j += 4)
-        if (j < nv)
-          *reinterpret_cast<float4*>(dst + j) =
-              make_float4(__uint_as_float(r[j >> 5][j & 31]), __uint_as_float(r[j >> 5][(j + 1) & 31]),
-                          __uint_as_float(r[j >> 5][(j + 2) & 31]), __uint_as_float(r[j >> 5][(j + 3) & 31]));
+    for (int j = 0; j < kCN; ++j) srow[j] = __uint_as_float(r[j >> 5][j & 31]);
+  }
+  __syncthreads();
+  if (ok) {
+    const int nv4 = min(kCN, p.n_out - n0) / 4;  // float4s per row (n_out - n0 is a multiple of 8)
+    for (int i = threadIdx.x; i < kCM * (kCN / 4); i += kCThreads) {
+      const int rr = i / (kCN / 4), q4 = i - rr * (kCN / 4);
+      const int row = m0 + rr;
+      if (row >= p.rows || q4 >= nv4) continue;
+      const float* sv = stile + rr * kStilePitch + 4 * q4;
+      *reinterpret_cast<float4*>(p.partial + (static_cast<size_t>(split) * p.rows + row) * p.n_out + n0 +
+                                 4 * q4) = make_float4(sv[0], sv[1], sv[2], sv[3]);
     }
   }
   tc_fence_before();
@@ -156,11 +167,10 @@ __global__ void __launch_bounds__(kApplyThreads) k_conv_apply(const uint16_t* __
                                                               const float* __restrict__ partial,
                                                               uint16_t* __restrict__ out, int rows,
                                                               int L, int d, int n_out, int n_split) {
-  const int per_row = d / 8;
-  const long long i = static_cast<long long>(blockIdx.x) * kApplyThreads + threadIdx.x;
-  const bool live = i < static_cast<long long>(rows) * per_row;
-  const int row = live ? static_cast<int>(i / per_row) : 0;
-  const int c = live ? static_cast<int>(i - static_cast<long long>(row) * per_row) * 8 : 0;
+  // block (row, chunk block): 8 channels per thread
+  const int row = blockIdx.x;
+  const int c = (blockIdx.y * kApplyThreads + threadIdx.x) * 8;
+  const bool live = c < d;
   const int t = row % L, g = c >> 4, G = d >> 4;
   // the inputs (not written by k_conv_corr) first, then wait for the partial sums
   uint4 xv = make_uint4(0u, 0u, 0u, 0u), pv = make_uint4(0u, 0u, 0u, 0u);
@@ -247,9 +257,8 @@ cudaError_t launch_conv2tap(const ConvLaunch& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   note_launches(1);
 
-  const long long work = static_cast<long long>(rows) * (a.d / 8);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((work + kApplyThreads - 1) / kApplyThreads));
+  cfg.gridDim = dim3(static_cast<unsigned>(rows), (a.d / 8 + kApplyThreads - 1) / kApplyThreads);
   cfg.blockDim = dim3(kApplyThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
