@@ -214,7 +214,7 @@ def verify_greedy(Z, path):
 
 
 def verify_sampling(Z, path, T: float, seed: int, b: int = 0):
-    """Z [L, V] for request index b; returns (out, accept_len, acc_margin, gumbel_margin)."""
+    """Z [L, V] for request index b; returns (out, accept_len, acc_margin, draw_margin)."""
     Z = _c(Z)
     L, V = Z.shape
     path = _c(path, np.int32)
@@ -262,7 +262,7 @@ def path_sample(S, ids, T: float, seed: int, b: int = 0):
 
 def verify_proposal(Z, path, cand, q, pidx, T: float, seed: int, b: int = 0):
     """Z [L, V]; the proposal's candidates cand [P, K], distributions q [P, K] and drawn
-    indices pidx [P]: (out, accept_len, acc_margin, gumbel_margin)."""
+    indices pidx [P]: (out, accept_len, acc_margin, draw_margin)."""
     Z = _c(Z)
     L, V = Z.shape
     cand = _c(cand, np.int32)
@@ -386,10 +386,10 @@ def select_verify(h, W, Wg, A, Bt, x0, Z, *, K: int = 16, path_mode: int = 0,
         "topk_gap": np.empty((n, P), np.float64),
         "path_margin": np.empty(n, np.float64),
         "acc_margin": np.empty(n, np.float64),
-        "gumbel_margin": np.empty(n, np.float64),
+        "draw_margin": np.empty(n, np.float64),
     }
     order = ["cand_ids", "cand_U", "gate", "S", "path", "path_score", "out_tokens", "accept_len",
-             "topk_gap", "path_margin", "acc_margin", "gumbel_margin"]
+             "topk_gap", "path_margin", "acc_margin", "draw_margin"]
     if Wq is not None:
         Wq = _c(Wq, np.uint8)
         w_scale = _c(w_scale, np.float32)

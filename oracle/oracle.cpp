@@ -112,7 +112,7 @@ inline double u01(uint64_t x) {
  *   key     = (seed, 0)
  *   accept  : counter (0, t, b, 0), word 0           -- position t = 1..L-1
  *   chunk   : counter (0, t, b, 2), word 0           -- the redraw's chunk choice
- *   gumbel  : counter (v >> 2, t, b, 1), word v & 3  -- the redraw within the chunk
+ *   inchunk : counter (0, t, b, 1), word 0           -- the redraw within the chunk
  *   path    : counter (0, t, b, 3), word 0           -- the sampled path's draw at t
  * The redraw from row t-1 uses position t; the bonus row L-1 uses t = L. */
 double uniform_counter(uint64_t seed, int64_t b, int t, uint64_t idx, uint64_t stream, int word) {
@@ -125,9 +125,7 @@ double uniform_counter(uint64_t seed, int64_t b, int t, uint64_t idx, uint64_t s
 
 double uniform_accept(uint64_t seed, int64_t b, int t) { return uniform_counter(seed, b, t, 0, 0, 0); }
 
-double uniform_gumbel(uint64_t seed, int64_t b, int t, int64_t v) {
-  return uniform_counter(seed, b, t, static_cast<uint64_t>(v) >> 2, 1, static_cast<int>(v & 3));
-}
+double uniform_inchunk(uint64_t seed, int64_t b, int t) { return uniform_counter(seed, b, t, 0, 1, 0); }
 
 double uniform_chunk(uint64_t seed, int64_t b, int t) { return uniform_counter(seed, b, t, 0, 2, 0); }
 
@@ -145,39 +143,40 @@ double row_lse(const void* Z, int zdtype, int64_t off, int64_t V, double T) {
   return m + std::log(s);
 }
 
-/* Gumbel-max draw from softmax(z/T) restricted to v in [lo, hi), v != excl:
- * argmax_v z_v/T + G_v with G_v = -log(-log U_v). The argmax of independent
- * Gumbel-perturbed logits is an exact sample from the renormalised softmax
- * (Gumbel 1954; the Gumbel-max trick). Returns the token and the relative gap
- * between the two largest keys. */
-int64_t gumbel_argmax(const void* Z, int zdtype, int64_t off, int64_t lo, int64_t hi, double T,
-                      uint64_t seed, int64_t b, int t, int64_t excl, double* rel_gap) {
-  int64_t best = -1;
-  double bk = -kInf, second = -kInf;
-  for (int64_t v = lo; v < hi; ++v) {
-    if (v == excl) continue;
-    double g = -std::log(-std::log(uniform_gumbel(seed, b, t, v)));
-    double key = widen(Z, zdtype, off + v) / T + g;
-    if (best < 0 || key > bk) {  // v increases, so strict '>' keeps the lower id on ties
-      second = bk;
-      bk = key;
-      best = v;
-    } else {
-      second = std::max(second, key);
-    }
+/* Inverse-CDF draw over the weights w[0..n) (w >= 0) with one uniform u: the first index
+ * whose cumulative weight exceeds u * sum(w) (in index order); if rounding leaves none, the
+ * last index with weight. Returns -1 when every weight is zero. margin = the smallest
+ * distance of the target u * sum(w) to a cumulative boundary, relative to the sum. */
+int64_t inverse_cdf(const std::vector<double>& w, double u, double* margin) {
+  double total = 0.0;
+  int64_t last = -1;
+  for (size_t i = 0; i < w.size(); ++i) {
+    total += w[i];
+    if (w[i] > 0.0) last = static_cast<int64_t>(i);
   }
-  *rel_gap = (second == -kInf) ? kInf : rel(bk - second, bk);
-  return best;
+  *margin = kInf;
+  if (last < 0) return -1;
+  const double target = u * total;
+  double cum = 0.0;
+  int64_t pick = -1;
+  for (size_t i = 0; i < w.size(); ++i) {
+    if (!(w[i] > 0.0)) continue;
+    cum += w[i];
+    *margin = std::min(*margin, std::fabs(cum - target) / total);
+    if (pick < 0 && cum > target) pick = static_cast<int64_t>(i);
+  }
+  return pick < 0 ? last : pick;
 }
 
 /* An exact draw from p = softmax(z/T) with token excl removed (excl < 0: none) and
  * renormalised, in two stages: (1) a chunk of kRedrawChunk consecutive tokens is chosen
  * with probability proportional to its mass under the residual distribution, by one
  * uniform against the chunks' cumulative masses in vocabulary order (if rounding leaves
- * no chunk above the target, the last chunk with mass is taken); (2) the token is the
- * Gumbel-max over that chunk. P(v) = (mass_c / total) (p_v / mass_c) = p_v / total.
- * margin = the smaller of the chunk choice's relative distance to a cumulative boundary
- * and the Gumbel draw's relative top-2 gap. */
+ * no chunk above the target, the last chunk with mass is taken); (2) the token, by a second
+ * uniform against the cumulative masses of the chunk's tokens in vocabulary order (the
+ * inverse CDF, exact like the first stage). P(v) = (mass_c / total) (p_v / mass_c) =
+ * p_v / total. margin = the smaller of the two stages' relative distances to a cumulative
+ * boundary. */
 int64_t redraw(const void* Z, int zdtype, int64_t off, int64_t V, double T, uint64_t seed,
                int64_t b, int t, int64_t excl, double* margin) {
   double m = -kInf;
@@ -199,21 +198,21 @@ int64_t redraw(const void* Z, int zdtype, int64_t off, int64_t V, double T, uint
     if (pick < 0 && cum > target) pick = c;
   }
   if (pick < 0) pick = last_nonzero;
-  double gmargin;
-  const int64_t y = gumbel_argmax(Z, zdtype, off, pick * kRedrawChunk,
-                                  std::min(V, (pick + 1) * kRedrawChunk), T, seed, b, t, excl,
-                                  &gmargin);
-  *margin = std::min(cmargin, gmargin);
-  return y;
+  const int64_t lo = pick * kRedrawChunk, hi = std::min(V, (pick + 1) * kRedrawChunk);
+  std::vector<double> w(hi - lo);
+  for (int64_t v = lo; v < hi; ++v) w[v - lo] = (v != excl) ? std::exp(widen(Z, zdtype, off + v) / T - m) : 0.0;
+  double imargin;
+  const int64_t y = inverse_cdf(w, uniform_inchunk(seed, b, t), &imargin);
+  *margin = std::min(cmargin, imargin);
+  return y < 0 ? lo : lo + y;
 }
 
 /* An exact draw from the residual r(v) = max(0, p(v) - q(v)) renormalised, with
  * p = softmax(z/T) over the row and q a proposal that is nonzero only on the K listed
  * candidates (cand[k] with probability qv[k]); K = 0 draws from p itself. The same two
- * stages as redraw(): a chunk by its residual mass, then the Gumbel-max over the chunk of
- * log r(v) + G_v. For a proposal that puts all its mass on one token this is redraw()
- * with that token excluded (the keys differ from redraw()'s by the constant log-sum-exp
- * of the row). */
+ * stages as redraw(): a chunk by its residual mass, then the inverse CDF of r over the
+ * chunk. For a proposal that puts all its mass on one token this is redraw() with that
+ * token excluded (the weights differ from redraw()'s by the row's constant normaliser). */
 int64_t redraw_residual(const void* Z, int zdtype, int64_t off, int64_t V, double T, uint64_t seed,
                         int64_t b, int t, const int32_t* cand, const double* qv, int K,
                         double* margin) {
@@ -241,23 +240,13 @@ int64_t redraw_residual(const void* Z, int zdtype, int64_t off, int64_t V, doubl
     if (pick < 0 && cum > target) pick = c;
   }
   if (pick < 0) pick = last_nonzero;
-  int64_t best = -1;
-  double bk = -kInf, second = -kInf;
-  for (int64_t v = pick * kRedrawChunk; v < std::min(V, (pick + 1) * kRedrawChunk); ++v) {
-    const double rv = resid(v);
-    if (!(rv > 0.0)) continue;
-    const double key = std::log(rv) - std::log(-std::log(uniform_gumbel(seed, b, t, v)));
-    if (best < 0 || key > bk) {
-      second = bk;
-      bk = key;
-      best = v;
-    } else {
-      second = std::max(second, key);
-    }
-  }
-  const double gmargin = (second == -kInf) ? kInf : rel(bk - second, bk);
-  *margin = std::min(cmargin, gmargin);
-  return best;
+  const int64_t lo = pick * kRedrawChunk, hi = std::min(V, (pick + 1) * kRedrawChunk);
+  std::vector<double> w(hi - lo);
+  for (int64_t v = lo; v < hi; ++v) w[v - lo] = resid(v);
+  double imargin;
+  const int64_t y = inverse_cdf(w, uniform_inchunk(seed, b, t), &imargin);
+  *margin = std::min(cmargin, imargin);
+  return y < 0 ? lo : lo + y;
 }
 
 /* ---- E4M3, the OCP 8-bit floating-point format ("OCP 8-bit Floating Point
@@ -585,11 +574,11 @@ int orc_verify_greedy(int zdtype, const void* Z, int L, int64_t V, const int32_t
  * with x_t removed and renormalised and stop (accept_len = t); when all are
  * accepted emit a bonus draw from p_{L-1} (accept_len = L). Draws use the
  * two-stage redraw above.
- * acc_margin = smallest |U - p| / p over the tests made; gum_margin = the
+ * acc_margin = smallest |U - p| / p over the tests made; draw_margin = the
  * redraw's margin. b is the request's batch index (part of the counter). */
 int orc_verify_sampling(int zdtype, const void* Z, int L, int64_t V, const int32_t* path,
                         double T, uint64_t seed, int64_t b, int32_t* out, int32_t* accept_len,
-                        double* acc_margin, double* gum_margin) {
+                        double* acc_margin, double* draw_margin) {
   if (L < 2 || V < 2 || !(T > 0.0)) return -1;
   for (int i = 0; i < L; ++i) out[i] = -1;
   double am = kInf;
@@ -603,13 +592,13 @@ int orc_verify_sampling(int zdtype, const void* Z, int L, int64_t V, const int32
       out[t - 1] = static_cast<int32_t>(x);
       continue;
     }
-    out[t - 1] = static_cast<int32_t>(redraw(Z, zdtype, off, V, T, seed, b, t, x, gum_margin));
+    out[t - 1] = static_cast<int32_t>(redraw(Z, zdtype, off, V, T, seed, b, t, x, draw_margin));
     *accept_len = t;
     *acc_margin = am;
     return 0;
   }
   const int64_t off = static_cast<int64_t>(L - 1) * V;
-  out[L - 1] = static_cast<int32_t>(redraw(Z, zdtype, off, V, T, seed, b, L, -1, gum_margin));
+  out[L - 1] = static_cast<int32_t>(redraw(Z, zdtype, off, V, T, seed, b, L, -1, draw_margin));
   *accept_len = L;
   *acc_margin = am;
   return 0;
@@ -685,7 +674,7 @@ int orc_path_sample(int P, int K, const double* S, const int32_t* ids, double T,
 int orc_verify_proposal(int zdtype, const void* Z, int L, int64_t V, const int32_t* path,
                         const int32_t* cand, const double* q, const int32_t* pidx, int K, double T,
                         uint64_t seed, int64_t b, int32_t* out, int32_t* accept_len,
-                        double* acc_margin, double* gum_margin) {
+                        double* acc_margin, double* draw_margin) {
   if (L < 2 || V < 2 || K < 1 || !(T > 0.0)) return -1;
   for (int i = 0; i < L; ++i) out[i] = -1;
   double am = kInf;
@@ -704,14 +693,14 @@ int orc_verify_proposal(int zdtype, const void* Z, int L, int64_t V, const int32
     out[t - 1] = static_cast<int32_t>(redraw_residual(Z, zdtype, off, V, T, seed, b, t,
                                                       cand + static_cast<int64_t>(t - 1) * K,
                                                       q + static_cast<int64_t>(t - 1) * K, K,
-                                                      gum_margin));
+                                                      draw_margin));
     *accept_len = t;
     *acc_margin = am;
     return 0;
   }
   const int64_t off = static_cast<int64_t>(L - 1) * V;
   out[L - 1] = static_cast<int32_t>(
-      redraw_residual(Z, zdtype, off, V, T, seed, b, L, nullptr, nullptr, 0, gum_margin));
+      redraw_residual(Z, zdtype, off, V, T, seed, b, L, nullptr, nullptr, 0, draw_margin));
   *accept_len = L;
   *acc_margin = am;
   return 0;
@@ -763,7 +752,7 @@ int orc_select_verify(int dtype, int zdtype, const void* h, const void* W, const
                       double T, uint64_t seed, const int64_t* reqs, int64_t nreq, int nthreads,
                       int32_t* cand_ids, double* cand_U, double* gate, double* S, int32_t* path,
                       double* path_score, int32_t* out, int32_t* accept_len, double* topk_gap,
-                      double* path_margin, double* acc_margin, double* gum_margin,
+                      double* path_margin, double* acc_margin, double* draw_margin,
                       const uint8_t* Wq, const float* w_scale) {
   if (L < 2 || K < 1 || V < K || B < 1) return -1;
   const int P = L - 1;
@@ -806,14 +795,14 @@ int orc_select_verify(int dtype, int zdtype, const void* h, const void* W, const
     const char* zb = static_cast<const char*>(Z) +
                      b * static_cast<int64_t>(L) * V * (zdtype == ORC_BF16 ? 2 : 4);
     acc_margin[q] = kInf;
-    gum_margin[q] = kInf;
+    draw_margin[q] = kInf;
     if (sampled)
       rc = orc_verify_proposal(zdtype, zb, L, V, path + q * P, ids, qprop.data(), pidx.data(), K,
                                T, seed, b, out + q * L, accept_len + q, acc_margin + q,
-                               gum_margin + q);
+                               draw_margin + q);
     else if (T > 0.0)
       rc = orc_verify_sampling(zdtype, zb, L, V, path + q * P, T, seed, b, out + q * L,
-                               accept_len + q, acc_margin + q, gum_margin + q);
+                               accept_len + q, acc_margin + q, draw_margin + q);
     else
       rc = orc_verify_greedy(zdtype, zb, L, V, path + q * P, out + q * L, accept_len + q);
     if (rc != 0) return rc;

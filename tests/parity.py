@@ -9,8 +9,9 @@ the case is excluded from the exact comparison and counted):
     downstream of it:
       - top-16 set of a row: boundary gap u_16 - u_17 < TOPK_GAP * |u_16|;
       - path: smallest relative best-vs-second margin on the path < PATH_MARGIN;
-      - sampling: an accept test with |U - p| / p < ACC_MARGIN, or a Gumbel draw whose
-        two best keys differ by < GUMBEL_MARGIN (relative);
+      - sampling: an accept test with |U - p| / p < ACC_MARGIN, or a redraw whose target
+        lies within DRAW_MARGIN (relative to the total) of a cumulative boundary, in the
+        chunk choice or within the chunk;
   * everywhere else token ids, paths and accept lengths must be identical.
 """
 from __future__ import annotations
@@ -25,7 +26,7 @@ SCORE_RTOL = 1e-3
 TOPK_GAP = 1e-3
 PATH_MARGIN = 1e-3
 ACC_MARGIN = 1e-4
-GUMBEL_MARGIN = 1e-4
+DRAW_MARGIN = 1e-4
 GATE_ATOL = 1e-4
 
 

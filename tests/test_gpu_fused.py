@@ -10,7 +10,7 @@ import torch
 
 from draft_speculative_decoding_gb300 import binding
 from draft_speculative_decoding_gb300 import workloads as wl
-from parity import (ACC_MARGIN, GUMBEL_MARGIN, PATH_MARGIN, TOPK_GAP, close, dims_for,
+from parity import (ACC_MARGIN, DRAW_MARGIN, PATH_MARGIN, TOPK_GAP, close, dims_for,
                     np_inputs, reorder_S_to, to_cpu)
 
 pytestmark = pytest.mark.gpu
@@ -81,7 +81,7 @@ def _compare(g, o, spec, reqs, T):
         same = (g["accept_len"][b] == o["accept_len"][q]
                 and g["out_tokens"][b].tolist() == o["out_tokens"][q].tolist())
         if not same:
-            assert T > 0 and (o["acc_margin"][q] < ACC_MARGIN or o["gumbel_margin"][q] < GUMBEL_MARGIN), \
+            assert T > 0 and (o["acc_margin"][q] < ACC_MARGIN or o["draw_margin"][q] < DRAW_MARGIN), \
                 f"request {b}: verification differs without a near-tie"
             diverged += 1
     return diverged
