@@ -30,34 +30,6 @@ __device__ __forceinline__ void philox4x64_10(uint64_t (&c)[4], uint64_t k0, uin
   }
 }
 
-// N independent Philox4x64-10 evaluations under one key, round by round across the N
-// counters so that their multiply chains overlap (the same function as N separate calls).
-template <int N>
-__device__ __forceinline__ void philox4x64_10_n(uint64_t (&c)[N][4], uint64_t k0, uint64_t k1) {
-  constexpr uint64_t kM0 = 0xD2E7470EE14C6C93ull;
-  constexpr uint64_t kM1 = 0xCA5A826395121157ull;
-  constexpr uint64_t kW0 = 0x9E3779B97F4A7C15ull;
-  constexpr uint64_t kW1 = 0xBB67AE8584CAA73Bull;
-#pragma unroll
-  for (int round = 0; round < 10; ++round) {
-    if (round > 0) {
-      k0 += kW0;
-      k1 += kW1;
-    }
-#pragma unroll
-    for (int j = 0; j < N; ++j) {
-      const uint64_t lo0 = kM0 * c[j][0], hi0 = __umul64hi(kM0, c[j][0]);
-      const uint64_t lo1 = kM1 * c[j][2], hi1 = __umul64hi(kM1, c[j][2]);
-      const uint64_t n0 = hi1 ^ c[j][1] ^ k0;
-      const uint64_t n2 = hi0 ^ c[j][3] ^ k1;
-      c[j][0] = n0;
-      c[j][1] = lo1;
-      c[j][2] = n2;
-      c[j][3] = lo0;
-    }
-  }
-}
-
 // Uniform (2j+1) * 2^-24 with j = the top 23 bits of the word: exact in fp32.
 __device__ __forceinline__ float u01_from_word(uint64_t w) {
   return static_cast<float>(2u * static_cast<uint32_t>(w >> 41) + 1u) * 0x1p-24f;
@@ -66,6 +38,14 @@ __device__ __forceinline__ float u01_from_word(uint64_t w) {
 // Accept-test uniform of draft position t of request b: counter (0, t, b, 0), word 0.
 __device__ __forceinline__ float uniform_accept(uint64_t seed, int b, int t) {
   uint64_t c[4] = {0ull, static_cast<uint64_t>(t), static_cast<uint64_t>(b), 0ull};
+  philox4x64_10(c, seed, 0ull);
+  return u01_from_word(c[0]);
+}
+
+// In-chunk uniform of the redraw for draft position t of request b (the token within the
+// chosen chunk, by inverse CDF): counter (0, t, b, 1), word 0.
+__device__ __forceinline__ float uniform_inchunk(uint64_t seed, int b, int t) {
+  uint64_t c[4] = {0ull, static_cast<uint64_t>(t), static_cast<uint64_t>(b), 1ull};
   philox4x64_10(c, seed, 0ull);
   return u01_from_word(c[0]);
 }

@@ -116,14 +116,6 @@ __device__ __forceinline__ unsigned long long pack_key(float v, int id) {
   return (static_cast<unsigned long long>(o) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(id));
 }
 
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const unsigned long long o = __shfl_xor_sync(0xffffffffu, k, off);
-    k = o > k ? o : k;
-  }
-  return k;
-}
 
 // ------------------------------------------------------------------ target rows
 // One block of 128 threads reduces kZChunk (4096) elements of one row of Z: each thread
@@ -613,12 +605,15 @@ struct VerifySmem {
   int ry[kMaxL];
   int info[4];
   float uc[kMaxL];                 // chunk-choice uniform of each possible redraw row
+  float ui[kMaxL];                 // in-chunk uniform of each possible redraw row
   float mass[kMaxZChunks];         // cumulative residual mass over chunks
-  unsigned long long gk[kTailThreads / 32];
+  float wsum[kTailThreads / 32];   // in-chunk weight of each warp's tokens
+  int wpick[kTailThreads / 32];    // each warp's first token past the target
+  int wlast[kTailThreads / 32];    // each warp's last token with weight
   // sampled proposals: the rejected position's candidates in the chosen chunk
   uint32_t inchunk[kZChunk / 32];  // bit j: token lo + j is a candidate
   int cand[kK];                    // candidate ids
-  float cadj[kK];                  // log(max(0, 1 - q/p)) added to the candidate's key
+  float cfac[kK];                  // max(0, 1 - q/p): the candidate's residual weight factor
   float take[kK];                  // min(p, q) of each candidate on the chunk-mass scale
 };
 
@@ -685,7 +680,10 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
         ok = uniform_accept(a.seed, b, lane + 1) < p / qx;
       }
     }
-    if (soft && lane < L) vs.uc[lane] = uniform_chunk(a.seed, b, lane + 1);
+    if (soft && lane < L) {
+      vs.uc[lane] = uniform_chunk(a.seed, b, lane + 1);
+      vs.ui[lane] = uniform_inchunk(a.seed, b, lane + 1);
+    }
     const unsigned fail = __ballot_sync(0xffffffffu, lane < P && !ok);
     const int n = fail ? __ffs(fail) - 1 : P;  // accepted drafts
     if (lane < L && (lane != n || !soft))
@@ -710,7 +708,7 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
     // sampled: mass each candidate takes out of its chunk, min(p, q) on the chunk scale
     // (unnormalised exp((z - M)/T), whose row total is exp(rl)); lane k holds candidate k
     int ck = -1;
-    float take = 0.f, cadj = 0.f;
+    float take = 0.f, cfac = 0.f;
     if (sampled && lane < kK) {
       ck = prop_cand[n * kK + lane];
       const float qk = prop_q[n * kK + lane];
@@ -718,12 +716,12 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
         const float zk = load1(a.Z, is_bf16, grow * a.V + ck);
         const float pk = expf((zk - M) * inv_T - vs.rl[n]);
         take = fminf(pk, qk) * expf(vs.rl[n]);
-        cadj = qk < pk ? log1pf(-qk / pk) : -INFINITY;
+        cfac = qk < pk ? 1.f - qk / pk : 0.f;
       } else {
         ck = -1;  // an id outside the vocabulary carries no target mass
       }
       vs.cand[lane] = ck;
-      vs.cadj[lane] = cadj;
+      vs.cfac[lane] = cfac;
       vs.take[lane] = take;
     }
     __syncwarp();
@@ -783,45 +781,71 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
     }
     __syncthreads();
   }
+  // the token within the chunk by inverse CDF: weights exp((z - M)/T) (times the residual
+  // factor of a sampled proposal's candidates; 0 for the excluded token), cumulated in
+  // vocabulary order, against one uniform times their total
   const int v0 = lo + threadIdx.x * 16;  // kZChunk = 16 tokens x 256 threads
-  unsigned long long best = 0ull;
-  if (v0 < hi) {
+  const float M = vs.rm[n];
+  float w[16];
+  float tsum = 0.f;
+  {
     float x[2][8] = {};
-    load8(a.Z, is_bf16, grow * a.V + v0, x[0]);
+    if (v0 < hi) load8(a.Z, is_bf16, grow * a.V + v0, x[0]);
     if (v0 + 8 < hi) load8(a.Z, is_bf16, grow * a.V + v0 + 8, x[1]);
-    uint64_t c[4][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      c[q][0] = static_cast<uint64_t>((v0 >> 2) + q);
-      c[q][1] = static_cast<uint64_t>(n + 1);
-      c[q][2] = static_cast<uint64_t>(b);
-      c[q][3] = 1ull;
-    }
-    philox4x64_10_n<4>(c, a.seed, 0ull);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const int v = v0 + 4 * q + w;
-        bool skip = v >= hi || v == excl;
-        float adj = 0.f;
-        if (sampled && !skip && (vs.inchunk[(v - lo) >> 5] >> ((v - lo) & 31) & 1u)) {
+    for (int j = 0; j < 16; ++j) {
+      const int v = v0 + j;
+      float wt = 0.f;
+      if (v < hi && v != excl) {
+        float fac = 1.f;
+        if (sampled && (vs.inchunk[(v - lo) >> 5] >> ((v - lo) & 31) & 1u))
           for (int k = 0; k < kK; ++k)
-            if (vs.cand[k] == v) adj = vs.cadj[k];
-          skip = adj == -INFINITY;  // q >= p: no residual mass
-        }
-        const float key = x[q >> 1][(q & 1) * 4 + w] * inv_T + adj - logf(-logf(u01_from_word(c[q][w])));
-        const unsigned long long k = pack_key(key, v);
-        if (!skip && k > best) best = k;
+            if (vs.cand[k] == v) fac = vs.cfac[k];
+        wt = expf((x[j >> 3][j & 7] - M) * inv_T) * fac;
       }
+      w[j] = wt;
+      tsum += wt;
+    }
   }
-  best = warp_max_u64(best);
-  if (lane == 0) vs.gk[warp] = best;
+  float incl = tsum;  // inclusive scan over the warp, then over the warps
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) vs.wsum[warp] = incl;
+  __syncthreads();
+  float before = 0.f, total = 0.f;
+#pragma unroll
+  for (int i = 0; i < kTailThreads / 32; ++i) {
+    if (i < warp) before += vs.wsum[i];
+    total += vs.wsum[i];
+  }
+  const float target = vs.ui[n] * total;
+  float cum = before + incl - tsum;
+  int mine = kIntMax, last = -1;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (w[j] > 0.f) {
+      cum += w[j];
+      last = v0 + j;
+      if (mine == kIntMax && cum > target) mine = v0 + j;
+    }
+  mine = __reduce_min_sync(0xffffffffu, mine);
+  last = __reduce_max_sync(0xffffffffu, last);
+  if (lane == 0) {
+    vs.wpick[warp] = mine;
+    vs.wlast[warp] = last;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
-    unsigned long long f = 0ull;
-    for (int w = 0; w < kTailThreads / 32; ++w) f = vs.gk[w] > f ? vs.gk[w] : f;
-    out[n] = static_cast<int>(~static_cast<uint32_t>(f & 0xffffffffu));
+    int pick = kIntMax, lastw = -1;
+    for (int i = 0; i < kTailThreads / 32; ++i) {
+      pick = min(pick, vs.wpick[i]);
+      lastw = max(lastw, vs.wlast[i]);
+    }
+    // rounding left no token past the target: the last with weight; no weight at all: lo
+    out[n] = pick != kIntMax ? pick : (lastw >= 0 ? lastw : lo);
   }
 }
 
