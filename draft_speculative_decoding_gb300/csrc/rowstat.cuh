@@ -8,6 +8,15 @@
 namespace dfs {
 
 constexpr int kIntMaxRs = 0x7fffffff;
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e): exp(y) = 2^(y log2 e)
+
+// 2^x on the special-function unit (ex2.approx.ftz.f32, relative error about 2^-22): one
+// instruction per term of the target rows' sums of exponentials.
+__device__ __forceinline__ float exp2_sfu(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // (max, argmax, sum of exp((z - max) * inv_T)); ties keep the lower index.
 struct RowStat {
@@ -103,6 +112,7 @@ __device__ __forceinline__ void rowstat_fold_bf16(RowStat& st, const uint4 (&q)[
                                                   const int (&v0)[NG], int V, float inv_T) {
   float m = -INFINITY, s = 0.f;
   int mi = kIntMaxRs;
+  const float c = inv_T * kLog2e;  // exp((x - m) / T) = 2^(x c - m c)
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     if (v0[g] >= V) continue;
@@ -120,13 +130,14 @@ __device__ __forceinline__ void rowstat_fold_bf16(RowStat& st, const uint4 (&q)[
         gj = j;
       }
     if (gm > m) {
-      if (kSoft) s *= expf((m - gm) * inv_T);
+      if (kSoft) s *= exp2_sfu((m - gm) * c);
       m = gm;
       mi = v0[g] + gj;
     }
     if (kSoft && m != -INFINITY) {
+      const float mc = m * c;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) s += expf((x[j] - m) * inv_T);
+      for (int j = 0; j < 8; ++j) s += exp2_sfu(fmaf(x[j], c, -mc));
     }
   }
   if (m == -INFINITY) return;
