@@ -74,6 +74,7 @@ struct LmheadParams {
   int stall_mma;                     // test hook: the MMA issuer stays idle
   const float* w_scale;              // E4M3 head: per-vocabulary scale [V]
   const float* h_scale;              // E4M3 head: per-row scale [rows_total]
+  uint32_t h_box_bytes;              // bytes one hidden-row box delivers (k_lmhead_tc, MT = 1)
 };
 
 template <int MT, int NT, int NBUF, int SW, int SH, int CL, int RS>
@@ -241,6 +242,13 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
     tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
     tmem_relinquish();
   }
+  if (MT == 1 && p.h_box_bytes < static_cast<uint32_t>(Cfg::kHBytes)) {
+    // Fewer hidden rows than a tile: the boxes fill only the first rows of each stage, so the
+    // rest is zeroed once (the MMA reads 128 rows; the epilogue skips the padding rows).
+    uint4* hz = reinterpret_cast<uint4*>(hring);
+    for (int i = threadIdx.x; i < SH * Cfg::kHBytes / 16; i += blockDim.x) hz[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();  // generic writes made visible to the tensor cores' reads
+  }
   tc_fence_before();
   __syncthreads();
   if (CL > 1) cluster_sync();  // peers' barriers are initialised before any multicast
@@ -337,7 +345,7 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
             break;
           }
           const uint32_t fb = smem_u32(&hfull[stage]);
-          mbar_arrive_expect_tx(fb, Cfg::kHBytes);
+          mbar_arrive_expect_tx(fb, MT == 1 ? p.h_box_bytes : static_cast<uint32_t>(Cfg::kHBytes));
           const uint32_t sa = smem_u32(hring + size_t(stage) * Cfg::kHBytes);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
@@ -992,7 +1000,11 @@ bool lmhead_row_split(int rows_total, int variant, int G) {
 cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
   LmheadParams prm;
   memset(&prm, 0, sizeof(prm));
-  if (!encode_bf16_2d(&prm.tm_h, a.hidden, a.d, a.rows_total, 64, 128))
+  // A row group smaller than a tile is fetched as one box of its rows rounded up to 8 (the
+  // single-CTA kernel zeroes the rest once); larger groups take 128-row boxes.
+  const int h_rows = a.rows_total <= 128 ? ((a.rows_total + 7) / 8) * 8 : 128;
+  prm.h_box_bytes = static_cast<uint32_t>(h_rows) * 128u;
+  if (!encode_bf16_2d(&prm.tm_h, a.hidden, a.d, a.rows_total, 64, h_rows))
     return cudaErrorInvalidValue;
   // Dummy-but-valid maps when a tile kind is not used, so every map is well formed.
   if (!encode_bf16_2d(&prm.tm_w, a.vocab ? a.W : a.hidden, a.vocab ? a.V : a.d,
@@ -1071,6 +1083,7 @@ cudaError_t launch_lmhead_e4m3(const LmheadLaunch& a, cudaStream_t s) {
   if (!encode_u8_2d(&prm.tm_w, a.Wq, a.d, a.V, 128, 128)) return cudaErrorInvalidValue;
   // gate tiles stay bf16: the bf16 rows and W_g (128 W_g rows per CTA of a pair)
   if (!encode_bf16_2d(&prm.tm_h, a.hidden, a.d, a.rows_total, 64, 128)) return cudaErrorInvalidValue;
+  prm.h_box_bytes = 128u * 128u;
   if (!encode_bf16_2d(&prm.tm_g, a.gate ? a.Wg : a.hidden, a.d, a.gate ? a.r : a.rows_total, 64,
                       128))
     return cudaErrorInvalidValue;
