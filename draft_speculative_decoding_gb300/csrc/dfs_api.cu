@@ -624,7 +624,8 @@ namespace {
 
 int check_conv(int B, int L, int d) {
   if (B < 1 || L < 1 || d < 64) return DFS_ERR_INVALID;
-  if (d % 64 != 0 || d > 16384 || static_cast<long long>(B) * L > (1LL << 24)) return DFS_ERR_UNSUPPORTED;
+  // rows index the GEMM's second grid dimension in 128-row tiles (at most 65535 of them)
+  if (d % 64 != 0 || d > 16384 || static_cast<long long>(B) * L > (1LL << 22)) return DFS_ERR_UNSUPPORTED;
   return DFS_OK;
 }
 

@@ -261,7 +261,8 @@ int dfs_next_tokens(int B, int L, const int32_t* out_tokens, const int32_t* acce
  * x: [B][L][d] bf16; base: [2][d] fp32; Wc: [d/8][d] bf16; out: [B][L][d] bf16, all device
  * memory owned by the caller, 16-byte aligned; out must not overlap x. Correction sums are
  * fp32 (tensor cores, summed over K splits in a fixed order: results repeat bit for bit);
- * the output is rounded to bf16 once. d a multiple of 64, at most 16384; L >= 1.
+ * the output is rounded to bf16 once. d a multiple of 64, at most 16384; L >= 1; B*L at most
+ * 2^22 (DFS_ERR_UNSUPPORTED beyond).
  * ws: dfs_conv2tap_workspace_size(B, L, d) bytes (the error word and fp32 partial sums),
  * 16-byte aligned, initialised once with dfs_workspace_init; dfs_get_device_error reads its
  * error word. Asynchronous on `stream`: two kernels, the second a programmatic dependent. */
