@@ -63,6 +63,7 @@ int check_dims(const dfs_dims* d) {
   if (d->r % 8 != 0 || d->r > dfs::kMaxRank) return DFS_ERR_UNSUPPORTED;
   if (d->dtype == DFS_BF16 && d->d % 64 != 0) return DFS_ERR_UNSUPPORTED;
   if (static_cast<long long>(d->B) * d->L > (1LL << 30)) return DFS_ERR_UNSUPPORTED;
+  if (d->B > 65535) return DFS_ERR_UNSUPPORTED;  // requests index the tail's second grid dimension
   return DFS_OK;
 }
 

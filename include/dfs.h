@@ -31,7 +31,8 @@
  *     calls that share a workspace and may run concurrently on the GPU race.
  *   * Token ids are int32 in [0, V). Ties: among equal values the lower token id
  *     wins, in every argmax (top-K order, path steps, target argmax, draws).
- *   * K must be 16. 2 <= L <= 16. Block row 0 of each request holds the verified
+ *   * K must be 16. 2 <= L <= 16, 1 <= B <= 65535 (DFS_ERR_UNSUPPORTED beyond).
+ *     Block row 0 of each request holds the verified
  *     slot (the last verified token x0); rows 1..L-1 are the draft positions, so a
  *     request proposes L-1 tokens.
  *   * Return value: DFS_OK, or a negative dfs_status. Argument errors are found
