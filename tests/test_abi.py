@@ -61,3 +61,25 @@ def test_host_only_calls(lib):
                                7, ctypes.c_void_p(0x3000), None, None) == binding.DFS_ERR_INVALID
     # calls rejected on the host launch nothing
     assert binding.dfs_launch_count() == launches
+
+
+def test_host_limits_of_the_convolution_and_the_hand_off(lib):
+    launches = binding.dfs_launch_count()
+    ws = lib.dfs_conv2tap_workspace_size
+    assert ws(32, 8, 5120) > 256                  # error word + partial sums
+    assert ws(2, 4, 96) == 0                      # d not a multiple of 64
+    assert ws(1, 1, 32) == 0                      # d below 64
+    assert ws(1 << 12, 1 << 11, 64) == 0          # more than 2^22 rows
+    assert ws(1 << 11, 1 << 11, 64) > 0
+    P = ctypes.c_void_p
+    assert lib.dfs_conv2tap(2, 4, 96, P(0x1000), P(0x2000), P(0x3000), P(0x4000), P(0x5000),
+                            1 << 20, None) == binding.DFS_ERR_UNSUPPORTED
+    # out overlapping x is an argument error, found before anything is enqueued
+    assert lib.dfs_conv2tap(2, 4, 128, P(0x10000), P(0x2000), P(0x3000), P(0x10100), P(0x5000),
+                            1 << 20, None) == binding.DFS_ERR_INVALID
+    assert lib.dfs_next_tokens(0, 8, P(0x1000), P(0x2000), P(0x3000), None) == binding.DFS_ERR_INVALID
+    assert lib.dfs_next_tokens(4, 17, P(0x1000), P(0x2000), P(0x3000), None) == binding.DFS_ERR_INVALID
+    big = binding.make_dims(65536, 2, 1024, 256, 32, 0, 0)  # more requests than the grid holds
+    assert lib.dfs_path_select(ctypes.byref(big), None, None, 0, None, None, None) == \
+        binding.DFS_ERR_UNSUPPORTED
+    assert binding.dfs_launch_count() == launches
