@@ -251,11 +251,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D (M = 128 per CTA; M = 256 for
 // an MMA across a CTA pair).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int n, bool b_mn_major, int m = 128) {
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int n, bool b_mn_major, int m = 128,
+                                                      bool a_mn_major = false) {
   return (1u << 4)                          // D format: f32
          | (1u << 7)                        // A format: bf16
          | (1u << 10)                       // B format: bf16
-         | (0u << 15)                       // A K-major
+         | ((a_mn_major ? 1u : 0u) << 15)   // A major-ness
          | ((b_mn_major ? 1u : 0u) << 16)   // B major-ness
          | (static_cast<uint32_t>(n >> 3) << 17)
          | (static_cast<uint32_t>(m >> 4) << 24);
@@ -298,6 +299,46 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
       "bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// 3D tiled load (c0 innermost) into this CTA's shared memory, counted on the barrier at
+// shared::cluster address `bar` (this CTA's or its pair peer's). The box lands densely, its
+// outer dimensions flattened into consecutive rows of the innermost one.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap, uint32_t bar,
+                                                 int c0, int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// 16 bytes from shared::cluster address `addr` (this CTA's or a peer's shared memory).
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Named barrier `id` over `count` threads (whole warps).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// The same barrier, returning whether `pred` held in every participating thread.
+__device__ __forceinline__ bool named_bar_and(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // Tensor memory for pair MMAs: one warp of each CTA of the pair executes these together.

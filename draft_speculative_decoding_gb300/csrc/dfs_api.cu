@@ -33,12 +33,16 @@ int device_sm_count() {
   return cache[dev];
 }
 
-// Tile-shape choice for row groups of 129..256 rows: 5 (default) = CTA pairs with pair MMAs,
-// each CTA staging half of the W tile; 4 = CTA pairs with per-CTA MMAs sharing each W tile
-// by multicast. Read from DFS_LMHEAD_VARIANT on each call, for tuning.
+// Tile-shape choice for calls of more than 128 rows: 0 (default) = the vocabulary-major pair
+// kernel where it needs fewer passes over W, else the row-major pair kernel; 6 = always the
+// vocabulary-major pair kernel (pair MMAs over 256 vocabulary entries x the drafted rows);
+// 5 = always the row-major pair kernel (256 rows x 256 vocabulary columns, each CTA staging
+// half of the W tile); 4 = CTA pairs with per-CTA MMAs sharing each W tile by multicast.
+// Read from DFS_LMHEAD_VARIANT on each call, for tuning.
 int lmhead_variant_override() {
   const char* s = std::getenv("DFS_LMHEAD_VARIANT");
-  return (s != nullptr && std::atoi(s) == 4) ? 4 : 5;
+  const int v = s != nullptr ? std::atoi(s) : 0;
+  return (v == 4 || v == 5 || v == 6) ? v : 0;
 }
 
 struct Layout {

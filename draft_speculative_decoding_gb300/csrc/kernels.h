@@ -29,9 +29,11 @@ struct LmheadLaunch {
   int G;               // grid of the vocabulary launch = lists per row
   float* gate_out;     // [rows_total][r]
   int* err;
-  int lmhead_variant;  // row groups of 129..256 rows: 5 = CTA pairs with pair MMAs (each
-                       // CTA stages half of the W tile); 4 = CTA pairs with per-CTA MMAs
-                       // (the W tile multicast to both)
+  int lmhead_variant;  // more than 128 rows: 0 = 6 where it needs fewer passes over W,
+                       // else 5; 6 = CTA pairs with pair MMAs over 256 vocabulary entries x
+                       // the drafted rows of up to 2 nb requests; 5 = pair MMAs over 256-row
+                       // groups (each CTA stages half of the W tile); 4 = per-CTA MMAs (the
+                       // W tile multicast to both)
   int cluster;         // CTAs per cluster sharing hidden-row tiles by multicast (1, 2 or 4)
   // Test hooks: the limit of every bounded wait (0: the default), and a switch that keeps the
   // MMA issuer idle so that the other roles' waits run out and report DFS_ERR_TIMEOUT.

@@ -32,6 +32,8 @@
 // (cta_group::2, M = 256 x N = 256 across two SMs): each CTA stages only half of the W tile,
 // which halves the shared-memory bytes per MMA -- at 256 rows the tensor pipe must run near
 // full rate alongside the HBM stream, and shared-memory bandwidth, not HBM, was the limit.
+// k_lmhead_vt is the pair kernel with vocabulary on M and only the drafted rows on N, for
+// calls where that saves whole passes over W.
 // Every mbarrier wait is bounded; on expiry the kernel sets the error word, stops all
 // roles, and frees its tensor memory.
 #include <cuda.h>
@@ -75,6 +77,10 @@ struct LmheadParams {
   const float* w_scale;              // E4M3 head: per-vocabulary scale [V]
   const float* h_scale;              // E4M3 head: per-row scale [rows_total]
   uint32_t h_box_bytes;              // bytes one hidden-row box delivers (k_lmhead_tc, MT = 1)
+  // k_lmhead_vt: the drafted rows of requests b0 .. b0 + 2 nb - 1 (nb per CTA of a pair)
+  CUtensorMap tm_h3;     // hidden as [B][L][d], box 64 (k) x (L - 1) (positions 1..) x nb
+  int b0, nb, n_req;     // first request of the group, requests per CTA, requests in total
+  uint32_t stage_bytes;  // one ring stage: 128 A rows + the group's drafted rows, 64 k each
 };
 
 template <int MT, int NT, int NBUF, int SW, int SH, int CL, int RS>
@@ -823,6 +829,386 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
   cluster_sync();  // neither CTA leaves while its peer may still use the pair's resources
 }
 
+// ------------------------------------------------------------------ vocabulary-major tiles
+// The same pair MMAs with the operands' roles exchanged: 256 vocabulary entries (or W_g
+// rows) on M -- 128 in each CTA's TMEM lanes, W read MN-major exactly as the pair kernel
+// stages it -- and the group's drafted rows on N. A block's verified slot (position 0) has
+// no drafted token, so it needs no logits: each CTA fetches the rows of positions 1..L-1 of
+// its nb requests as one 3-D box of h viewed as [B][L][d], and N = 2 nb (L - 1) (224 at 32
+// blocks of 8) instead of the 256 rows the row-major tiles compute. The real gain is in
+// passes over W: a group holds 2 nb requests whatever L is, so where B L rows exceed a
+// multiple of 256 only because of the verified slots (32 blocks of 9: 288 rows, 256 drafted)
+// one pass replaces two. At 32 blocks of 8 (one pass either way) the row-major kernel stays
+// the faster: the turn-around below costs more than the 1/8 of tensor work it saves.
+//
+// Each CTA's accumulator holds 128 vocabulary entries (lanes) x N drafted rows (columns),
+// but the keep-top-16 is per row over the vocabulary, i.e. across lanes. The epilogue
+// therefore turns the rows around in shared memory, four 32-row chunks per round: all four
+// epilogue warps load their lane quarter of the round's chunks with tcgen05.ld and store them
+// as [row][vocabulary] (rows padded to 129 floats), then warp q reads back chunk q of the
+// round, one row per thread and 128 consecutive vocabulary entries in increasing id order,
+// and offers them to the row's sorted top-16 in registers (a thread owns rows 32 q + lane
+// and 128 + 32 q + lane), so the four warps rank in parallel. Two named barriers per round
+// order the stores, the reads and the next round's stores.
+// At the end the odd CTA's lists (its 128 vocabulary entries per tile) are read by the
+// leader through distributed shared memory and merged by (value desc, id asc) into one
+// partial list per row and pair, the layout the tail reads.
+template <int S>
+struct VtCfg {
+  static constexpr int kABytes = 128 * 128;  // 128 vocabulary entries (or W_g rows) x 64 k
+  static constexpr int kHMaxBytes = 128 * 128;  // up to 128 drafted rows per CTA x 64 k
+  static constexpr int kNBuf = 2;
+  static constexpr int kAccCols = 256;  // N <= 256
+  static constexpr int kTmemCols = 512;
+  static constexpr int kEpiWarps = 4;  // warps 4..7, one TMEM lane quarter each
+  static constexpr int kZWarps = 4;    // warps 2, 3, 8, 9
+  static constexpr int kThreads = 32 * 10;
+  // a turned-around row: 128 floats + 1 of skew (the lanes' reads of one column hit 32 banks)
+  static constexpr int kXStride = 129;
+  static constexpr int kXBytes = 4 * 32 * kXStride * 4;  // one round: four 32-row chunks
+  static constexpr int kAuxBytes = kXBytes;
+  static constexpr int kBarBytes = 8 * (2 * S + 2 * kNBuf) + 16;
+  static constexpr size_t smem(uint32_t stage_bytes) {
+    return 1024 + size_t(S) * stage_bytes + size_t(kAuxBytes) + kBarBytes;
+  }
+  // five stages hold up to 120 drafted rows per CTA (a 31 KB stage); 128 rows take four
+  static constexpr uint32_t kMaxStage = S >= 5 ? kABytes + 120 * 128 : kABytes + kHMaxBytes;
+  static constexpr size_t kSmemMax = smem(kMaxStage);
+  static_assert(kSmemMax <= 232448, "shared memory");
+  static_assert(kXBytes >= 2 * 128 * 2 * kK * 4, "the peer's lists fit the round buffer");
+  static_assert(kXBytes % 16 == 0, "the barriers follow 16-byte aligned");
+};
+
+// (x, id) enters t when it ranks before t's last member by (value desc, id asc); it goes
+// after every member that ranks before it.
+__device__ __forceinline__ void top16_insert_ranked(Top16& t, float x, int id) {
+  if (!ranks_before(x, id, t.v[kK - 1], t.i[kK - 1])) return;
+  bool ge[kK];
+#pragma unroll
+  for (int k = 0; k < kK; ++k) ge[k] = ranks_before(t.v[k], t.i[k], x, id);
+#pragma unroll
+  for (int k = kK - 1; k >= 1; --k) {
+    t.v[k] = ge[k] ? t.v[k] : (ge[k - 1] ? x : t.v[k - 1]);
+    t.i[k] = ge[k] ? t.i[k] : (ge[k - 1] ? id : t.i[k - 1]);
+  }
+  t.v[0] = ge[0] ? t.v[0] : x;
+  t.i[0] = ge[0] ? t.i[0] : id;
+}
+
+template <int S>
+__global__ void __launch_bounds__(VtCfg<S>::kThreads, 1)
+    k_lmhead_vt(const __grid_constant__ LmheadParams p) {
+  using Cfg = VtCfg<S>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t stage_bytes = p.stage_bytes;
+  uint8_t* ring = smem;
+  float* xbuf = reinterpret_cast<float*>(ring + size_t(S) * stage_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xbuf) + Cfg::kAuxBytes);
+  uint64_t* full = bars;            // leader: both CTAs' bytes of a stage have landed
+  uint64_t* empty = bars + S;       // each CTA: the pair MMAs reading a stage are done
+  uint64_t* tfull = bars + 2 * S;   // each CTA: an accumulator is complete
+  uint64_t* tempty = tfull + Cfg::kNBuf;  // leader: both CTAs have drained an accumulator
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + Cfg::kNBuf);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int P = p.L - 1;
+  const int hrows = p.nb * P;  // drafted rows per CTA; the pair MMAs' N is twice that
+  const int N = 2 * hrows;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < Cfg::kNBuf; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 2 * Cfg::kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&p.tm_h3);
+    prefetch_tensormap(&p.tm_w);
+    prefetch_tensormap(&p.tm_g);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before either signals the other's
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  grid_dependents_launch();
+
+  const int n_tiles = p.n_vocab_tiles + p.n_gate_tiles;
+  const int cid = blockIdx.x >> 1;
+  const int ncl = gridDim.x >> 1;
+  const int KB = p.d / 64;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------- TMA producer: 128 A rows + this CTA's drafted rows
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_keep = policy_evict_last();
+      const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);  // the leader's barriers
+      const uint32_t tx = static_cast<uint32_t>(Cfg::kABytes + hrows * 128);
+      const int hb = p.b0 + static_cast<int>(rank) * p.nb;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = cid; ok && tile < n_tiles; tile += ncl) {
+        const PairTile pt = pair_tile(tile, ncl, p.n_gate_tiles, n_tiles);
+        const int n0 = pt.n0 + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * tx);
+          const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
+          const uint32_t sw = smem_u32(ring + size_t(stage) * stage_bytes);
+          if (pt.vocab) {
+            tma_load_2d_pair(sw, &p.tm_w, fb, n0, kb * 64, pol_stream);
+            tma_load_2d_pair(sw + 8192, &p.tm_w, fb, n0 + 64, kb * 64, pol_stream);
+          } else {
+            tma_load_2d_pair(sw, &p.tm_g, fb, kb * 64, n0, pol_keep);
+          }
+          tma_load_3d_pair(sw + Cfg::kABytes, &p.tm_h3, fb, kb * 64, 1, hb, pol_keep);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (ok) {  // the releases of the last stages land before this CTA may exit
+        for (int i = 0; i < S; ++i) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) break;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader && !p.stall_mma) {
+      // ------------------------------------------------------- pair MMA issuer (leader)
+      const uint32_t id_vocab = idesc_bf16_f32(N, false, 256, true);  // A = W, MN-major
+      const uint32_t id_gate = idesc_bf16_f32(N, false, 256, false);  // A = W_g, K-major
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = cid; ok && tile < n_tiles; tile += ncl) {
+        const bool is_vocab = pair_tile(tile, ncl, p.n_gate_tiles, n_tiles).vocab;
+        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, p.err, abort_flag, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sw = smem_u32(ring + size_t(stage) * stage_bytes);
+          const uint32_t sh = sw + Cfg::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {  // K = 16 per instruction: 32 bytes of a K-major row
+            const uint64_t bdesc = smem_desc_sw128(sh + kk * 32, 0, 1024);
+            const uint64_t adesc = is_vocab ? smem_desc_sw128(sw + kk * 2048, 8192, 1024)
+                                            : smem_desc_sw128(sw + kk * 32, 0, 1024);
+            tc_mma_bf16_pair(d0, adesc, bdesc, is_vocab ? id_vocab : id_gate, (kb | kk) != 0);
+          }
+          tc_commit_pair_multicast(smem_u32(&empty[stage]), 0x3);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(smem_u32(&tfull[acc]), 0x3);
+        if (++acc == Cfg::kNBuf) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 2 || warp == 3 || warp >= 8) {
+    // ------------------------------------------------ target-logit row statistics
+    const int zw = warp < 4 ? warp - 2 : warp - 6;
+    if (blockIdx.x == 0 && p.zero_ptr != nullptr)
+      for (int i = zw * 32 + lane; i < p.zero_count; i += 32 * Cfg::kZWarps) p.zero_ptr[i] = 0;
+    const int n_units = p.z_rows * p.z_nchunk;
+    const int is_bf16 = p.zdtype == 0;
+    for (int u = blockIdx.x * Cfg::kZWarps + zw; u < n_units; u += gridDim.x * Cfg::kZWarps) {
+      const int row = u / p.z_nchunk, chunk = u - row * p.z_nchunk;
+      const RowStat st = zchunk_stat_warp(p.Z, is_bf16, static_cast<size_t>(row) * p.V, chunk,
+                                          p.V, p.z_inv_T, lane);
+      if (lane == 0) {
+        const size_t o = static_cast<size_t>(row) * p.z_nchunk + chunk;
+        p.zmax[o] = st.m;
+        p.zarg[o] = st.i;
+        if (p.z_inv_T > 0.f) p.zsum[o] = st.s;
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
+    const int nchunk = (N + 31) >> 5;
+    Top16 top0, top1;  // rows 32 q + lane and 128 + 32 q + lane of the group's N
+    top16_init(top0);
+    top16_init(top1);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = cid; tile < n_tiles; tile += ncl) {
+      const PairTile pt = pair_tile(tile, ncl, p.n_gate_tiles, n_tiles);
+      const bool w_ok = mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, p.err, abort_flag, p.wait_limit_ns);
+      // all four warps go on, or none: the barriers below need every one of them
+      if (!named_bar_and(2, 128, w_ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * Cfg::kAccCols);
+      const int vbase = pt.n0 + static_cast<int>(rank) * 128;  // this CTA's first M entry
+      if (pt.vocab) {
+#pragma unroll
+        for (int rd = 0; rd < 2; ++rd) {
+          if (4 * rd < nchunk) {
+#pragma unroll 1
+            for (int k = 0; k < 4; ++k) {  // this warp's lane quarter of the round's chunks
+              const int c = 4 * rd + k;
+              if (c < nchunk) {
+                uint32_t rr[32];
+                tmem_ld_32x32b_x32(tbase + c * 32, rr);
+                tmem_ld_wait();
+                float* xb = xbuf + k * (32 * Cfg::kXStride) + q * 32 + lane;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) xb[j * Cfg::kXStride] = __uint_as_float(rr[j]);
+              }
+            }
+            named_bar_sync(2, 128);
+            if (4 * rd + q < nchunk) {  // chunk 4 rd + q: row 32 (4 rd + q) + lane
+              Top16& top = rd == 0 ? top0 : top1;
+              const float* xrow = xbuf + (q * 32 + lane) * Cfg::kXStride;
+#pragma unroll 1
+              for (int sub = 0; sub < 4; ++sub) {
+                uint32_t v[32];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) v[u] = __float_as_uint(xrow[sub * 32 + u]);
+                const int cbase = vbase + sub * 32;
+                top16_offer32(top, v, cbase, p.V - cbase);  // entries past V are not tokens
+              }
+            }
+            named_bar_sync(2, 128);  // the round's reads are done before the next stores
+          }
+        }
+      } else {
+        // gate tile: lane = unit j of g (a W_g row), column = drafted row; sigmoid, and the
+        // 32 lanes of a store write 32 consecutive units of one row
+        const int unit = vbase + q * 32 + lane;
+        for (int c = 0; c < nchunk; ++c) {
+          uint32_t rr[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = c * 32 + j;
+            const int half = col >= hrows, i = col - half * hrows;
+            const int b = p.b0 + half * p.nb + i / P, t = 1 + i % P;
+            if (col < N && b < p.n_req && unit < p.r)
+              p.gate_out[(static_cast<size_t>(b) * p.L + t) * p.r + unit] =
+                  1.0f / (1.0f + expf(-__uint_as_float(rr[j])));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
+      if (++acc == Cfg::kNBuf) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+    // every warp's reads of the round buffer are done before it is reused for the lists
+    named_bar_sync(2, 128);
+    if (ok && !leader) {
+      // the odd CTA leaves its lists in its own round buffer for the leader to read
+      float* dst = xbuf + static_cast<size_t>(q * 32 + lane) * (2 * kK);
+#pragma unroll
+      for (int k = 0; k < kK; ++k) {
+        dst[k] = top0.v[k];
+        dst[kK + k] = __int_as_float(top0.i[k]);
+        dst[128 * 2 * kK + k] = top1.v[k];
+        dst[128 * 2 * kK + kK + k] = __int_as_float(top1.i[k]);
+      }
+    }
+    // -------------------------------------------------------------- teardown (epilogue)
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // every pair MMA and TMEM read of both CTAs is done; the lists are out
+    if (ok && leader && p.write_partials) {
+      const uint32_t peer = mapa_shared(smem_u32(xbuf), 1) +
+                            static_cast<uint32_t>(q * 32 + lane) * (2 * kK * 4);
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        Top16& top = s == 0 ? top0 : top1;
+        const uint32_t src = peer + static_cast<uint32_t>(s) * (128 * 2 * kK * 4);
+        float pv[kK];
+        int pi[kK];
+#pragma unroll
+        for (int u = 0; u < kK / 4; ++u) {
+          const float4 a = ld_dsmem_f4(src + u * 16);
+          const float4 b = ld_dsmem_f4(src + kK * 4 + u * 16);
+          pv[4 * u] = a.x; pv[4 * u + 1] = a.y; pv[4 * u + 2] = a.z; pv[4 * u + 3] = a.w;
+          pi[4 * u] = __float_as_int(b.x); pi[4 * u + 1] = __float_as_int(b.y);
+          pi[4 * u + 2] = __float_as_int(b.z); pi[4 * u + 3] = __float_as_int(b.w);
+        }
+#pragma unroll
+        for (int k = 0; k < kK; ++k) top16_insert_ranked(top, pv[k], pi[k]);
+        const int col = (4 * s + q) * 32 + lane;  // the drafted row this list belongs to
+        const int half = col >= hrows, i = col - half * hrows;
+        const int b = p.b0 + half * p.nb + i / P, t = 1 + i % P;
+        if (col < N && b < p.n_req) {
+          const size_t grow = static_cast<size_t>(b) * p.L + t;
+          const size_t off = (grow * p.G + cid) * kK;  // one list per pair
+          float4* ov = reinterpret_cast<float4*>(p.part_val + off);
+          int4* oi = reinterpret_cast<int4*>(p.part_idx + off);
+#pragma unroll
+          for (int j = 0; j < kK / 4; ++j) {
+            ov[j] = make_float4(top.v[4 * j], top.v[4 * j + 1], top.v[4 * j + 2], top.v[4 * j + 3]);
+            oi[j] = make_int4(top.i[4 * j], top.i[4 * j + 1], top.i[4 * j + 2], top.i[4 * j + 3]);
+          }
+        }
+      }
+    }
+    cluster_sync();  // the peer's lists stay in place until the leader has read them
+    return;
+  }
+
+  // -------------------------------------------------------------- teardown (other warps)
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+  }
+  cluster_sync();
+}
+
 // ------------------------------------------------------------------ row quantisation
 // One block per row of h [rows, d] bf16 (d a multiple of 8): the row's largest magnitude,
 // its power-of-two scale (the smallest 2^e with amax <= 448 * 2^e, from the exponent and
@@ -925,6 +1311,51 @@ bool encode_u8_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
   return r == CUDA_SUCCESS;
 }
 
+// h [B][L][d] bf16 seen as a 3-D tensor (d innermost), box 64 (k) x (L - 1) positions x nb
+// requests, 128-byte swizzle: one box is the drafted rows of nb requests, 128 B each, in
+// (request, position) order; requests past B are zero-filled.
+bool encode_bf16_drafted_rows(CUtensorMap* m, const void* base, int d, int L, int B, int nb) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(L) * d * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(L - 1), static_cast<cuuint32_t>(nb)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int S>
+cudaError_t launch_vt(const LmheadParams& prm, int grid, cudaStream_t s) {
+  using Cfg = VtCfg<S>;
+  auto kern = k_lmhead_vt<S>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::kSmemMax));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::smem(prm.stage_bytes);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
+}
+
 template <int MT, int NT, int NBUF, int SW, int SH, int CL, int RS = 0>
 cudaError_t launch_cfg(const LmheadParams& prm, int grid, cudaStream_t s) {
   using Cfg = LmCfg<MT, NT, NBUF, SW, SH, CL, RS>;
@@ -990,6 +1421,48 @@ cudaError_t launch_cluster(const LmheadParams& prm, int grid, int cl, cudaStream
   return launch_cfg<MT, NT, NBUF, SW, SH, 1>(prm, grid, s);
 }
 
+// Requests per CTA of a vocabulary-major group: a multiple of 8 (so N = 2 nb (L - 1) is a
+// multiple of 16) with nb (L - 1) <= 128; 0 when a block has more than 16 drafted positions.
+int vt_requests_per_cta(int L) { return (L >= 2 && L - 1 <= 16) ? 8 * (16 / (L - 1)) : 0; }
+
+// The vocabulary launches of a call with more than 128 rows on k_lmhead_vt: groups of up to
+// 2 nb_max requests, the last one with nb shrunk to what it holds (rounded up to 8).
+cudaError_t launch_vt_groups(const LmheadLaunch& a, LmheadParams& prm, int nb_max, cudaStream_t s) {
+  const int B = a.rows_total / a.L;
+  prm.n_vocab_tiles = (a.V + 255) / 256;
+  prm.n_gate_tiles = a.gate ? (a.r + 255) / 256 : 0;
+  prm.write_partials = 1;
+  if (!encode_bf16_2d(&prm.tm_g, a.gate ? a.Wg : a.hidden, a.d, a.gate ? a.r : a.rows_total, 64,
+                      128))
+    return cudaErrorInvalidValue;
+  for (int b0 = 0; b0 < B; b0 += 2 * nb_max) {
+    const int bg = B - b0 < 2 * nb_max ? B - b0 : 2 * nb_max;
+    const int half = (((bg + 1) / 2) + 7) / 8 * 8;
+    const int nb = half < nb_max ? half : nb_max;
+    if (!encode_bf16_drafted_rows(&prm.tm_h3, a.hidden, a.d, a.L, B, nb)) return cudaErrorInvalidValue;
+    prm.b0 = b0;
+    prm.nb = nb;
+    prm.n_req = B;
+    prm.stage_bytes = static_cast<uint32_t>(VtCfg<5>::kABytes + nb * (a.L - 1) * 128);
+    const bool first = b0 == 0;  // the statistics and the counter reset ride on the first
+    prm.Z = a.Z;
+    prm.zdtype = a.zdtype;
+    prm.z_rows = first ? a.z_rows : 0;
+    prm.z_nchunk = a.z_nchunk;
+    prm.z_inv_T = a.z_inv_T;
+    prm.zmax = a.zmax;
+    prm.zarg = a.zarg;
+    prm.zsum = a.zsum;
+    prm.zero_ptr = first ? a.zero_ptr : nullptr;
+    prm.zero_count = first ? a.zero_count : 0;
+    // five ring stages when they fit next to the turn-around buffers, else four
+    const cudaError_t e = prm.stage_bytes <= VtCfg<5>::kMaxStage ? launch_vt<5>(prm, a.G, s)
+                                                                   : launch_vt<4>(prm, a.G, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace
 
 bool lmhead_row_split(int rows_total, int variant, int G) {
@@ -1023,6 +1496,19 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
   prm.err = a.err;
   prm.wait_limit_ns = a.wait_limit_ns > 0 ? a.wait_limit_ns : kWaitLimitNs;
   prm.stall_mma = a.stall_mma;
+  // More than 128 rows with the vocabulary: the vocabulary-major pair kernel computes the
+  // drafted rows only, so it needs fewer passes over W when the verified slots tip the rows
+  // over a multiple of 256 (e.g. 32 blocks of 9); per pass it is a little slower than the
+  // row-major pair kernel (its epilogue turns the rows around in shared memory). Chosen when
+  // it saves a pass (variant 0), or always (6); 5 and 4 force the row-major shapes.
+  int vt_nb = (rs && a.vocab) ? vt_requests_per_cta(a.L) : 0;
+  if (vt_nb > 0 && a.lmhead_variant != 6) {
+    const int B = a.rows_total / a.L;
+    const int vt_passes = (B + 2 * vt_nb - 1) / (2 * vt_nb);
+    const int pair_passes = (a.rows_total + 255) / 256;
+    if (a.lmhead_variant != 0 || vt_passes >= pair_passes) vt_nb = 0;
+  }
+  if (vt_nb > 0) return launch_vt_groups(a, prm, vt_nb, s);
   for (int row0 = 0; row0 < a.rows_total; row0 += 256) {
     prm.row0 = row0;
     // the target-logit statistics and the counter reset ride on the first launch only

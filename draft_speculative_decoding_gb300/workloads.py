@@ -89,8 +89,12 @@ LONG_BLOCK = WorkloadSpec("long_block_B16_L16_V151936_d4096", B=16, L=16, V=1519
 # captures.
 THROUGHPUT_PROFILE = THROUGHPUT.with_(name="throughput_B32_L8_V65536_d5120_zipf", V=65536)
 
+# The throughput workload with blocks of 9: 288 rows, of which 256 are drafted, so skipping the
+# verified slots saves a whole pass over W_vocab (the vocabulary-major LM head).
+THROUGHPUT_BLOCK9 = THROUGHPUT.with_(name="throughput_B32_L9_V151936_d5120_zipf", L=9)
+
 WORKLOADS = {w.name: w for w in (TINY, SINGLE, SMALL_BATCH, THROUGHPUT, LONG_BLOCK,
-                                 THROUGHPUT_PROFILE)}
+                                 THROUGHPUT_PROFILE, THROUGHPUT_BLOCK9)}
 
 
 def torch_dtype(spec: WorkloadSpec) -> torch.dtype:

@@ -31,6 +31,11 @@ SMALL = [
     wl.TINY.with_(name="pairs_few_tiles", dtype="bf16", B=20, L=8, V=1040, d=64, r=256, seed=37),
     wl.TINY.with_(name="pairs_L16", dtype="bf16", B=16, L=16, V=6000, d=256, r=256, seed=38,
                   agreement=("top1_linear", 0.85, 0.55)),
+    # the vocabulary-major LM head, chosen because it saves a pass over W: 288 rows of which
+    # 256 drafted (with a gate tile); 320 rows of blocks of 5, 256 drafted
+    wl.TINY.with_(name="vt_32x9", dtype="bf16", B=32, L=9, V=3000, d=128, r=256, seed=39,
+                  zipf=True),
+    wl.TINY.with_(name="vt_64x5", dtype="bf16", B=64, L=5, V=2600, d=128, r=64, seed=40),
 ]
 
 
@@ -146,6 +151,37 @@ def test_fused_launch_count(lib):
         torch.cuda.synchronize()
         rows = spec.B * spec.L
         assert binding.dfs_launch_count() - before == (rows + 255) // 256 + 1
+
+
+def test_fused_launch_count_vocabulary_major(lib):
+    """Where the drafted rows alone fit fewer 256-row groups (32 blocks of 9: 288 rows, 256
+    drafted), one vocabulary-major LM-head launch replaces two."""
+    spec = [s for s in SMALL if s.name == "vt_32x9"][0]
+    data = wl.generate(spec, "cuda")
+    dims = dims_for(spec)
+    ws = binding.alloc_workspace(dims)
+    before = binding.dfs_launch_count()
+    binding.dfs_select_verify(dims, data["h"], data["W"], data["Wg"], data["A"], data["Bt"],
+                              data["x0"], data["Z"], binding.DFS_PATH_GREEDY, 0.0, 1, ws)
+    torch.cuda.synchronize()
+    assert binding.dfs_launch_count() - before == 1 + 1
+
+
+@pytest.mark.parametrize("name", ["fused_groups", "pairs_256rows_r512", "pairs_L16"])
+@pytest.mark.parametrize("mode,T", [(binding.DFS_PATH_VITERBI, 0.0), (binding.DFS_PATH_SAMPLE, 0.8)])
+def test_fused_vocabulary_major_forced(lib, orc, name, mode, T, monkeypatch):
+    """The vocabulary-major LM head forced where the row-major one is the default: several
+    request groups with a one-request last group, two gate tiles, 15 drafted rows a block."""
+    monkeypatch.setenv("DFS_LMHEAD_VARIANT", "6")
+    spec = [s for s in SMALL if s.name == name][0]
+    data = wl.generate(spec, "cuda")
+    npd = np_inputs(data)
+    g = _run(data, spec, mode, T, seed=spec.seed + 200)
+    o = orc.select_verify(npd["h"], npd["W"], npd["Wg"], npd["A"], npd["Bt"], npd["x0"], npd["Z"],
+                          path_mode=mode, temperature=T, seed=spec.seed + 200)
+    diverged = _compare(g, o, spec, list(range(spec.B)), T)
+    assert diverged <= max(1, spec.B // 8)
+    _invariants(g, spec, npd, T)
 
 
 FULL = [
