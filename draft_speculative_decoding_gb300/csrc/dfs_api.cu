@@ -37,12 +37,11 @@ int device_sm_count() {
 // kernel where it needs fewer passes over W, else the row-major pair kernel; 6 = always the
 // vocabulary-major pair kernel (pair MMAs over 256 vocabulary entries x the drafted rows);
 // 5 = always the row-major pair kernel (256 rows x 256 vocabulary columns, each CTA staging
-// half of the W tile); 4 = CTA pairs with per-CTA MMAs sharing each W tile by multicast.
-// Read from DFS_LMHEAD_VARIANT on each call, for tuning.
+// half of the W tile). Read from DFS_LMHEAD_VARIANT on each call, for tuning.
 int lmhead_variant_override() {
   const char* s = std::getenv("DFS_LMHEAD_VARIANT");
   const int v = s != nullptr ? std::atoi(s) : 0;
-  return (v == 4 || v == 5 || v == 6) ? v : 0;
+  return (v == 5 || v == 6) ? v : 0;
 }
 
 struct Layout {
@@ -74,8 +73,8 @@ int check_dims(const dfs_dims* d) {
 bool make_layout(const dfs_dims& d, Layout* L) {
   const int sms = device_sm_count();
   if (sms <= 0) return false;
-  // one list per CTA of the persistent LM-head grid: a multiple of 4 so clusters tile it
-  L->G = d.dtype == DFS_BF16 ? ((sms < dfs::kMaxLists ? sms : dfs::kMaxLists) / 4) * 4 : 1;
+  // one list per CTA of the persistent LM-head grid: even, so CTA pairs tile it
+  L->G = d.dtype == DFS_BF16 ? ((sms < dfs::kMaxLists ? sms : dfs::kMaxLists) / 2) * 2 : 1;
   if (L->G < 1) L->G = 1;
   L->nchunk = (d.V + dfs::kZChunk - 1) / dfs::kZChunk;
   const size_t rows = static_cast<size_t>(d.B) * d.L;
@@ -109,7 +108,7 @@ bool make_layout(const dfs_dims& d, Layout* L) {
 // Partial top-16 lists per row that the LM-head kernel leaves for the tail.
 int lists_per_row(const dfs_dims& d, const Layout& L) {
   return (d.dtype == DFS_BF16 &&
-          dfs::lmhead_row_split(d.B * d.L, lmhead_variant_override(), L.G)) ? L.G / 2 : L.G;
+          dfs::lmhead_row_split(d.B * d.L, L.G)) ? L.G / 2 : L.G;
 }
 
 template <typename T>
@@ -175,18 +174,6 @@ cudaError_t run_lmhead_kernels(const dfs_dims& d, const Layout& L, void* ws, con
 cudaError_t run_zreduce(const dfs_dims& d, const Layout& L, void* ws, const void* Z, float T,
                         cudaStream_t s);
 
-// Step a1 (+ a2 when gate): LM head, partial top-16 lists, gate rows.
-// With Z != nullptr the target-logit row statistics (and the per-call counter reset) are
-// produced alongside: by the tensor-core kernel's spare warps, or by the standalone
-// reduction kernel on the fp32 path.
-// CTAs per cluster of the LM-head kernel (they share the hidden-row tiles by TMA
-// multicast): 1, 2 or 4, default 2. Read from DFS_LMHEAD_CLUSTER on each call, for tuning.
-int lmhead_cluster() {
-  const char* s = std::getenv("DFS_LMHEAD_CLUSTER");
-  const int v = s ? std::atoi(s) : 2;
-  return (v == 1 || v == 2 || v == 4) ? v : 2;
-}
-
 // Where the target-logit row statistics are computed: 1 = by the LM-head kernel's spare
 // warps (default), 0 = by the standalone reduction kernel before it. Read from DFS_Z_FUSED
 // on each call, for tuning; both do the same work.
@@ -208,6 +195,10 @@ bool z_fused() {
   return s == nullptr || std::atoi(s) != 0;
 }
 
+// Step a1 (+ a2 when gate): LM head, partial top-16 lists, gate rows.
+// With Z != nullptr the target-logit row statistics (and the per-call counter reset) are
+// produced alongside: by the tensor-core kernel's spare warps, or by the standalone
+// reduction kernel on the fp32 path.
 cudaError_t run_lmhead(const dfs_dims& d, const Layout& L, void* ws, const void* hidden,
                        const void* W, const void* Wg, bool vocab, bool gate, cudaStream_t s,
                        const void* Z = nullptr, float T = 0.f) {
@@ -245,7 +236,6 @@ cudaError_t run_lmhead_kernels(const dfs_dims& d, const Layout& L, void* ws, con
     a.gate_out = at<float>(ws, L.gate);
     a.err = at<int>(ws, L.err);
     a.lmhead_variant = lmhead_variant_override();
-    a.cluster = lmhead_cluster();
     a.wait_limit_ns = debug_wait_limit_ns();
     a.stall_mma = debug_stall_mma();
     if (Z != nullptr) {

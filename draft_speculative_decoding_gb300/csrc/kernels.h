@@ -32,9 +32,7 @@ struct LmheadLaunch {
   int lmhead_variant;  // more than 128 rows: 0 = 6 where it needs fewer passes over W,
                        // else 5; 6 = CTA pairs with pair MMAs over 256 vocabulary entries x
                        // the drafted rows of up to 2 nb requests; 5 = pair MMAs over 256-row
-                       // groups (each CTA stages half of the W tile); 4 = per-CTA MMAs (the
-                       // W tile multicast to both)
-  int cluster;         // CTAs per cluster sharing hidden-row tiles by multicast (1, 2 or 4)
+                       // groups (each CTA stages half of the W tile)
   // Test hooks: the limit of every bounded wait (0: the default), and a switch that keeps the
   // MMA issuer idle so that the other roles' waits run out and report DFS_ERR_TIMEOUT.
   unsigned long long wait_limit_ns;
@@ -94,7 +92,7 @@ cudaError_t launch_quantize_rows_e4m3(const void* h, int rows, int d, void* q, f
                                       cudaStream_t s);
 // Whether a call with these rows runs on CTA pairs that split the rows (then each row gets
 // G / 2 partial lists, one per pair, instead of G).
-bool lmhead_row_split(int rows_total, int variant, int G);
+bool lmhead_row_split(int rows_total, int G);
 
 // ---- a1 (+a2) for fp32 inputs, on CUDA cores ----
 struct LmheadSimtLaunch {

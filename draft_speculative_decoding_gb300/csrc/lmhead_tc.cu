@@ -26,9 +26,8 @@
 //   * four more warps stream the target logits (16-byte loads, read once, a whole 4096-token
 //     chunk per warp in flight) and write per-chunk row statistics (max, argmax, sum of exp)
 //     for verification, so those bytes move while the tensor pipe works on W.
-// k_lmhead_tc serves row groups of up to 128 rows (M = 128 x N = 256 per CTA; clusters share
-// the hidden-row tiles by multicast) and, as variant 4, CTA pairs that split 256 rows with
-// the W tile multicast to both. k_lmhead_pair serves 129..256 rows with pair MMAs
+// k_lmhead_tc serves row groups of up to 128 rows (M = 128 x N = 256 per CTA, each CTA loading
+// its own hidden-row and W boxes). k_lmhead_pair serves 129..256 rows with pair MMAs
 // (cta_group::2, M = 256 x N = 256 across two SMs): each CTA stages only half of the W tile,
 // which halves the shared-memory bytes per MMA -- at 256 rows the tensor pipe must run near
 // full rate alongside the HBM stream, and shared-memory bandwidth, not HBM, was the limit.
@@ -83,7 +82,7 @@ struct LmheadParams {
   uint32_t stage_bytes;  // one ring stage: 128 A rows + the group's drafted rows, 64 k each
 };
 
-template <int MT, int NT, int NBUF, int SW, int SH, int CL, int RS>
+template <int MT, int NT, int NBUF, int SW, int SH>
 struct LmCfg {
   static constexpr int kWBytes = NT * 128;        // NT columns x 64 bf16 (or NT gate rows)
   static constexpr int kHBytes = MT * 128 * 128;  // MT tiles of 128 rows x 64 bf16
@@ -102,9 +101,6 @@ struct LmCfg {
   static_assert(kAccCols * NBUF <= 512, "TMEM holds 512 fp32 columns");
   static_assert(NT % 64 == 0 && NT >= 64 && NT <= 256, "N tile");
   static_assert(kSmem <= 232448, "shared memory");
-  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
-  static_assert(!RS || (CL == 2 && MT == 1), "a row-split pair is a cluster of two 128-row CTAs");
-  static constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
 };
 
 // A row's running top-16, kept sorted by (value desc, id asc); v[15] is the entry threshold.
@@ -203,10 +199,10 @@ __device__ __forceinline__ void store_gate32(float* dst, const uint32_t (&r)[32]
   }
 }
 
-template <int MT, int NT, int NBUF, int SW, int SH, int CL, int RS>
-__global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads, 1)
+template <int MT, int NT, int NBUF, int SW, int SH>
+__global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH>::kThreads, 1)
     k_lmhead_tc(const __grid_constant__ LmheadParams p) {
-  using Cfg = LmCfg<MT, NT, NBUF, SW, SH, CL, RS>;
+  using Cfg = LmCfg<MT, NT, NBUF, SW, SH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -228,11 +224,11 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
   if (threadIdx.x == 0) {
     for (int s = 0; s < SW; ++s) {
       mbar_init(smem_u32(&wfull[s]), 1);
-      mbar_init(smem_u32(&wempty[s]), RS ? 2 : 1);  // a shared W stage: both CTAs release it
+      mbar_init(smem_u32(&wempty[s]), 1);
     }
     for (int s = 0; s < SH; ++s) {
       mbar_init(smem_u32(&hfull[s]), 1);
-      mbar_init(smem_u32(&hempty[s]), RS ? 1 : CL);  // shared hidden rows: every CTA releases
+      mbar_init(smem_u32(&hempty[s]), 1);
     }
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
@@ -257,24 +253,14 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
   }
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   // Every CTA of this persistent grid is resident now: let the dependent tail kernel launch
   // onto SMs as they free up (it waits for this grid's completion before reading).
   grid_dependents_launch();
 
-  // Tiles: vocabulary tiles, then gate tiles. Clusters either share the hidden rows (each
-  // CTA its own tile; tiles padded so the CL CTAs of a cluster process the same number: a
-  // CTA takes tile s*CL + rank for super-tiles s = cluster, cluster + clusters, ..., and a
-  // padding tile streams zeros and produces nothing) or, as a row-split pair (RS), share
-  // the W tile: both CTAs take the same tile t = cluster, cluster + clusters, ..., CTA
-  // rank r computing rows 128r..128r+127 of it.
+  // Tiles: vocabulary tiles, then gate tiles; CTA c takes tiles c, c + grid, c + 2 grid, ...
   const int n_tiles = p.n_vocab_tiles + p.n_gate_tiles;
-  const int n_loop = RS ? n_tiles : (n_tiles + CL - 1) / CL;
-  const int rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int cid = blockIdx.x / CL;
-  const int ncl = gridDim.x / CL;
   const int KB = p.d / 64;
   const int first_z_extra = 4 + Cfg::kEpiWarps;  // warps first_z_extra.. are Z warps 1..3
 
@@ -286,12 +272,9 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int sup = cid; ok && sup < n_loop; sup += ncl) {
-        const int tile = RS ? sup : sup * CL + rank;
-        const bool is_pad = tile >= n_tiles;
-        const bool is_vocab = tile < p.n_vocab_tiles || is_pad;
-        // padding tiles load boxes wholly past the vocabulary: zeros
-        const int n0 = is_pad ? ((p.V + 63) / 64) * 64 : (is_vocab ? tile : tile - p.n_vocab_tiles) * NT;
+      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+        const bool is_vocab = tile < p.n_vocab_tiles;
+        const int n0 = (is_vocab ? tile : tile - p.n_vocab_tiles) * NT;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&wempty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) {
             ok = false;
@@ -300,35 +283,13 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
           const uint32_t fb = smem_u32(&wfull[stage]);
           mbar_arrive_expect_tx(fb, Cfg::kWBytes);
           const uint32_t sb = smem_u32(wring + size_t(stage) * Cfg::kWBytes);
-          if (RS) {  // this CTA's half of the boxes, delivered to both CTAs of the pair
-            if (is_vocab) {
-#pragma unroll
-              for (int c = 0; c < NT / 64; ++c)
-                if ((c & 1) == rank)
-                  tma_load_2d_multicast(sb + c * 8192, &p.tm_w, fb, n0 + c * 64, kb * 64,
-                                        Cfg::kClusterMask, pol_stream);
-            } else {
-              tma_load_2d_multicast(sb + rank * (NT / 2) * 128, &p.tm_g, fb, kb * 64,
-                                    n0 + rank * (NT / 2), Cfg::kClusterMask, pol_keep);
-            }
-          } else if (is_vocab) {
+          if (is_vocab) {
 #pragma unroll
             for (int c = 0; c < NT / 64; ++c)
               tma_load_2d(sb + c * 8192, &p.tm_w, fb, n0 + c * 64, kb * 64, pol_stream);
           } else {
             tma_load_2d(sb, &p.tm_g, fb, kb * 64, n0, pol_keep);
           }
-          if (++stage == SW) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-      }
-      // A shared stage is released by both CTAs; this CTA may exit only after the peer's
-      // last releases have arrived on its barriers.
-      if (RS && ok) {
-        for (int i = 0; i < SW; ++i) {
-          if (!mbar_wait_bounded(smem_u32(&wempty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) break;
           if (++stage == SW) {
             stage = 0;
             phase ^= 1;
@@ -343,8 +304,7 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int sup = cid; ok && sup < n_loop; sup += ncl) {
-        const int tile = RS ? sup : sup * CL + rank;
+      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&hempty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) {
             ok = false;
@@ -354,26 +314,8 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
           mbar_arrive_expect_tx(fb, MT == 1 ? p.h_box_bytes : static_cast<uint32_t>(Cfg::kHBytes));
           const uint32_t sa = smem_u32(hring + size_t(stage) * Cfg::kHBytes);
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            if (RS)
-              tma_load_2d(sa, &p.tm_h, fb, kb * 64, p.row0 + rank * 128, pol_keep);
-            else if (CL == 1)
-              tma_load_2d(sa + mt * 16384, &p.tm_h, fb, kb * 64, p.row0 + mt * 128, pol_keep);
-            else if (mt % CL == rank)  // this CTA's share, delivered to every CTA of the cluster
-              tma_load_2d_multicast(sa + mt * 16384, &p.tm_h, fb, kb * 64, p.row0 + mt * 128,
-                                    Cfg::kClusterMask, pol_keep);
-          }
-          if (++stage == SH) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-      }
-      // Before this CTA may exit, every stage must have been released by every CTA of the
-      // cluster (their releases arrive on this CTA's barriers).
-      if (CL > 1 && !RS && ok) {
-        for (int i = 0; i < SH; ++i) {
-          if (!mbar_wait_bounded(smem_u32(&hempty[stage]), phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) break;
+          for (int mt = 0; mt < MT; ++mt)
+            tma_load_2d(sa + mt * 16384, &p.tm_h, fb, kb * 64, p.row0 + mt * 128, pol_keep);
           if (++stage == SH) {
             stage = 0;
             phase ^= 1;
@@ -391,9 +333,8 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int sup = cid; ok && sup < n_loop; sup += ncl) {
-        const int tile = RS ? sup : sup * CL + rank;
-        const bool is_vocab = tile < p.n_vocab_tiles || tile >= n_tiles;
+      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+        const bool is_vocab = tile < p.n_vocab_tiles;
         if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, abort_flag, p.wait_limit_ns)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
@@ -419,14 +360,8 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
                           (kb | kk) != 0);
             }
           }
-          if (RS)
-            tc_commit_multicast(smem_u32(&wempty[ws]), Cfg::kClusterMask);
-          else
-            tc_commit(smem_u32(&wempty[ws]));
-          if (CL == 1 || RS)
-            tc_commit(smem_u32(&hempty[hs]));
-          else
-            tc_commit_multicast(smem_u32(&hempty[hs]), Cfg::kClusterMask);
+          tc_commit(smem_u32(&wempty[ws]));
+          tc_commit(smem_u32(&hempty[hs]));
           if (++ws == SW) {
             ws = 0;
             wph ^= 1;
@@ -467,16 +402,14 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
     const int e = warp - 4;
     const int mt = e >> 2;
     const int q = warp & 3;  // TMEM lane quarter this warp may read
-    const int row = (RS ? rank : mt) * 128 + q * 32 + lane;
+    const int row = mt * 128 + q * 32 + lane;
     const int grow = p.row0 + row;
     const bool valid = row < p.rows && (grow % p.L) != 0;  // skip each block's verified slot
     Top16 top;
     top16_init(top);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int sup = cid; sup < n_loop; sup += ncl) {
-      const int tile = RS ? sup : sup * CL + rank;
-      const bool is_pad = tile >= n_tiles;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
       const bool is_vocab = tile < p.n_vocab_tiles;
       const int n0 = (is_vocab ? tile : tile - p.n_vocab_tiles) * NT;
       if (!mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, p.err, abort_flag, p.wait_limit_ns)) break;
@@ -488,7 +421,7 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
         __syncwarp();  // tcgen05.ld is warp-collective; lanes diverged on row validity
         tmem_ld_32x32b_x32(tbase + c * 32, rr);
         tmem_ld_wait();
-        if (!valid || is_pad) continue;
+        if (!valid) continue;
         const int cbase = n0 + c * 32;
         if (is_vocab) {
           top16_offer32(top, rr, cbase, p.V - cbase);  // columns past V are not tokens
@@ -505,8 +438,7 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
       }
     }
     if (p.write_partials && valid) {
-      // one list per CTA computing the row: per cluster for a row-split pair
-      const size_t off = (static_cast<size_t>(grow) * p.G + (RS ? cid : blockIdx.x)) * kK;
+      const size_t off = (static_cast<size_t>(grow) * p.G + blockIdx.x) * kK;  // one list per CTA
       float4* pv = reinterpret_cast<float4*>(p.part_val + off);
       int4* pi = reinterpret_cast<int4*>(p.part_idx + off);
 #pragma unroll
@@ -525,7 +457,6 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH, CL, RS>::kThreads,
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
-  if (CL > 1) cluster_sync();  // no CTA leaves while a peer may still signal its barriers
 }
 
 
@@ -1356,10 +1287,10 @@ cudaError_t launch_vt(const LmheadParams& prm, int grid, cudaStream_t s) {
   return e;
 }
 
-template <int MT, int NT, int NBUF, int SW, int SH, int CL, int RS = 0>
+template <int MT, int NT, int NBUF, int SW, int SH>
 cudaError_t launch_cfg(const LmheadParams& prm, int grid, cudaStream_t s) {
-  using Cfg = LmCfg<MT, NT, NBUF, SW, SH, CL, RS>;
-  auto kern = k_lmhead_tc<MT, NT, NBUF, SW, SH, CL, RS>;
+  using Cfg = LmCfg<MT, NT, NBUF, SW, SH>;
+  auto kern = k_lmhead_tc<MT, NT, NBUF, SW, SH>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1367,19 +1298,8 @@ cudaError_t launch_cfg(const LmheadParams& prm, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(Cfg::kThreads);
-  cfg.dynamicSmemBytes = Cfg::kSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(prm);
+  const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) note_launches(1);
   return e;
 }
@@ -1412,13 +1332,6 @@ cudaError_t launch_pair(const LmheadParams& prm, int grid, cudaStream_t s, bool 
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
   if (e == cudaSuccess) note_launches(1);
   return e;
-}
-
-template <int MT, int NT, int NBUF, int SW, int SH>
-cudaError_t launch_cluster(const LmheadParams& prm, int grid, int cl, cudaStream_t s) {
-  if (cl == 4 && grid % 4 == 0) return launch_cfg<MT, NT, NBUF, SW, SH, 4>(prm, grid, s);
-  if (cl >= 2 && grid % 2 == 0) return launch_cfg<MT, NT, NBUF, SW, SH, 2>(prm, grid, s);
-  return launch_cfg<MT, NT, NBUF, SW, SH, 1>(prm, grid, s);
 }
 
 // Requests per CTA of a vocabulary-major group: a multiple of 8 (so N = 2 nb (L - 1) is a
@@ -1465,10 +1378,7 @@ cudaError_t launch_vt_groups(const LmheadLaunch& a, LmheadParams& prm, int nb_ma
 
 }  // namespace
 
-bool lmhead_row_split(int rows_total, int variant, int G) {
-  (void)variant;  // both shapes for 129..256 rows leave one partial list per CTA pair
-  return rows_total > 128 && G % 2 == 0;
-}
+bool lmhead_row_split(int rows_total, int G) { return rows_total > 128 && G % 2 == 0; }
 
 cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
   LmheadParams prm;
@@ -1488,7 +1398,7 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
   prm.d = a.d;
   prm.r = a.r;
   // More than 128 rows: CTA pairs split each row group (gate-only launches included)
-  const bool rs = lmhead_row_split(a.rows_total, a.lmhead_variant, a.vocab ? a.G : 2);
+  const bool rs = lmhead_row_split(a.rows_total, a.vocab ? a.G : 2);
   prm.G = rs ? a.G / 2 : a.G;  // partial lists per row: one per CTA, or per pair when split
   prm.part_val = a.part_val;
   prm.part_idx = a.part_idx;
@@ -1500,7 +1410,7 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
   // drafted rows only, so it needs fewer passes over W when the verified slots tip the rows
   // over a multiple of 256 (e.g. 32 blocks of 9); per pass it is a little slower than the
   // row-major pair kernel (its epilogue turns the rows around in shared memory). Chosen when
-  // it saves a pass (variant 0), or always (6); 5 and 4 force the row-major shapes.
+  // it saves a pass (variant 0), or always (6); 5 forces the row-major pair kernel.
   int vt_nb = (rs && a.vocab) ? vt_requests_per_cta(a.L) : 0;
   if (vt_nb > 0 && a.lmhead_variant != 6) {
     const int B = a.rows_total / a.L;
@@ -1525,29 +1435,18 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
     prm.zero_count = first ? a.zero_count : 0;
     prm.rows = a.rows_total - row0 < 256 ? a.rows_total - row0 : 256;
     // Row groups of up to 128 rows: one M tile x 256 vocabulary columns per CTA,
-    // double-buffered TMEM, clusters sharing the hidden rows. 129..256 rows: CTA pairs on
-    // one 256-column tile, 128 rows each: pair MMAs with each CTA staging half of the W tile
-    // (variant 5, the default), or per-CTA MMAs with the W tile multicast to both CTAs
-    // (variant 4).
-    const int variant = rs ? (a.lmhead_variant == 4 ? 4 : 5) : 0;
+    // double-buffered TMEM. 129..256 rows: CTA pairs on one 256-column tile, 128 rows each,
+    // pair MMAs with each CTA staging half of the W tile.
     const int NT = 256;
     prm.n_vocab_tiles = a.vocab ? (a.V + NT - 1) / NT : 0;
     prm.n_gate_tiles = a.gate ? (a.r + NT - 1) / NT : 0;
     prm.write_partials = a.vocab ? 1 : 0;
     if (!encode_bf16_2d(&prm.tm_g, a.gate ? a.Wg : a.hidden, a.d, a.gate ? a.r : a.rows_total,
-                        64, static_cast<uint32_t>(a.gate ? (variant >= 4 ? NT / 2 : NT) : 128)))
+                        64, static_cast<uint32_t>(a.gate ? (rs ? NT / 2 : NT) : 128)))
       return cudaErrorInvalidValue;
     const int grid = a.vocab ? a.G : (prm.n_gate_tiles > 0 ? prm.n_gate_tiles : 1) * (rs ? 2 : 1);
-    cudaError_t e;
-    // Clusters share the hidden rows by multicast; the gate-only launch (a tile or two)
-    // runs without.
-    const int cl = a.vocab ? a.cluster : 1;
-    if (variant == 5)
-      e = launch_pair<7, false>(prm, grid, s);
-    else if (variant == 4)
-      e = launch_cfg<1, 256, 2, 5, 4, 2, 1>(prm, grid, s);
-    else
-      e = launch_cluster<1, 256, 2, 5, 4>(prm, grid, cl, s);
+    const cudaError_t e = rs ? launch_pair<7, false>(prm, grid, s)
+                             : launch_cfg<1, 256, 2, 5, 4>(prm, grid, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

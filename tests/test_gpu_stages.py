@@ -47,7 +47,7 @@ def _oracle_candidates(orc, npd, spec):
 
 
 @pytest.mark.parametrize("spec", SHAPES, ids=lambda s: s.name)
-@pytest.mark.parametrize("variant", ["4", "5", "6"])
+@pytest.mark.parametrize("variant", ["5", "6"])
 def test_lmhead_topk(lib, orc, spec, variant, monkeypatch):
     monkeypatch.setenv("DFS_LMHEAD_VARIANT", variant)
     data, npd = _gen(spec)
