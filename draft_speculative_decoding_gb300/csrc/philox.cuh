@@ -42,18 +42,10 @@ __device__ __forceinline__ float uniform_accept(uint64_t seed, int b, int t) {
   return u01_from_word(c[0]);
 }
 
-// In-chunk uniform of the redraw for draft position t of request b (the token within the
-// chosen chunk, by inverse CDF): counter (0, t, b, 1), word 0.
-__device__ __forceinline__ float uniform_inchunk(uint64_t seed, int b, int t) {
+// The redraw's one uniform for draft position t of request b (the draw from row t - 1, or
+// from the bonus row when t = L): counter (0, t, b, 1), word 0.
+__device__ __forceinline__ float uniform_redraw(uint64_t seed, int b, int t) {
   uint64_t c[4] = {0ull, static_cast<uint64_t>(t), static_cast<uint64_t>(b), 1ull};
-  philox4x64_10(c, seed, 0ull);
-  return u01_from_word(c[0]);
-}
-
-// Chunk-choice uniform of the redraw for draft position t of request b: counter
-// (0, t, b, 2), word 0.
-__device__ __forceinline__ float uniform_chunk(uint64_t seed, int b, int t) {
-  uint64_t c[4] = {0ull, static_cast<uint64_t>(t), static_cast<uint64_t>(b), 2ull};
   philox4x64_10(c, seed, 0ull);
   return u01_from_word(c[0]);
 }

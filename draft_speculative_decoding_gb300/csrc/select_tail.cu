@@ -604,8 +604,8 @@ struct VerifySmem {
   float rm[kMaxL], rl[kMaxL], zx[kMaxL];
   int ry[kMaxL];
   int info[4];
-  float uc[kMaxL];                 // chunk-choice uniform of each possible redraw row
-  float ui[kMaxL];                 // in-chunk uniform of each possible redraw row
+  float ur[kMaxL];                 // the redraw uniform of each possible redraw row
+  float frac;                      // the target's place within the chosen chunk's mass, [0, 1]
   float mass[kMaxZChunks];         // cumulative residual mass over chunks
   float wsum[kTailThreads / 32];   // in-chunk weight of each warp's tokens
   int wpick[kTailThreads / 32];    // each warp's first token past the target
@@ -619,12 +619,15 @@ struct VerifySmem {
 
 // Verification of request b given its path (shared memory), by the whole block: row
 // statistics (one warp per row), the acceptance tests of all positions in parallel (one lane
-// each), then for T > 0 the redraw: a chunk of the row chosen by its residual mass, and the
-// Gumbel-max inside it.
+// each), then for T > 0 the redraw: the first token of the row, in vocabulary order, whose
+// cumulative residual weight exceeds one uniform times the row's total. It is found in two
+// steps that take the same decision: the chunk whose cumulative mass first exceeds the
+// target (from the per-chunk row statistics), then the token inside that chunk by its own
+// cumulative weights, against the target's remainder past the earlier chunks.
 // With a sampled proposal (prop_q != nullptr: q[P][16] over the candidates cand[P][16], the
 // drawn one at pidx[t-1]) a draft is accepted when U < p(x_t) / q(x_t), and the redraw is
 // from the residual max(0, p - q): a chunk's mass loses min(p, q) of each candidate in it,
-// and a candidate's Gumbel key gains log(max(0, 1 - q/p)). Without one the proposal is the
+// and a candidate's weight is scaled by max(0, 1 - q/p). Without one the proposal is the
 // path itself (q = 1 on x_t).
 // Statistics of target row `row` (max, argmax, log of the sum of exp), by one warp.
 __device__ void row_stat_publish(const TailLaunch& a, int row, float* dst) {
@@ -680,10 +683,7 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
         ok = uniform_accept(a.seed, b, lane + 1) < p / qx;
       }
     }
-    if (soft && lane < L) {
-      vs.uc[lane] = uniform_chunk(a.seed, b, lane + 1);
-      vs.ui[lane] = uniform_inchunk(a.seed, b, lane + 1);
-    }
+    if (soft && lane < L) vs.ur[lane] = uniform_redraw(a.seed, b, lane + 1);
     const unsigned fail = __ballot_sync(0xffffffffu, lane < P && !ok);
     const int n = fail ? __ffs(fail) - 1 : P;  // accepted drafts
     if (lane < L && (lane != n || !soft))
@@ -760,14 +760,26 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
       run = __shfl_sync(0xffffffffu, cum, 31);
     }
     __syncwarp();
-    const float target = vs.uc[n] * run;
+    const float target = vs.ur[n] * run;
     int pick = -1;
     for (int c0 = 0; c0 < a.nchunk && pick < 0; c0 += 32) {
       const int c = c0 + lane;
       const unsigned above = __ballot_sync(0xffffffffu, c < a.nchunk && vs.mass[c] > target);
       if (above) pick = c0 + __ffs(above) - 1;
     }
-    if (lane == 0) vs.info[1] = pick < 0 ? last_nonzero : pick;
+    if (lane == 0) {
+      vs.info[1] = pick < 0 ? last_nonzero : pick;
+      // the target's remainder past the earlier chunks, as a fraction of the chunk's mass;
+      // 1 when rounding left no chunk above the target (then the chunk's last token with
+      // weight is drawn, as a whole-row scan would take the row's last)
+      float frac = 1.f;
+      if (pick >= 0) {
+        const float before = pick > 0 ? vs.mass[pick - 1] : 0.f;
+        const float mc = vs.mass[pick] - before;
+        frac = mc > 0.f ? fminf(fmaxf((target - before) / mc, 0.f), 1.f) : 1.f;
+      }
+      vs.frac = frac;
+    }
   }
   __syncthreads();
   const int lo = vs.info[1] * kZChunk;
@@ -783,7 +795,7 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
   }
   // the token within the chunk by inverse CDF: weights exp((z - M)/T) (times the residual
   // factor of a sampled proposal's candidates; 0 for the excluded token), cumulated in
-  // vocabulary order, against one uniform times their total
+  // vocabulary order, against the target's place within the chunk times their total
   const int v0 = lo + threadIdx.x * 16;  // kZChunk = 16 tokens x 256 threads
   const float M = vs.rm[n];
   float w[16];
@@ -821,7 +833,7 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
     if (i < warp) before += vs.wsum[i];
     total += vs.wsum[i];
   }
-  const float target = vs.ui[n] * total;
+  const float target = vs.frac * total;
   float cum = before + incl - tsum;
   int mine = kIntMax, last = -1;
 #pragma unroll

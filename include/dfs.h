@@ -158,10 +158,10 @@ int dfs_path_select(const dfs_dims* dims, const float* S, const int32_t* cand_id
  *     and renormalised; after L-1 acceptances a bonus token is drawn from p_{L-1}.
  *     Draws: Philox4x64-10 (Salmon et al., SC'11), key (seed, 0); the accept test of
  *     position t uses counter (0, t, b, 0) word 0. The draw from row t-1 (t = L for the
- *     bonus row) is exact in two stages: a chunk of 4096 consecutive tokens is chosen
- *     with probability proportional to its residual mass (one uniform, counter
- *     (0, t, b, 2) word 0, against the cumulative masses in vocabulary order), then the
- *     Gumbel-max over that chunk, with counter (v>>2, t, b, 1) word v&3 for token v;
+ *     bonus row) takes one uniform U, counter (0, t, b, 1) word 0, and emits the first
+ *     token v in vocabulary order whose cumulative weight w_0 + ... + w_v exceeds U times
+ *     the row's total weight, with w_v = exp(Z[b,t-1,v] / T) for v != x_t and 0 for the
+ *     removed token (if rounding leaves no such token, the last token with weight).
  *     U = ((word >> 41) + 0.5) * 2^-23 (exact in fp32).
  *   out_tokens [B, L] int32 out: the emitted tokens, then -1
  *   accept_len [B] int32 out: tokens emitted, 1..L (includes the verifier's token) */
@@ -196,7 +196,8 @@ int dfs_verify_noalloc(const dfs_dims* dims, const int32_t* path, const void* ta
  *   counter (0, t, b, 3), word 0, against the cumulative q in candidate order), and the
  *   verification is speculative sampling against that proposal: accept x_t when
  *   U < p_{t-1}(x_t) / q_t(x_t); on the first rejection emit a draw from the residual
- *   max(0, p_{t-1} - q_t) renormalised; when all are accepted a bonus draw from p_{L-1}.
+ *   max(0, p_{t-1} - q_t) renormalised (dfs_verify's draw with these weights); when all are
+ *   accepted a bonus draw from p_{L-1}.
  *   path_score_opt is then the summed scores of the drawn path. With temperature 0 the
  *   mode is DFS_PATH_GREEDY. (dfs_path_select does not take it: it has no seed.) */
 int dfs_select_verify(const dfs_dims* dims, const void* hidden, const void* W_vocab,

@@ -69,6 +69,7 @@ def _load():
                 "orc_sample_verify_many": ([i32, P, i32, i64, P, P, i32, f64, u64, i64, i64, i32,
                                             P, P, P], i32),
                 "orc_philox4x64": ([P, P, P], None),
+                "orc_redraw_uniforms": ([i32, P, i64, f64, i64, P, P, i32, P, i64, P, P], i32),
                 "orc_select_verify": ([i32, i32, P, P, P, P, P, P, P, i64, i32, i64, i64, i64,
                                        i32, i32, f64, u64, P, i64, i32] + [P] * 14, i32),
                 "orc_e4m3_decode": ([P, i64, P], None),
@@ -296,6 +297,23 @@ def sample_verify_many(Z, S, ids, T: float, seed0: int, n: int, b: int = 0,
                                           nthreads or default_threads(), _ptr(paths), _ptr(out),
                                           _ptr(acc)), "sample_verify_many")
     return paths, out, acc
+
+
+def redraw_uniforms(z, T: float, u, excl: int = -1, cand=None, q=None):
+    """The verification's redraw of one target row z [V] for the given uniforms u [n]:
+    without cand, a draw from softmax(z/T) with token excl removed; with cand [K] and q [K],
+    a draw from the residual max(0, p - q). Returns (tokens int64 [n], margins f64 [n])."""
+    z = _c(z).reshape(-1)
+    u = _c(u, np.float64).reshape(-1)
+    out = np.empty(u.size, np.int64)
+    mg = np.empty(u.size, np.float64)
+    K = 0 if cand is None else len(cand)
+    cand = _c(cand if cand is not None else np.zeros(1), np.int32)
+    q = _c(q if q is not None else np.zeros(1), np.float64)
+    _check(_load().orc_redraw_uniforms(_dtype_code(z), _ptr(z), z.size, float(T), int(excl),
+                                       _ptr(cand), _ptr(q), K, _ptr(u), u.size, _ptr(out),
+                                       _ptr(mg)), "redraw_uniforms")
+    return out, mg
 
 
 def philox4x64(ctr, key) -> np.ndarray:

@@ -25,8 +25,10 @@
  *   orc_path_greedy .......... hand-worked golden lattice; A = 0 gives top-1
  *   orc_verify_greedy ........ equality with target-argmax decoding
  *   orc_verify_sampling ...... chi-square of emitted-token marginals against
- *                              the target softmax (1e6 draws; and draws over a
- *                              vocabulary of several redraw chunks); limiting cases
+ *                              the target softmax (1e6 draws; and redraws over a
+ *                              vocabulary of 9192 tokens); limiting cases
+ *   orc_redraw_uniforms ...... enumeration: on a grid of n uniforms each token is
+ *                              drawn n * (its residual probability) times, within one
  *   orc_philox4x64 ........... numpy.random.Philox raw output
  *   accept length ............ closed form that reproduces the [Blog] Table 1
  *                              verify lengths 4.27 / 6.79
@@ -111,8 +113,7 @@ inline double u01(uint64_t x) {
 /* Counter layout shared by definition (not by code) with the GPU path:
  *   key     = (seed, 0)
  *   accept  : counter (0, t, b, 0), word 0           -- position t = 1..L-1
- *   chunk   : counter (0, t, b, 2), word 0           -- the redraw's chunk choice
- *   inchunk : counter (0, t, b, 1), word 0           -- the redraw within the chunk
+ *   redraw  : counter (0, t, b, 1), word 0           -- the redraw's one uniform
  *   path    : counter (0, t, b, 3), word 0           -- the sampled path's draw at t
  * The redraw from row t-1 uses position t; the bonus row L-1 uses t = L. */
 double uniform_counter(uint64_t seed, int64_t b, int t, uint64_t idx, uint64_t stream, int word) {
@@ -125,14 +126,9 @@ double uniform_counter(uint64_t seed, int64_t b, int t, uint64_t idx, uint64_t s
 
 double uniform_accept(uint64_t seed, int64_t b, int t) { return uniform_counter(seed, b, t, 0, 0, 0); }
 
-double uniform_inchunk(uint64_t seed, int64_t b, int t) { return uniform_counter(seed, b, t, 0, 1, 0); }
-
-double uniform_chunk(uint64_t seed, int64_t b, int t) { return uniform_counter(seed, b, t, 0, 2, 0); }
+double uniform_redraw(uint64_t seed, int64_t b, int t) { return uniform_counter(seed, b, t, 0, 1, 0); }
 
 double uniform_path(uint64_t seed, int64_t b, int t) { return uniform_counter(seed, b, t, 0, 3, 0); }
-
-/* Tokens per chunk of the two-stage redraw. */
-const int64_t kRedrawChunk = 4096;
 
 /* log-sum-exp of z/T over one row, in double. */
 double row_lse(const void* Z, int zdtype, int64_t off, int64_t V, double T) {
@@ -145,8 +141,8 @@ double row_lse(const void* Z, int zdtype, int64_t off, int64_t V, double T) {
 
 /* Inverse-CDF draw over the weights w[0..n) (w >= 0) with one uniform u: the first index
  * whose cumulative weight exceeds u * sum(w) (in index order); if rounding leaves none, the
- * last index with weight. Returns -1 when every weight is zero. margin = the smallest
- * distance of the target u * sum(w) to a cumulative boundary, relative to the sum. */
+ * last index with weight. Returns -1 when every weight is zero. margin = the distance of
+ * the target u * sum(w) to the nearest cumulative boundary, relative to the sum. */
 int64_t inverse_cdf(const std::vector<double>& w, double u, double* margin) {
   double total = 0.0;
   int64_t last = -1;
@@ -168,85 +164,34 @@ int64_t inverse_cdf(const std::vector<double>& w, double u, double* margin) {
   return pick < 0 ? last : pick;
 }
 
-/* An exact draw from p = softmax(z/T) with token excl removed (excl < 0: none) and
- * renormalised, in two stages: (1) a chunk of kRedrawChunk consecutive tokens is chosen
- * with probability proportional to its mass under the residual distribution, by one
- * uniform against the chunks' cumulative masses in vocabulary order (if rounding leaves
- * no chunk above the target, the last chunk with mass is taken); (2) the token, by a second
- * uniform against the cumulative masses of the chunk's tokens in vocabulary order (the
- * inverse CDF, exact like the first stage). P(v) = (mass_c / total) (p_v / mass_c) =
- * p_v / total. margin = the smaller of the two stages' relative distances to a cumulative
- * boundary. */
-int64_t redraw(const void* Z, int zdtype, int64_t off, int64_t V, double T, uint64_t seed,
-               int64_t b, int t, int64_t excl, double* margin) {
+/* An exact draw from p = softmax(z/T) over one row with token excl removed (excl < 0:
+ * none) and renormalised: the weights exp(z_v/T - max) of every other token, cumulated in
+ * vocabulary order, against the one uniform u (inverse_cdf). margin as inverse_cdf's. */
+int64_t redraw(const void* Z, int zdtype, int64_t off, int64_t V, double T, double u, int64_t excl,
+               double* margin) {
   double m = -kInf;
   for (int64_t v = 0; v < V; ++v) m = std::max(m, widen(Z, zdtype, off + v) / T);
-  const int64_t nchunk = (V + kRedrawChunk - 1) / kRedrawChunk;
-  std::vector<double> mass(nchunk, 0.0);
-  for (int64_t c = 0; c < nchunk; ++c)
-    for (int64_t v = c * kRedrawChunk; v < std::min(V, (c + 1) * kRedrawChunk); ++v)
-      if (v != excl) mass[c] += std::exp(widen(Z, zdtype, off + v) / T - m);
-  double total = 0.0;
-  for (int64_t c = 0; c < nchunk; ++c) total += mass[c];
-  const double target = uniform_chunk(seed, b, t) * total;
-  int64_t pick = -1, last_nonzero = 0;
-  double cum = 0.0, cmargin = kInf;
-  for (int64_t c = 0; c < nchunk; ++c) {
-    cum += mass[c];
-    if (mass[c] > 0.0) last_nonzero = c;
-    if (c + 1 < nchunk) cmargin = std::min(cmargin, std::fabs(cum - target) / total);
-    if (pick < 0 && cum > target) pick = c;
-  }
-  if (pick < 0) pick = last_nonzero;
-  const int64_t lo = pick * kRedrawChunk, hi = std::min(V, (pick + 1) * kRedrawChunk);
-  std::vector<double> w(hi - lo);
-  for (int64_t v = lo; v < hi; ++v) w[v - lo] = (v != excl) ? std::exp(widen(Z, zdtype, off + v) / T - m) : 0.0;
-  double imargin;
-  const int64_t y = inverse_cdf(w, uniform_inchunk(seed, b, t), &imargin);
-  *margin = std::min(cmargin, imargin);
-  return y < 0 ? lo : lo + y;
+  std::vector<double> w(V);
+  for (int64_t v = 0; v < V; ++v) w[v] = (v != excl) ? std::exp(widen(Z, zdtype, off + v) / T - m) : 0.0;
+  const int64_t y = inverse_cdf(w, u, margin);
+  return y < 0 ? 0 : y;
 }
 
 /* An exact draw from the residual r(v) = max(0, p(v) - q(v)) renormalised, with
  * p = softmax(z/T) over the row and q a proposal that is nonzero only on the K listed
- * candidates (cand[k] with probability qv[k]); K = 0 draws from p itself. The same two
- * stages as redraw(): a chunk by its residual mass, then the inverse CDF of r over the
- * chunk. For a proposal that puts all its mass on one token this is redraw() with that
- * token excluded (the weights differ from redraw()'s by the row's constant normaliser). */
-int64_t redraw_residual(const void* Z, int zdtype, int64_t off, int64_t V, double T, uint64_t seed,
-                        int64_t b, int t, const int32_t* cand, const double* qv, int K,
-                        double* margin) {
+ * candidates (cand[k] with probability qv[k]); K = 0 draws from p itself. The weights r(v),
+ * cumulated in vocabulary order, against the one uniform u (inverse_cdf). For a proposal
+ * that puts all its mass on one token this is redraw() with that token excluded (the
+ * weights differ from redraw()'s by the row's constant normaliser). */
+int64_t redraw_residual(const void* Z, int zdtype, int64_t off, int64_t V, double T, double u,
+                        const int32_t* cand, const double* qv, int K, double* margin) {
   const double lse = row_lse(Z, zdtype, off, V, T);
-  auto resid = [&](int64_t v) {  // r(v), and whether v is a listed candidate
-    const double pv = std::exp(widen(Z, zdtype, off + v) / T - lse);
-    for (int k = 0; k < K; ++k)
-      if (cand[k] == v) return std::max(0.0, pv - qv[k]);
-    return pv;
-  };
-  const int64_t nchunk = (V + kRedrawChunk - 1) / kRedrawChunk;
-  std::vector<double> mass(nchunk, 0.0);
-  for (int64_t c = 0; c < nchunk; ++c)
-    for (int64_t v = c * kRedrawChunk; v < std::min(V, (c + 1) * kRedrawChunk); ++v)
-      mass[c] += resid(v);
-  double total = 0.0;
-  for (int64_t c = 0; c < nchunk; ++c) total += mass[c];
-  const double target = uniform_chunk(seed, b, t) * total;
-  int64_t pick = -1, last_nonzero = 0;
-  double cum = 0.0, cmargin = kInf;
-  for (int64_t c = 0; c < nchunk; ++c) {
-    cum += mass[c];
-    if (mass[c] > 0.0) last_nonzero = c;
-    if (c + 1 < nchunk) cmargin = std::min(cmargin, std::fabs(cum - target) / total);
-    if (pick < 0 && cum > target) pick = c;
-  }
-  if (pick < 0) pick = last_nonzero;
-  const int64_t lo = pick * kRedrawChunk, hi = std::min(V, (pick + 1) * kRedrawChunk);
-  std::vector<double> w(hi - lo);
-  for (int64_t v = lo; v < hi; ++v) w[v - lo] = resid(v);
-  double imargin;
-  const int64_t y = inverse_cdf(w, uniform_inchunk(seed, b, t), &imargin);
-  *margin = std::min(cmargin, imargin);
-  return y < 0 ? lo : lo + y;
+  std::vector<double> w(V);
+  for (int64_t v = 0; v < V; ++v) w[v] = std::exp(widen(Z, zdtype, off + v) / T - lse);
+  for (int k = 0; k < K; ++k)
+    if (cand[k] >= 0 && cand[k] < V) w[cand[k]] = std::max(0.0, w[cand[k]] - qv[k]);
+  const int64_t y = inverse_cdf(w, u, margin);
+  return y < 0 ? 0 : y;
 }
 
 /* ---- E4M3, the OCP 8-bit floating-point format ("OCP 8-bit Floating Point
@@ -572,8 +517,8 @@ int orc_verify_greedy(int zdtype, const void* Z, int L, int64_t V, const int32_t
  * deterministic proposal. p_i = softmax(Z[i]/T). For t = 1..L-1: accept x_t
  * when U < p_{t-1}(x_t); on the first rejection emit a draw from p_{t-1}
  * with x_t removed and renormalised and stop (accept_len = t); when all are
- * accepted emit a bonus draw from p_{L-1} (accept_len = L). Draws use the
- * two-stage redraw above.
+ * accepted emit a bonus draw from p_{L-1} (accept_len = L). Each draw is redraw() above
+ * with the position's one redraw uniform.
  * acc_margin = smallest |U - p| / p over the tests made; draw_margin = the
  * redraw's margin. b is the request's batch index (part of the counter). */
 int orc_verify_sampling(int zdtype, const void* Z, int L, int64_t V, const int32_t* path,
@@ -592,13 +537,15 @@ int orc_verify_sampling(int zdtype, const void* Z, int L, int64_t V, const int32
       out[t - 1] = static_cast<int32_t>(x);
       continue;
     }
-    out[t - 1] = static_cast<int32_t>(redraw(Z, zdtype, off, V, T, seed, b, t, x, draw_margin));
+    out[t - 1] = static_cast<int32_t>(
+        redraw(Z, zdtype, off, V, T, uniform_redraw(seed, b, t), x, draw_margin));
     *accept_len = t;
     *acc_margin = am;
     return 0;
   }
   const int64_t off = static_cast<int64_t>(L - 1) * V;
-  out[L - 1] = static_cast<int32_t>(redraw(Z, zdtype, off, V, T, seed, b, L, -1, draw_margin));
+  out[L - 1] = static_cast<int32_t>(
+      redraw(Z, zdtype, off, V, T, uniform_redraw(seed, b, L), -1, draw_margin));
   *accept_len = L;
   *acc_margin = am;
   return 0;
@@ -690,7 +637,8 @@ int orc_verify_proposal(int zdtype, const void* Z, int L, int64_t V, const int32
       out[t - 1] = static_cast<int32_t>(x);
       continue;
     }
-    out[t - 1] = static_cast<int32_t>(redraw_residual(Z, zdtype, off, V, T, seed, b, t,
+    out[t - 1] = static_cast<int32_t>(redraw_residual(Z, zdtype, off, V, T,
+                                                      uniform_redraw(seed, b, t),
                                                       cand + static_cast<int64_t>(t - 1) * K,
                                                       q + static_cast<int64_t>(t - 1) * K, K,
                                                       draw_margin));
@@ -699,8 +647,8 @@ int orc_verify_proposal(int zdtype, const void* Z, int L, int64_t V, const int32
     return 0;
   }
   const int64_t off = static_cast<int64_t>(L - 1) * V;
-  out[L - 1] = static_cast<int32_t>(
-      redraw_residual(Z, zdtype, off, V, T, seed, b, L, nullptr, nullptr, 0, draw_margin));
+  out[L - 1] = static_cast<int32_t>(redraw_residual(Z, zdtype, off, V, T, uniform_redraw(seed, b, L),
+                                                    nullptr, nullptr, 0, draw_margin));
   *accept_len = L;
   *acc_margin = am;
   return 0;
@@ -731,6 +679,20 @@ int orc_sample_verify_many(int zdtype, const void* Z, int L, int64_t V, const do
     bad |= (rc != 0);
   }
   return bad ? -1 : 0;
+}
+
+/* The redraw of one target row Z [V] for given uniforms u [n] (instead of the counter's),
+ * for the enumeration pins: K = 0 draws from softmax(z/T) with token excl removed (excl < 0:
+ * none); K > 0 from the residual max(0, p - q) of the proposal cand [K] / qv [K] (excl is
+ * then ignored). out [n] token ids, margin [n] as inverse_cdf's. */
+int orc_redraw_uniforms(int zdtype, const void* Z, int64_t V, double T, int64_t excl,
+                        const int32_t* cand, const double* qv, int K, const double* u, int64_t n,
+                        int64_t* out, double* margin) {
+  if (V < 1 || !(T > 0.0) || K < 0 || n < 0) return -1;
+  for (int64_t i = 0; i < n; ++i)
+    out[i] = K > 0 ? redraw_residual(Z, zdtype, 0, V, T, u[i], cand, qv, K, margin + i)
+                   : redraw(Z, zdtype, 0, V, T, u[i], excl, margin + i);
+  return 0;
 }
 
 /* Raw Philox4x64-10 block, exposed for the library pin. */

@@ -10,8 +10,7 @@ the case is excluded from the exact comparison and counted):
       - top-16 set of a row: boundary gap u_16 - u_17 < TOPK_GAP * |u_16|;
       - path: smallest relative best-vs-second margin on the path < PATH_MARGIN;
       - sampling: an accept test with |U - p| / p < ACC_MARGIN, or a redraw whose target
-        lies within DRAW_MARGIN (relative to the total) of a cumulative boundary, in the
-        chunk choice or within the chunk;
+        lies within DRAW_MARGIN (relative to the row's total) of a cumulative boundary;
   * everywhere else token ids, paths and accept lengths must be identical.
 """
 from __future__ import annotations

@@ -111,7 +111,7 @@ def test_point_mass_proposal_is_the_deterministic_verification(orc):
         assert np.all(pidx == 3) and np.all(q[:, 3] == 1.0)
         a = orc.verify_proposal(Z, path, ids, q, pidx, T, seed)
         b = orc.verify_sampling(Z, path, T, seed)
-        if min(a[3], b[3]) < 1e-9:  # the two redraws' keys differ by a constant: near-ties
+        if min(a[3], b[3]) < 1e-9:  # the redraws' weights differ by a constant factor: near-ties
             continue
         assert a[0].tolist() == b[0].tolist() and a[1] == b[1]
 

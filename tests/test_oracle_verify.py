@@ -220,8 +220,8 @@ def test_sampling_depends_on_request_index_and_seed(orc):
 
 
 @pytest.fixture(scope="module")
-def multichunk_runs(orc):
-    """A vocabulary of three redraw chunks (4096, 4096, 1000 tokens) with very different
+def multiblock_runs(orc):
+    """A vocabulary of 9192 tokens in three blocks (4096, 4096, 1000) with very different
     masses; the proposal has negligible probability, so every draw is a redraw."""
     rng = np.random.default_rng(99)
     V, T = 2 * 4096 + 1000, 1.0
@@ -236,23 +236,79 @@ def multichunk_runs(orc):
     return dict(Z=Z, T=T, x=x, out=out, acc=acc, n=n, V=V)
 
 
-def test_redraw_chunk_choice_follows_residual_mass(multichunk_runs):
-    r = multichunk_runs
+def test_redraw_block_masses_follow_residual_target(multiblock_runs):
+    r = multiblock_runs
     assert np.all(r["acc"] == 1)
     p = _softmax(r["Z"][0], r["T"])
     p[r["x"]] = 0.0
     p /= p.sum()
-    chunk = r["out"][:, 0] // 4096
-    counts = np.bincount(chunk, minlength=3).astype(np.float64)
+    block = r["out"][:, 0] // 4096
+    counts = np.bincount(block, minlength=3).astype(np.float64)
     expect = np.array([p[:4096].sum(), p[4096:8192].sum(), p[8192:].sum()])
     assert _chi2_pvalue(counts, expect) > 0.01
 
 
-def test_redraw_token_distribution_is_residual_target(multichunk_runs):
-    r = multichunk_runs
+def test_redraw_token_distribution_is_residual_target(multiblock_runs):
+    r = multiblock_runs
     p = _softmax(r["Z"][0], r["T"])
     p[r["x"]] = 0.0
     p /= p.sum()
     counts = np.bincount(r["out"][:, 0], minlength=r["V"]).astype(np.float64)
     assert counts[r["x"]] == 0
     assert _chi2_pvalue(counts, p) > 0.01
+
+
+# ------------------------------------------------- the redraw enumerated over uniforms
+N_GRID = 1 << 16
+
+
+def _grid():
+    return (np.arange(N_GRID, dtype=np.float64) + 0.5) / N_GRID
+
+
+def _check_inverse_cdf(tokens, probs):
+    """On the grid of N uniforms (j + 1/2) / N, an exact inverse-CDF sampler in vocabulary
+    order draws each token a number of times within one of N times its probability (the
+    grid points in an interval of length p number N p rounded up or down), and the tokens
+    drawn do not decrease as the uniform grows."""
+    counts = np.bincount(tokens, minlength=probs.size).astype(np.float64)
+    assert counts.sum() == N_GRID
+    assert np.all(np.abs(counts - N_GRID * probs) <= 1.0), (counts, N_GRID * probs)
+    assert np.all(np.diff(tokens) >= 0)
+
+
+@pytest.mark.parametrize("V,T,excl", [(9, 0.7, 3), (9, 1.0, -1), (64, 2.5, 0), (64, 0.3, 63)])
+def test_redraw_enumerated_is_exact_without_the_rejected_token(orc, V, T, excl):
+    """The redraw after a rejected token x draws from softmax(z/T) with x removed and
+    renormalised ("DFlash 2: Keep Drafting Parallel", §"A lightweight path selector":
+    rejection sampling recovers the exact target distribution); without a rejected token
+    (the bonus row), from softmax(z/T) itself."""
+    rng = np.random.default_rng(V + excl + 7)
+    z = (rng.standard_normal(V) * 2).astype(np.float32)
+    p = _softmax(z, T)
+    if excl >= 0:
+        p[excl] = 0.0
+        p /= p.sum()
+    tok, _ = orc.redraw_uniforms(z, T, _grid(), excl=excl)
+    if excl >= 0:
+        assert not np.any(tok == excl)
+    _check_inverse_cdf(tok, p)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_redraw_enumerated_residual_of_a_sampled_proposal(orc, seed):
+    """The redraw after rejecting a sampled proposal q draws from max(0, p - q)
+    renormalised (speculative sampling's residual)."""
+    rng = np.random.default_rng(seed)
+    V, T, K = 40, 1.3, 6
+    z = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    p = _softmax(z, T)
+    cand = rng.choice(V, K, replace=False).astype(np.int32)
+    q = rng.dirichlet(np.ones(K))
+    r = p.copy()
+    r[cand] = np.maximum(0.0, p[cand] - q)
+    r /= r.sum()
+    tok, _ = orc.redraw_uniforms(z, T, _grid(), cand=cand, q=q)
+    _check_inverse_cdf(tok, r)
+    # a candidate that the proposal over-weights (q >= p) is never drawn
+    assert not np.any(np.isin(tok, cand[q >= p[cand]]))
