@@ -56,17 +56,15 @@ struct Layout {
   int G, nchunk;
 };
 
+// Everything after the verification's own checks: the LM head's width, rank and dtype.
 int check_dims(const dfs_dims* d) {
   if (d == nullptr) return DFS_ERR_INVALID;
-  if (d->B < 1 || d->L < 2 || d->K < 1 || d->V < 1 || d->d < 1 || d->r < 1) return DFS_ERR_INVALID;
-  if ((d->dtype != DFS_BF16 && d->dtype != DFS_FP32) || (d->zdtype != DFS_BF16 && d->zdtype != DFS_FP32))
-    return DFS_ERR_UNSUPPORTED;
-  if (d->K != kK || d->L > dfs::kMaxL || d->V < kK || d->V % 8 != 0) return DFS_ERR_UNSUPPORTED;
-  if (d->V > dfs::kMaxZChunks * dfs::kZChunk) return DFS_ERR_UNSUPPORTED;
+  if (d->d < 1 || d->r < 1) return DFS_ERR_INVALID;
+  const int rc = dfs::check_verify_dims(d);
+  if (rc != DFS_OK) return rc;
+  if (d->dtype != DFS_BF16 && d->dtype != DFS_FP32) return DFS_ERR_UNSUPPORTED;
   if (d->r % 8 != 0 || d->r > dfs::kMaxRank) return DFS_ERR_UNSUPPORTED;
   if (d->dtype == DFS_BF16 && d->d % 64 != 0) return DFS_ERR_UNSUPPORTED;
-  if (static_cast<long long>(d->B) * d->L > (1LL << 30)) return DFS_ERR_UNSUPPORTED;
-  if (d->B > 65535) return DFS_ERR_UNSUPPORTED;  // requests index the tail's second grid dimension
   return DFS_OK;
 }
 
@@ -294,6 +292,17 @@ std::atomic<unsigned long long> g_launches{0};
 
 namespace dfs {
 void note_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n)); }
+
+int check_verify_dims(const dfs_dims* d) {
+  if (d == nullptr) return DFS_ERR_INVALID;
+  if (d->B < 1 || d->L < 2 || d->K < 1 || d->V < 1) return DFS_ERR_INVALID;
+  if (d->zdtype != DFS_BF16 && d->zdtype != DFS_FP32) return DFS_ERR_UNSUPPORTED;
+  if (d->K != kK || d->L > kMaxL || d->V < kK || d->V % 8 != 0) return DFS_ERR_UNSUPPORTED;
+  if (d->V > kMaxZChunks * kZChunk) return DFS_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->B) * d->L > (1LL << 30)) return DFS_ERR_UNSUPPORTED;
+  if (d->B > 65535) return DFS_ERR_UNSUPPORTED;  // requests index the tail's second grid dimension
+  return DFS_OK;
+}
 }  // namespace dfs
 
 extern "C" {

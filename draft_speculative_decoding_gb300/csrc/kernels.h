@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/dfs.h"
+
 namespace dfs {
 
 constexpr int kK = 16;          // candidates kept per draft position
@@ -76,6 +78,10 @@ cudaError_t launch_conv2tap(const ConvLaunch& a, cudaStream_t s);
 // 128-byte swizzle, zero fill outside the matrix (the LM-head kernels' encoding).
 bool encode_bf16_2d_tile(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                          uint32_t inner_box, uint32_t outer_box);
+
+// The shape checks every verification entry point makes (dfs_verify, dfs_verify_noalloc and,
+// inside check_dims, every other call): B, L, K, V and zdtype. DFS_OK or the status to return.
+int check_verify_dims(const dfs_dims* d);
 
 // Adds n to the process-wide count of kernels this library has launched. Every launch site
 // calls it once the runtime has accepted the launch; dfs_launch_count reads the total.

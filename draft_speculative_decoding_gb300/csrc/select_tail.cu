@@ -119,38 +119,43 @@ __device__ __forceinline__ unsigned long long pack_key(float v, int id) {
 
 // ------------------------------------------------------------------ target rows
 // One block of 128 threads reduces kZChunk (4096) elements of one row of Z: each thread
-// holds 4 groups of 8 consecutive elements, the groups 1024 elements apart.
+// holds 4 groups of 8 consecutive elements, the groups 1024 elements apart. Block (c, y)
+// takes chunk c of rows y, y + gridDim.y, ... (any number of rows with at most 65535 blocks
+// in the second grid dimension).
 template <bool kSoft>
-__global__ void __launch_bounds__(128) k_zreduce(const void* Z, int is_bf16, int V, int nchunk,
-                                                 float inv_T, float* zmax, int* zarg, float* zsum,
-                                                 int* zero_ptr, int zero_count) {
+__global__ void __launch_bounds__(128) k_zreduce(const void* Z, int is_bf16, int rows, int V,
+                                                 int nchunk, float inv_T, float* zmax, int* zarg,
+                                                 float* zsum, int* zero_ptr, int zero_count) {
   if (blockIdx.x == 0 && blockIdx.y == 0 && zero_ptr != nullptr)
     for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero_ptr[i] = 0;
-  const int row = blockIdx.y, chunk = blockIdx.x;
-  const size_t rbase = static_cast<size_t>(row) * V;
-  float x[4][8];
-  int v0[4];
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    v0[g] = chunk * kZChunk + g * 1024 + threadIdx.x * 8;
-    if (v0[g] < V) load8_stream(Z, is_bf16, rbase + v0[g], x[g]);
-  }
-  RowStat st = rowstat_empty();
-  rowstat_fold<4, kSoft>(st, x, v0, V, inv_T);
-  st = warp_combine(st, inv_T);
+  const int chunk = blockIdx.x;
   __shared__ RowStat ws[4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) ws[warp] = st;
-  __syncthreads();
-  if (warp == 0) {
-    st = lane < 4 ? ws[lane] : rowstat_empty();
-    st = warp_combine(st, inv_T);
-    if (lane == 0) {
-      const size_t o = static_cast<size_t>(row) * nchunk + chunk;
-      zmax[o] = st.m;
-      zarg[o] = st.i;
-      if (kSoft) zsum[o] = st.s;
+  for (int row = blockIdx.y; row < rows; row += gridDim.y) {
+    const size_t rbase = static_cast<size_t>(row) * V;
+    float x[4][8];
+    int v0[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      v0[g] = chunk * kZChunk + g * 1024 + threadIdx.x * 8;
+      if (v0[g] < V) load8_stream(Z, is_bf16, rbase + v0[g], x[g]);
     }
+    RowStat st = rowstat_empty();
+    rowstat_fold<4, kSoft>(st, x, v0, V, inv_T);
+    st = warp_combine(st, inv_T);
+    if (lane == 0) ws[warp] = st;
+    __syncthreads();
+    if (warp == 0) {
+      st = lane < 4 ? ws[lane] : rowstat_empty();
+      st = warp_combine(st, inv_T);
+      if (lane == 0) {
+        const size_t o = static_cast<size_t>(row) * nchunk + chunk;
+        zmax[o] = st.m;
+        zarg[o] = st.i;
+        if (kSoft) zsum[o] = st.s;
+      }
+    }
+    __syncthreads();  // ws is rewritten by the next row
   }
 }
 
@@ -1168,13 +1173,13 @@ cudaError_t allow_smem() {
 }  // namespace
 
 cudaError_t launch_zreduce(const ZReduceLaunch& a, cudaStream_t s) {
-  dim3 grid(a.nchunk, a.rows);
+  dim3 grid(a.nchunk, a.rows < 65535 ? a.rows : 65535);
   if (a.inv_T > 0.f)
-    k_zreduce<true><<<grid, 128, 0, s>>>(a.Z, a.zdtype == 0, a.V, a.nchunk, a.inv_T, a.zmax,
-                                         a.zarg, a.zsum, a.zero_ptr, a.zero_count);
+    k_zreduce<true><<<grid, 128, 0, s>>>(a.Z, a.zdtype == 0, a.rows, a.V, a.nchunk, a.inv_T,
+                                         a.zmax, a.zarg, a.zsum, a.zero_ptr, a.zero_count);
   else
-    k_zreduce<false><<<grid, 128, 0, s>>>(a.Z, a.zdtype == 0, a.V, a.nchunk, 0.f, a.zmax,
-                                          a.zarg, a.zsum, a.zero_ptr, a.zero_count);
+    k_zreduce<false><<<grid, 128, 0, s>>>(a.Z, a.zdtype == 0, a.rows, a.V, a.nchunk, 0.f,
+                                          a.zmax, a.zarg, a.zsum, a.zero_ptr, a.zero_count);
   return counted(cudaGetLastError());
 }
 

@@ -16,7 +16,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "../../include/dfs.h"
 #include "kernels.h"
@@ -32,19 +31,12 @@ inline size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 // The device address of g_verify_scratch on the current device. In host code the array's
 // name only stands in for the symbol; the address a kernel can use comes from the runtime,
-// once per device, with that device current (the first call on each device does this).
+// asked on every call with the caller's device current (a lookup that allocates nothing), so
+// it is never stale, even after the device's context has been reset and created again.
 void* scratch_on_current_device() {
-  static std::mutex mu;
-  static void* addr[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr) return nullptr;
-    addr[dev] = p;
-  }
-  return addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess) return nullptr;
+  return p;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -54,17 +46,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 extern "C" int dfs_verify_noalloc(const dfs_dims* d, const int32_t* path,
                                   const void* target_logits, float temperature, uint64_t seed,
                                   int32_t* out_tokens, int32_t* accept_len, void* stream) {
-  if (d == nullptr || path == nullptr || target_logits == nullptr || out_tokens == nullptr ||
-      accept_len == nullptr)
+  // the same shape checks as dfs_verify, then the same argument checks
+  const int rc = dfs::check_verify_dims(d);
+  if (rc != DFS_OK) return rc;
+  if (!(temperature >= 0.f)) return DFS_ERR_INVALID;
+  if (path == nullptr || target_logits == nullptr || out_tokens == nullptr || accept_len == nullptr)
     return DFS_ERR_INVALID;
   if (!aligned16(path) || !aligned16(target_logits) || !aligned16(out_tokens) ||
       !aligned16(accept_len))
     return DFS_ERR_INVALID;
-  if (d->B < 1 || d->L < 2 || d->V < 1) return DFS_ERR_INVALID;
-  if (!(temperature >= 0.f)) return DFS_ERR_INVALID;
-  if (d->K != dfs::kK || d->L > dfs::kMaxL || d->V < dfs::kK || d->V % 8 != 0 ||
-      d->V > dfs::kMaxZChunks * dfs::kZChunk || (d->zdtype != DFS_BF16 && d->zdtype != DFS_FP32))
-    return DFS_ERR_UNSUPPORTED;
 
   const size_t B = static_cast<size_t>(d->B);
   const size_t rows = B * static_cast<size_t>(d->L);

@@ -178,12 +178,15 @@ int dfs_verify(const dfs_dims* dims, const int32_t* path, const void* target_log
  *   library until the process exits. The call returns DFS_ERR_WORKSPACE when the shape
  *   needs more, roughly when 12 * B * L * ceil(V / 4096) + 4 * B bytes exceed 4 MiB
  *   (B * L up to about 9000 at V = 151936).
- *   Set-up: the first call on each device asks the runtime for the array's device address,
- *   with that device current; make that first call before any stream capture.
+ *   Set-up: every call asks the runtime for the array's device address on the current
+ *   device (a lookup that allocates nothing), so the address stays right even after the
+ *   device's context is reset and created again. The first call on a device may also load
+ *   the library's device code there; make that first call before any stream capture.
  *   Sharing: all calls use the one array, which keeps the last call's contents; each call
  *   clears the counters it needs. Calls that overlap on the GPU (other streams, other host
  *   threads) race on it: issue them one after another on one stream.
- *   Arguments: as dfs_verify; of dims only B, L, K, V and zdtype are read. */
+ *   Arguments: as dfs_verify; of dims only B, L, K, V and zdtype are read, and they are
+ *   checked exactly as dfs_verify checks them. */
 int dfs_verify_noalloc(const dfs_dims* dims, const int32_t* path, const void* target_logits,
                        float temperature, uint64_t seed, int32_t* out_tokens, int32_t* accept_len,
                        void* stream);

@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from draft_speculative_decoding_gb300 import binding, build
 
@@ -82,4 +83,26 @@ def test_host_limits_of_the_convolution_and_the_hand_off(lib):
     big = binding.make_dims(65536, 2, 1024, 256, 32, 0, 0)  # more requests than the grid holds
     assert lib.dfs_path_select(ctypes.byref(big), None, None, 0, None, None, None) == \
         binding.DFS_ERR_UNSUPPORTED
+    assert binding.dfs_launch_count() == launches
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-only check; the GPU test covers it there")
+def test_noalloc_host_checks(lib):
+    """dfs_verify_noalloc rejects on the host, before any device call: a shape whose row
+    statistics exceed its built-in scratch (DFS_ERR_WORKSPACE), the shapes dfs_verify
+    rejects (the same checks), and a negative temperature."""
+    P = ctypes.c_void_p
+    launches = binding.dfs_launch_count()
+    args = (P(0x1000), P(0x2000), 0.0, 0, P(0x3000), P(0x4000), None)
+    big = binding.make_dims(22, 16, 4194304, 64, 8, 0, 0)
+    assert lib.dfs_verify_noalloc(ctypes.byref(big), *args) == binding.DFS_ERR_WORKSPACE
+    for B, L, V, K in ((65536, 2, 1024, 16), (2, 17, 1024, 16), (2, 8, 1020, 16), (2, 8, 1024, 8)):
+        dims = binding.make_dims(B, L, V, 64, 8, 0, 0)
+        dims.K = K
+        assert lib.dfs_verify_noalloc(ctypes.byref(dims), *args) == binding.DFS_ERR_UNSUPPORTED
+        assert lib.dfs_verify(ctypes.byref(dims), P(0x1000), P(0x2000), 0.0, 0, P(0x3000),
+                              P(0x4000), P(0x5000), 1 << 30, None) == binding.DFS_ERR_UNSUPPORTED
+    ok = binding.make_dims(2, 8, 1024, 64, 8, 0, 0)
+    assert lib.dfs_verify_noalloc(ctypes.byref(ok), P(0x1000), P(0x2000), -1.0, 0, P(0x3000),
+                                  P(0x4000), None) == binding.DFS_ERR_INVALID
     assert binding.dfs_launch_count() == launches

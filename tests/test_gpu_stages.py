@@ -171,3 +171,30 @@ def test_verify_sampling(lib, orc, T, L, V):
             assert am < ACC_MARGIN or gm < DRAW_MARGIN, f"request {b}: differs without a near-tie"
             diverged += 1
     assert diverged <= B // 16
+
+
+def test_verify_greedy_more_rows_than_one_grid_dimension(lib):
+    """More target rows than the 65535 blocks of a grid's second dimension (4375 requests of
+    16 positions = 70000 rows over a 4096-token vocabulary): the row statistics still cover
+    every row. Every request is checked against target-argmax decoding of its rows, which
+    greedy verification must reproduce token for token."""
+    rng = np.random.default_rng(70000)
+    B, L, V = 4375, 16, 4096
+    Zt = (torch.randn(B, L, V, device="cuda", generator=torch.Generator("cuda").manual_seed(3))
+          * 3).to(torch.bfloat16)
+    y = Zt.float().argmax(-1)  # lower id on ties, as the library's rule
+    path = y[:, :L - 1].clone()
+    flip = torch.from_numpy(rng.random((B, L - 1)) > 0.9).cuda()
+    path[flip] = (path[flip] + 1) % V
+    path = path.to(torch.int32).contiguous()
+    dims = binding.make_dims(B, L, V, 64, 8, binding.DFS_BF16, binding.DFS_BF16)
+    ws = binding.alloc_workspace(dims)
+    out, acc = binding.dfs_verify(dims, path, Zt, 0.0, 0, ws)
+    torch.cuda.synchronize()
+    y, path, out, acc = to_cpu(y), to_cpu(path), to_cpu(out), to_cpu(acc)
+    agree = path == y[:, :L - 1]
+    n = np.where(agree.all(1), L - 1, np.argmin(agree, axis=1))  # leading agreements
+    assert np.array_equal(acc, n + 1)
+    for b in range(B):
+        assert out[b, :n[b]].tolist() == path[b, :n[b]].tolist()
+        assert out[b, n[b]] == y[b, n[b]] and np.all(out[b, n[b] + 1:] == -1)

@@ -52,8 +52,37 @@ def test_noalloc_matches_workspace_verify_twice(lib, T, zdtype):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(lib):
-    dims = binding.make_dims(4096, 16, 151936, 64, 8, binding.DFS_BF16, binding.DFS_BF16)
-    rc = lib.dfs_verify_noalloc(ctypes.byref(dims), ctypes.c_void_p(0x1000),
-                                ctypes.c_void_p(0x2000), 0.0, 0, ctypes.c_void_p(0x3000),
-                                ctypes.c_void_p(0x4000), None)
+    """22 requests of 16 positions over the largest vocabulary (4194304 tokens, 1024 chunks)
+    need more than the built-in 4 MiB of row statistics: the call returns DFS_ERR_WORKSPACE.
+    Every buffer is real and as large as the shape says (the target logits take 2.95 GB), so
+    nothing the call could launch would read outside them."""
+    B, L, V = 22, 16, 4194304
+    dims = binding.make_dims(B, L, V, 64, 8, binding.DFS_BF16, binding.DFS_BF16)
+    Z = torch.empty(B, L, V, dtype=torch.bfloat16, device="cuda")
+    path = torch.zeros(B, L - 1, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, L, dtype=torch.int32, device="cuda")
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    before = binding.dfs_launch_count()
+    rc = lib.dfs_verify_noalloc(ctypes.byref(dims), binding._ptr(path), binding._ptr(Z), 0.0, 0,
+                                binding._ptr(out), binding._ptr(acc), None)
     assert rc == binding.DFS_ERR_WORKSPACE
+    assert binding.dfs_launch_count() == before  # rejected before anything was enqueued
+    del Z
+
+
+@pytest.mark.parametrize("T", [0.0, 0.8])
+def test_noalloc_more_rows_than_one_grid_dimension(lib, T):
+    """70000 target rows (more than a grid's second dimension holds) fit the scratch at a
+    4096-token vocabulary; two calls in a row agree with dfs_verify."""
+    B, L, V = 4375, 16, 4096
+    dims = binding.make_dims(B, L, V, 64, 8, binding.DFS_BF16, binding.DFS_BF16)
+    ws = binding.alloc_workspace(dims)
+    gen = torch.Generator("cuda").manual_seed(17)
+    for call in range(2):
+        Z = (torch.randn(B, L, V, device="cuda", generator=gen) * 3).to(torch.bfloat16)
+        path = Z.float().argmax(-1)[:, :L - 1].to(torch.int32).contiguous()
+        path[::3, 2] = (path[::3, 2] + 1) % V
+        ref_out, ref_acc = binding.dfs_verify(dims, path, Z, T, 40 + call, ws)
+        out, acc = binding.dfs_verify_noalloc(dims, path, Z, T, 40 + call)
+        torch.cuda.synchronize()
+        assert torch.equal(acc, ref_acc) and torch.equal(out, ref_out), f"call {call}"
