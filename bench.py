@@ -30,6 +30,7 @@ import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
+sys.path.insert(1, os.path.join(ROOT, "tests"))  # the planted-target checks of the loop leg
 
 METRIC = "draft blocks/s for select+verify at B=32,L=8,V=151936; % of HBM roofline"
 UNIT = "blocks/s"
@@ -126,7 +127,12 @@ class ClockSampler:
         except ValueError:
             return None
 
-    def stop(self):
+    def in_window(self, t0, t1):
+        return [r for r in list(self.rows) if (w := self._when(r[0])) is not None and t0 <= w <= t1]
+
+    def stop(self, t0=None, t1=None):
+        """Stops sampling; summarises the samples taken between t0 and t1 (default: the
+        marked window)."""
         if self.proc is None:
             return None
         time.sleep(0.15)  # let the sample that covers the window's end arrive
@@ -137,10 +143,11 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        t0, t1 = self.window
+        t0 = self.window[0] if t0 is None else t0
+        t1 = self.window[1] if t1 is None else t1
         rows = self.rows
         if t0 is not None and t1 is not None:
-            rows = [r for r in rows if (w := self._when(r[0])) is not None and t0 <= w <= t1]
+            rows = self.in_window(t0, t1)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -233,7 +240,28 @@ def run_ours(args):
         uuid = None
     clocks = ClockSampler(uuid)
     ms_greedy, _, launches = timed(0.0, args.steps, args.warmup, clocks=clocks)
-    clk = clocks.stop()
+    # The sampler reports every 50 ms. When the timed region held fewer than 10 samples, the
+    # same greedy steps keep running, untimed, for 0.6 s right after it, and the clock record
+    # comes from those samples (said so in the record).
+    t_win = clocks.window[:]
+    clk_note = "samples taken inside the timed region"
+    if clocks.proc is not None and len(clocks.in_window(*t_win)) < 10:
+        t_probe0 = datetime.datetime.now()
+        i = 0
+        while (datetime.datetime.now() - t_probe0).total_seconds() < 0.6:
+            for _ in range(20):
+                step(args.warmup + args.steps + i, 0.0)
+                i += 1
+            torch.cuda.synchronize()
+        t_win = [t_probe0, datetime.datetime.now()]
+        clk_note = (f"the timed region ({ms_greedy * args.steps:.1f} ms) is shorter than 10 "
+                    f"sampler periods: samples taken over {i} more of the same greedy steps "
+                    f"run untimed right after it")
+    clk = clocks.stop(*t_win)
+    if clk is not None:
+        clk["window"] = clk_note
+        if clk.get("sm_mhz"):
+            clk["sm_kcycles_per_step"] = round(ms_greedy * clk["sm_mhz"], 1)
     # the dominant kernel's own duration, from events recorded around it on its stream (a
     # separate pass: an event between two kernels stops the second launching early)
     _, lm_ms, _ = timed(0.0, args.steps, 1, trace=True)
@@ -358,6 +386,7 @@ def run_ours(args):
     # recorded into one CUDA graph, for B = 1, 8 and the workload's B (its first requests).
     # Planted: at the workload's B, staged greedy cycles against targets whose argmax agrees
     # with each drafted token with the page's Table 1 Recall@1 rates (closed form 4.27).
+    import planted
     from draft_speculative_decoding_gb300 import cycles as cyc_mod
     cyc_legs = {}
     n_cyc = 30
@@ -400,18 +429,18 @@ def run_ours(args):
                               "accepted_tokens_per_s": round(mean_acc_c * Bc * 1e3 / ms_cyc, 1),
                               "mean_accept_len": round(mean_acc_c, 3)}
         del g_c, ws_c
-    if spec.L - 1 == len(cyc_mod.TABLE1_RECALL_AT_1):
+    if spec.L - 1 == len(planted.TABLE1_RECALL_AT_1):
         gen_p = torch.Generator(device=dev).manual_seed(spec.seed + 7)
         x0p = data["x0"].clone()
-        runs = cyc_mod.planted_cycles(dims, data, hs, Zs[0], x0p, ws, cyc_mod.TABLE1_RECALL_AT_1,
+        runs = planted.planted_cycles(dims, data, hs, Zs[0], x0p, ws, planted.TABLE1_RECALL_AT_1,
                                       40, gen_p)
         torch.cuda.synchronize()
         acc_p = torch.stack([a for a, _ in runs]).float()
-        exact_p = all(torch.equal(a.long(), cyc_mod.leading_agreements(g)) for a, g in runs)
+        exact_p = all(torch.equal(a.long(), planted.leading_agreements(g)) for a, g in runs)
         planted = {"cycles": 40, "requests": spec.B,
                    "mean_accept_len": round(acc_p.mean().item(), 3),
                    "std_error": round(acc_p.std().item() / math.sqrt(acc_p.numel()), 3),
-                   "closed_form": round(cyc_mod.closed_form_accept_len(cyc_mod.TABLE1_RECALL_AT_1), 3),
+                   "closed_form": round(planted.closed_form_accept_len(planted.TABLE1_RECALL_AT_1), 3),
                    "every_accept_len_as_planted": exact_p}
         assert binding.dfs_get_device_error(ws) == binding.DFS_OK
     else:  # the Recall@1 rates are given for blocks of 8 only
@@ -512,9 +541,17 @@ def run_ours(args):
     lm_kernel = ("k_lmhead_vt" if vt else "k_lmhead_pair" if rows > 128 else "k_lmhead_tc") + \
         " (LM head + top-16 + gate tiles + target-row statistics)"
 
-    cpu = None
+    cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(data, spec, args.cpu_seconds)
+        gpu_ref = {}
+        for T in (0.0, args.sampling_temperature):  # the inputs the oracle's leg reads
+            res = binding.dfs_select_verify(dims, data["h"], data["W"], data["Wg"], data["A"],
+                                            data["Bt"], data["x0"], data["Z"], mode, T, spec.seed,
+                                            ws, want_intermediates=True, stream=stream)
+            torch.cuda.synchronize()
+            gpu_ref[T] = {k: v.cpu().numpy() for k, v in res.items()}
+        cpu, parity = cpu_baseline(data, spec, args.cpu_seconds, mode,
+                                   args.sampling_temperature, gpu_ref)
 
     if rank == 0:
         line = {
@@ -526,7 +563,8 @@ def run_ours(args):
                        "d": spec.d, "r": spec.r, "path_mode": args.path_mode,
                        "temperature": 0.0, "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2: W_vocab {w_bytes / 1e9:.2f} GB read "
-                             f"every step; {nrot} rotating target-logit and hidden buffers"},
+                             f"every step"},
+            "l2_rotation": f"{nrot} rotating target-logit and hidden buffers",
             "hbm_roofline_frac_step": round(step_achieved / peaks["hbm_gbs"], 4),
             "roofline": {"kernel": lm_kernel,
                          "bound": "hbm", "achieved": round(achieved, 1),
@@ -580,30 +618,87 @@ def run_ours(args):
             "gpu_launches": launches,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "parity": parity,
         }
         print(json.dumps(line), flush=True)
     replicas.finalize()
 
 
-def cpu_baseline(data, spec, budget_s):
-    """The fp64 oracle as it stands, on this host's cores, over requests of the same batch
-    until the time budget is spent (at least one request)."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model", "CPU part"):
+            for line in info.splitlines():
+                if line.lower().startswith(key.lower()) and ":" in line:
+                    return f"{key}: {line.split(':', 1)[1].strip()}"
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def cpu_baseline(data, spec, budget_s, path_mode, T_samp, gpu_ref):
+    """The fp64 oracle as it stands, on this host's cores: requests of the same batch, one
+    call each, until the time budget is spent (at least one request), greedy (T = 0) and
+    sampling (T_samp), all cores; and one request on one core. The oracle's outputs of the
+    greedy and sampling runs are then compared with the GPU's outputs for the same inputs
+    and seeds (gpu_ref), request by request, with the near-tie exclusions counted per rule."""
+    import numpy as np
+
     import oracle
+    import parity as par
     from draft_speculative_decoding_gb300 import workloads as wl
 
     npd = {k: wl.to_numpy_bits(data[k]) for k in ("h", "W", "Wg", "A", "Bt", "x0", "Z")}
     threads = oracle.default_threads()
     oracle.build()
-    n, t0 = 0, time.perf_counter()
-    while n < spec.B and (n == 0 or time.perf_counter() - t0 < budget_s):
-        oracle.select_verify(npd["h"], npd["W"], npd["Wg"], npd["A"], npd["Bt"], npd["x0"],
-                             npd["Z"], path_mode=0, temperature=0.0, seed=spec.seed, reqs=[n],
-                             nthreads=threads)
-        n += 1
-    dt = time.perf_counter() - t0
-    return {"value": round(n / dt, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{n} of {spec.B} requests of {spec.name}, greedy path, T=0, "
-                      f"{dt:.1f} s wall"}
+
+    def run(T, nthreads, budget, max_req):
+        outs, n, t0 = [], 0, time.perf_counter()
+        while n < max_req and (n == 0 or time.perf_counter() - t0 < budget):
+            outs.append(oracle.select_verify(npd["h"], npd["W"], npd["Wg"], npd["A"], npd["Bt"],
+                                             npd["x0"], npd["Z"], path_mode=path_mode,
+                                             temperature=T, seed=spec.seed, reqs=[n],
+                                             nthreads=nthreads))
+            n += 1
+        return n, time.perf_counter() - t0, outs
+
+    n_g, dt_g, outs_g = run(0.0, threads, budget_s, spec.B)
+    n_s, dt_s, outs_s = run(T_samp, threads, budget_s, spec.B)
+    n_1, dt_1, _ = run(0.0, 1, 0.0, 1)
+    checks = {}
+    for T, outs in ((0.0, outs_g), (T_samp, outs_s)):
+        o = {k: np.concatenate([x[k] for x in outs]) for k in outs[0] if k != "reqs"}
+        tally = par.new_tally()
+        tally["mismatch"] = 0
+        for q in range(len(outs)):
+            try:
+                par.compare_request(gpu_ref[T], o, q, q, spec, T, tally)
+            except AssertionError:
+                tally["mismatch"] += 1
+        checks["greedy" if T == 0 else f"sampling_T{T}"] = tally
+    mode = {0: "greedy", 1: "viterbi"}[path_mode]
+    base = {"value": round(n_g / dt_g, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "sample": f"{n_g} of {spec.B} requests of {spec.name}, {mode} path, T=0, "
+                      f"{dt_g:.1f} s wall",
+            "single_core": {"value": round(n_1 / dt_1, 4), "unit": UNIT, "cores": 1,
+                            "sample": f"1 request, {mode} path, T=0, {dt_1:.1f} s wall"},
+            "sampling": {"temperature": T_samp, "value": round(n_s / dt_s, 4), "unit": UNIT,
+                         "cores": threads,
+                         "sample": f"{n_s} of {spec.B} requests, {mode} path, T={T_samp}, "
+                                   f"{dt_s:.1f} s wall"}}
+    return base, {"workload": spec.name, "compared": "GPU vs oracle on the requests the "
+                  "oracle ran above (same inputs and seeds)", **checks}
 
 
 # ------------------------------------------------------------------- reference arm (oracle)
@@ -645,9 +740,12 @@ def run_reference(args):
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": spec.name, "B": spec.B, "L": spec.L, "K": 16, "V": spec.V,
-                   "d": spec.d, "r": spec.r, "path_mode": "greedy", "temperature": 0.0},
+                   "d": spec.d, "r": spec.r, "path_mode": "greedy", "temperature": 0.0,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: W_vocab {spec.d * spec.V * 2 / 1e9:.2f} GB "
+                         f"read every step"},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)

@@ -256,31 +256,6 @@ def conv_inputs(spec: ConvSpec, device="cpu") -> dict:
     return {"x": x.to(device), "base": base.float().contiguous().to(device), "Wc": Wc.to(device)}
 
 
-def plant_target_argmax(Z: torch.Tensor, path: torch.Tensor, recall, gen: torch.Generator):
-    """Synthetic target for a decode loop: in place, each target row i of Z [B, L, V] gets a
-    planted argmax (logit 64, above any drawn value) that equals the drafted token path[:, i]
-    with probability recall[i], independently per row and request, and otherwise another
-    token drawn uniformly; the bonus row L-1 gets a uniform token. Returns (agree [B, L-1]
-    bool, handle) where handle restores Z with restore_target(Z, handle)."""
-    B, L, V = Z.shape
-    dev = Z.device
-    r = torch.as_tensor(list(recall)[:L - 1], dtype=torch.float32, device=dev)
-    agree = torch.rand(B, L - 1, generator=gen, device=dev) < r[None, :]
-    other = (path.long() + 1 + torch.randint(0, V - 1, (B, L - 1), generator=gen, device=dev)) % V
-    tok = torch.cat([torch.where(agree, path.long(), other),
-                     torch.randint(0, V, (B, 1), generator=gen, device=dev)], dim=1)
-    bi = torch.arange(B, device=dev)[:, None].expand(B, L)
-    ti = torch.arange(L, device=dev)[None, :].expand(B, L)
-    saved = Z[bi, ti, tok].clone()
-    Z[bi, ti, tok] = 64.0
-    return agree, (bi, ti, tok, saved)
-
-
-def restore_target(Z: torch.Tensor, handle) -> None:
-    bi, ti, tok, saved = handle
-    Z[bi, ti, tok] = saved
-
-
 def to_numpy_bits(t: torch.Tensor):
     """Host numpy view of a tensor as the oracle takes it: bf16 -> uint16 bits, fp32 as is,
     integers as int32/int64."""

@@ -10,11 +10,14 @@ import json
 import math
 import os
 
+import numpy as np
+
 import pytest
 import torch
 
 from draft_speculative_decoding_gb300 import binding, cycles
 from draft_speculative_decoding_gb300 import workloads as wl
+import planted
 from parity import dims_for
 
 pytestmark = pytest.mark.gpu
@@ -36,15 +39,15 @@ def test_planted_cycles_accept_lengths(lib):
     recall = json.load(open(GOLDEN))["recall_at_1"]
     x0 = data["x0"].clone()
     gen = torch.Generator(device="cuda").manual_seed(5)
-    runs = cycles.planted_cycles(dims, data, [data["h"]], data["Z"], x0, ws, recall, 60, gen)
+    runs = planted.planted_cycles(dims, data, [data["h"]], data["Z"], x0, ws, recall, 60, gen)
     torch.cuda.synchronize()
     assert binding.dfs_get_device_error(ws) == binding.DFS_OK
     accs = torch.stack([a for a, _ in runs])
     for acc, agree in runs:
-        assert torch.equal(acc.long(), cycles.leading_agreements(agree))
+        assert torch.equal(acc.long(), planted.leading_agreements(agree))
     n = accs.numel()
     mean, sd = accs.float().mean().item(), accs.float().std().item()
-    want = cycles.closed_form_accept_len(recall)
+    want = planted.closed_form_accept_len(recall)
     assert abs(mean - want) < 4 * sd / math.sqrt(n), (mean, want)
 
 
@@ -95,3 +98,50 @@ def test_fused_loop_hands_off_and_replays_from_a_graph(lib):
     torch.cuda.synchronize()
     assert torch.equal(x0g, eager_x0)
     assert binding.dfs_get_device_error(ws) == binding.DFS_OK
+
+
+@pytest.mark.parametrize("mode,T", [(binding.DFS_PATH_GREEDY, 0.0), (binding.DFS_PATH_VITERBI, 0.8),
+                                    (binding.DFS_PATH_SAMPLE, 0.8)])
+def test_fused_loop_matches_the_oracle_cycle_by_cycle(lib, orc, mode, T):
+    """The multi-cycle loop ([Blog] Fig. 1: each cycle's last emitted token is the next
+    cycle's last verified token) against the oracle run the same way: five cycles at B = 8
+    over rotating hidden states and target logits, the oracle's x0 handed off from its own
+    outputs. Every cycle's path, tokens and accept length must be identical; a request that
+    diverges on a near-tie is counted and dropped from the later cycles (its x0 differs)."""
+    from parity import compare_request, new_tally, np_inputs, oracle_head, oracle_step, report
+    spec = SPEC.with_(name="cycles_oracle", B=8, seed=73)
+    data = wl.generate(spec, "cuda")
+    hs = [data["h"], data["h"].roll(1, dims=0).contiguous()]
+    Zs = [data["Z"], wl.fresh_targets(data, 31), wl.fresh_targets(data, 32)]
+    dims = dims_for(spec)
+    ws = binding.alloc_workspace(dims)
+    npd = np_inputs(data)
+    heads = []
+    for h in hs:  # the oracle's LM head of each hidden-state set, once
+        npd_h = dict(npd, h=wl.to_numpy_bits(h))
+        heads.append((npd_h, oracle_head(orc, npd_h, spec)))
+    x0 = data["x0"].clone()
+    x0_o = npd["x0"].copy()
+    live = set(range(spec.B))
+    tally = new_tally()
+    n_cycles = 5
+    for c in range(n_cycles):
+        res, _ = cycles.fused_cycles(dims, data, [hs[c % 2]], [Zs[c % 3]], x0, ws, mode, 1,
+                                     seed0=100 + c, temperature=T, want_intermediates=True)
+        torch.cuda.synchronize()
+        assert binding.dfs_get_device_error(ws) == binding.DFS_OK
+        g = {k: v.cpu().numpy() for k, v in res.items()}
+        npd_h, head = heads[c % 2]
+        o = oracle_step(orc, npd_h, spec, head, mode, T, 100 + c, x0=x0_o,
+                        Z=wl.to_numpy_bits(Zs[c % 3]))
+        for b in sorted(live):
+            if not compare_request(g, o, b, b, spec, T, tally):
+                live.discard(b)
+        # the oracle's own hand-off: each request's last emitted token
+        x0_o = np.array([o["out_tokens"][b][o["accept_len"][b] - 1] for b in range(spec.B)],
+                        np.int32)
+        # the loop's hand-off on the device equals the oracle's for every request still live
+        got = x0.cpu().numpy()
+        assert all(got[b] == x0_o[b] for b in live), f"cycle {c}: hand-off differs"
+    report(f"{spec.name} mode={mode} T={T} ({n_cycles} cycles)", tally)
+    assert len(live) >= spec.B - 2

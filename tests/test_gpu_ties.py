@@ -1,0 +1,111 @@
+"""Exact logit ties planted in the LM head, inside the top-16 and exactly at its 16/17
+boundary, on every LM-head kernel: the lower token id must win everywhere, both in the
+order of the 16 candidates and in which of the tied tokens make the cut ("DFlash 2: Keep
+Drafting Parallel", §"The right tokens are already there": the 16 best per position; the
+tie rule is the library's, lower id first).
+
+Construction (no near-tie rule applies: the tied logits are equal in fp32 and in fp64):
+every hidden row has h[d-1] = 16; a base column w0 (bf16, w0[d-1] = 1) gives every row a
+logit h . w0 near 16 (positive); 18 columns of W, spread over the vocabulary, are w0 scaled
+by 2^e with e = 4, 4, 3, 3, 3, 2, 2, 1, 1, 1, 1, 0 x 7. A power-of-two scale is exact in
+every product and partial sum, so columns with equal e have bit-identical logits on the
+tensor cores and in the oracle, and even the smallest (e = 0) lies far above every other
+logit of the row. The top-16 is then the 11 columns with e >= 1 and the 5 lowest ids of the
+7 with e = 0."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from draft_speculative_decoding_gb300 import binding
+from draft_speculative_decoding_gb300 import workloads as wl
+from parity import close, to_cpu
+
+pytestmark = pytest.mark.gpu
+
+EXPONENTS = [4, 4, 3, 3, 3, 2, 2, 1, 1, 1, 1] + [0] * 7
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from draft_speculative_decoding_gb300 import build
+    build.build()
+    return binding.load()
+
+
+def _tie_inputs(B, L, V, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    h = torch.randn(B, L, d, generator=g)
+    h[..., d - 1] = 16.0
+    W = torch.randn(d, V, generator=g) / math.sqrt(d)
+    w0 = (torch.randn(d, generator=g) / math.sqrt(d)).to(torch.bfloat16).float()
+    w0[d - 1] = 1.0
+    hot = torch.randperm(V, generator=g)[:len(EXPONENTS)]
+    for e, v in zip(EXPONENTS, hot.tolist()):
+        W[:, v] = w0 * 2.0 ** e  # exact in bf16
+    return h.to(torch.bfloat16).contiguous(), W.to(torch.bfloat16).contiguous(), hot
+
+
+def _expected_ids(hot):
+    """The top-16 by (logit desc, id asc): groups by exponent, ids ascending in a group."""
+    ids = []
+    for e in (4, 3, 2, 1, 0):
+        ids += sorted(int(v) for v, x in zip(hot.tolist(), EXPONENTS) if x == e)
+    return ids[:16]
+
+
+CASES = [  # (B, L, V, variant): <= 128 rows; CTA pairs, row-major and vocabulary-major
+    (4, 8, 151936, "0"), (4, 8, 5000, "0"),
+    (32, 8, 151936, "5"), (32, 8, 151936, "6"), (20, 9, 5000, "5"), (20, 9, 5000, "6"),
+]
+
+
+@pytest.mark.parametrize("B,L,V,variant", CASES)
+def test_lmhead_ties_go_to_the_lower_id(lib, orc, B, L, V, variant, monkeypatch):
+    monkeypatch.setenv("DFS_LMHEAD_VARIANT", variant)
+    d = 256
+    h, W, hot = _tie_inputs(B, L, V, d, seed=B * 1000 + V)
+    want = _expected_ids(hot)
+    # the oracle (fp64, exact ties) gives the same ids, in the same order, for every row
+    rows = np.array([b * L + t for b in range(B) for t in range(1, L)])
+    o_ids, o_U, _ = orc.topk(orc.logits(wl.to_numpy_bits(h), wl.to_numpy_bits(W), rows), 16)
+    assert all(o_ids[i].tolist() == want for i in range(len(rows)))
+    dims = binding.make_dims(B, L, V, d, 8, binding.DFS_BF16, binding.DFS_BF16)
+    ws = binding.alloc_workspace(dims)
+    ids, U = binding.dfs_lmhead_topk(dims, h.cuda(), W.cuda(), ws)
+    torch.cuda.synchronize()
+    assert binding.dfs_get_device_error(ws) == binding.DFS_OK
+    ids = to_cpu(ids).reshape(-1, 16)
+    U = to_cpu(U).reshape(-1, 16)
+    for i in range(len(rows)):
+        assert ids[i].tolist() == want, f"row {i}: {ids[i].tolist()} != {want}"
+        assert np.all(close(U[i], o_U[i]))
+        # the tied logits are bit-identical on the GPU too
+        for a, b in ((0, 1), (2, 3), (3, 4), (5, 6), (7, 8), (8, 9), (9, 10), (11, 15)):
+            assert U[i, a] == U[i, b], f"row {i}: slots {a} and {b} not tied"
+
+
+@pytest.mark.parametrize("B,L,V,variant", [(4, 8, 151936, "0"), (32, 8, 151936, "5"),
+                                           (32, 8, 151936, "6")])
+def test_fused_candidates_with_ties(lib, B, L, V, variant, monkeypatch):
+    """The fused call's merge (inside the tail kernel) keeps the same tie order."""
+    monkeypatch.setenv("DFS_LMHEAD_VARIANT", variant)
+    d, r = 256, 16
+    h, W, hot = _tie_inputs(B, L, V, d, seed=7 + B)
+    want = _expected_ids(hot)
+    g = torch.Generator().manual_seed(11)
+    Wg = (torch.randn(r, d, generator=g) / math.sqrt(d)).to(torch.bfloat16).cuda()
+    A = (torch.randn(V, r, generator=g) / math.sqrt(r)).to(torch.bfloat16).cuda()
+    Bt = (torch.randn(V, r, generator=g) / math.sqrt(r)).to(torch.bfloat16).cuda()
+    x0 = torch.randint(0, V, (B,), generator=g, dtype=torch.int32).cuda()
+    Z = torch.randn(B, L, V, generator=g).to(torch.bfloat16).cuda()
+    dims = binding.make_dims(B, L, V, d, r, binding.DFS_BF16, binding.DFS_BF16)
+    ws = binding.alloc_workspace(dims)
+    res = binding.dfs_select_verify(dims, h.cuda(), W.cuda(), Wg, A, Bt, x0, Z,
+                                    binding.DFS_PATH_GREEDY, 0.0, 1, ws, want_intermediates=True)
+    torch.cuda.synchronize()
+    assert binding.dfs_get_device_error(ws) == binding.DFS_OK
+    ids = to_cpu(res["cand_ids"]).reshape(-1, 16)
+    for i in range(ids.shape[0]):
+        assert ids[i].tolist() == want, f"row {i}"

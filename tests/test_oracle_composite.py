@@ -54,3 +54,20 @@ def test_select_verify_request_subset(orc):
                             path_mode=1, temperature=1.0, seed=3, reqs=[2, 0])
     for key in ("cand_ids", "path", "out_tokens", "accept_len"):
         np.testing.assert_array_equal(sub[key], full[key][[2, 0]])
+
+
+@pytest.mark.parametrize("mode,T", [(0, 0.0), (1, 0.0), (0, 0.7), (1, 1.3), (2, 0.7)])
+def test_stagewise_oracle_step_equals_select_verify(orc, mode, T):
+    """The GPU tests compose the oracle's step from its stages on a head computed once per
+    workload (tests/parity.py: oracle_head, oracle_step); that composition must equal the
+    oracle's own whole step."""
+    from parity import oracle_head, oracle_step
+    spec = wl.TINY.with_(name="stagewise", dtype="bf16", B=5, L=6, V=900, d=128, r=16, seed=8)
+    data = wl.generate(spec, "cpu")
+    npd = {k: wl.to_numpy_bits(data[k]) for k in ("h", "W", "Wg", "A", "Bt", "x0", "Z")}
+    ref = orc.select_verify(*[npd[k] for k in ("h", "W", "Wg", "A", "Bt", "x0", "Z")],
+                            path_mode=mode, temperature=T, seed=21)
+    got = oracle_step(orc, npd, spec, oracle_head(orc, npd, spec), mode, T, 21)
+    for k in ("cand_ids", "cand_U", "topk_gap", "S", "path", "path_score", "path_margin",
+              "out_tokens", "accept_len", "acc_margin", "draw_margin"):
+        assert np.array_equal(np.asarray(got[k]), np.asarray(ref[k])), k
