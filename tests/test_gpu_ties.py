@@ -109,3 +109,43 @@ def test_fused_candidates_with_ties(lib, B, L, V, variant, monkeypatch):
     ids = to_cpu(res["cand_ids"]).reshape(-1, 16)
     for i in range(ids.shape[0]):
         assert ids[i].tolist() == want, f"row {i}"
+
+
+@pytest.mark.parametrize("variant", ["5", "6"])
+def test_lmhead_logits_increasing_with_id(lib, orc, variant, monkeypatch):
+    """Logits that grow with the token id, equal within each run of three consecutive ids
+    (every later tile beats every list: the drafted-rows kernel's per-row queues overflow on
+    each tile after its warm-up and the tile is ranked through the turned-around accumulator
+    instead). The top-16 is five whole runs and the lowest id of the sixth: exact ties inside
+    it and at its 16/17 boundary, as the oracle gives them."""
+    monkeypatch.setenv("DFS_LMHEAD_VARIANT", variant)
+    B, L, V, d = 32, 8, 65528, 128
+    g = torch.Generator().manual_seed(5)
+    h = (torch.randn(B, L, d, generator=g) * 0.01).to(torch.bfloat16)
+    h[..., d - 1] = 16.0
+    h[..., d - 2] = 16.0
+    ramp = torch.div(torch.arange(V), 3, rounding_mode="floor").double() * (12.0 / V)
+    hi = ramp.to(torch.bfloat16)
+    lo = (ramp - hi.double()).to(torch.bfloat16)
+    W = torch.zeros(d, V, dtype=torch.bfloat16)
+    W[d - 1] = hi
+    W[d - 2] = lo
+    rows = np.array([b * L + t for b in range(B) for t in range(1, L)])
+    o_ids, o_U, _ = orc.topk(orc.logits(wl.to_numpy_bits(h), wl.to_numpy_bits(W), rows), 16)
+    dims = binding.make_dims(B, L, V, d, 8, binding.DFS_BF16, binding.DFS_BF16)
+    ws = binding.alloc_workspace(dims)
+    ids, U = binding.dfs_lmhead_topk(dims, h.cuda(), W.cuda(), ws)
+    torch.cuda.synchronize()
+    assert binding.dfs_get_device_error(ws) == binding.DFS_OK
+    ids = to_cpu(ids).reshape(-1, 16)
+    U = to_cpu(U).reshape(-1, 16)
+    top = V - 1 - (V - 1) % 3  # the first id of the highest run
+    want = [top + k for k in range(V - top)]
+    base = top
+    while len(want) < 16:
+        base -= 3
+        want += [base + k for k in range(min(3, 16 - len(want)))]
+    assert all(o_ids[i].tolist() == want for i in range(len(rows)))
+    for i in range(len(rows)):
+        assert ids[i].tolist() == o_ids[i].tolist(), f"row {i}"
+        assert np.all(close(U[i], o_U[i]))
