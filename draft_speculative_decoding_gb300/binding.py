@@ -18,7 +18,7 @@ from . import build as _build
 DFS_OK, DFS_ERR_INVALID, DFS_ERR_UNSUPPORTED, DFS_ERR_WORKSPACE, DFS_ERR_CUDA, DFS_ERR_TIMEOUT = \
     0, -1, -2, -3, -4, -5
 DFS_BF16, DFS_FP32 = 0, 1
-DFS_PATH_GREEDY, DFS_PATH_VITERBI, DFS_PATH_SAMPLE = 0, 1, 2
+DFS_PATH_GREEDY, DFS_PATH_VITERBI, DFS_PATH_SAMPLE, DFS_PATH_SAMPLE_JOINT = 0, 1, 2, 3
 K = 16
 
 # Every symbol include/dfs.h declares, with its ctypes signature.
@@ -49,6 +49,8 @@ SIGNATURES = {
     "dfs_select_verify": ([_DP, _P, _P, _P, _P, _P, _P, _P, _I, ctypes.c_float, ctypes.c_uint64,
                            _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
     "dfs_quantize_rows_e4m3": ([_DP, _P, _P, _P, _P], _I),
+    "dfs_e4m3_head_bytes": ([_I, _I], ctypes.c_size_t),
+    "dfs_pack_e4m3_head": ([_I, _I, _P, _P, _P], _I),
     "dfs_lmhead_topk_e4m3": ([_DP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], _I),
     "dfs_select_verify_e4m3": ([_DP, _P, _P, _P, _P, _P, _P, _P, _P, _I, ctypes.c_float,
                                 ctypes.c_uint64, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -251,6 +253,19 @@ def dfs_quantize_rows_e4m3(dims: Dims, hidden, stream=None):
     _check("dfs_quantize_rows_e4m3", load().dfs_quantize_rows_e4m3(
         ctypes.byref(dims), _ptr(hidden), _ptr(q), _ptr(sc), _stream(stream)))
     return q, sc
+
+
+def dfs_pack_e4m3_head(Wq, stream=None):
+    """Wq [V, d] uint8 E4M3 bytes (row-major, on the device) -> the packed head the E4M3 LM
+    head reads (dfs_e4m3_head_bytes(V, d) uint8)."""
+    V, d = Wq.shape
+    n = load().dfs_e4m3_head_bytes(V, d)
+    if n == 0:
+        raise DfsError("dfs_e4m3_head_bytes", DFS_ERR_UNSUPPORTED)
+    out = torch.empty(n, dtype=torch.uint8, device=Wq.device)
+    _check("dfs_pack_e4m3_head", load().dfs_pack_e4m3_head(V, d, _ptr(Wq), _ptr(out),
+                                                           _stream(stream)))
+    return out
 
 
 def dfs_next_tokens(out_tokens, accept_len, next_last_verified=None, stream=None):

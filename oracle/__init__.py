@@ -67,7 +67,8 @@ def _load():
                 "orc_verify_proposal": ([i32, P, i32, i64, P, P, P, P, i32, f64, u64, i64, P, P,
                                          P, P], i32),
                 "orc_sample_verify_many": ([i32, P, i32, i64, P, P, i32, f64, u64, i64, i64, i32,
-                                            P, P, P], i32),
+                                            i32, P, P, P], i32),
+                "orc_path_sample_joint": ([i32, i32, P, P, f64, u64, i64, P, P, P, P, P], i32),
                 "orc_philox4x64": ([P, P, P], None),
                 "orc_redraw_uniforms": ([i32, P, i64, f64, i64, P, P, i32, P, i64, P, P], i32),
                 "orc_select_verify": ([i32, i32, P, P, P, P, P, P, P, i64, i32, i64, i64, i64,
@@ -261,6 +262,24 @@ def path_sample(S, ids, T: float, seed: int, b: int = 0):
     return path, pidx, q, float(sc[0]), float(mg[0])
 
 
+def path_sample_joint(S, ids, T: float, seed: int, b: int = 0):
+    """Joint path draw over one request's lattice S [P, K, K], ids [P, K]: (path [P],
+    pidx [P], q [P, K], score, margin)."""
+    S = _c(S, np.float64)
+    P, K, _ = S.shape
+    ids = _c(ids, np.int32)
+    path = np.empty(P, np.int32)
+    pidx = np.empty(P, np.int32)
+    q = np.empty((P, K), np.float64)
+    sc = np.zeros(1, np.float64)
+    mg = np.zeros(1, np.float64)
+    _check(_load().orc_path_sample_joint(P, K, _ptr(S), _ptr(ids), float(T),
+                                         ctypes.c_uint64(seed & (2**64 - 1)), int(b), _ptr(path),
+                                         _ptr(pidx), _ptr(q), _ptr(sc), _ptr(mg)),
+           "path_sample_joint")
+    return path, pidx, q, float(sc[0]), float(mg[0])
+
+
 def verify_proposal(Z, path, cand, q, pidx, T: float, seed: int, b: int = 0):
     """Z [L, V]; the proposal's candidates cand [P, K], distributions q [P, K] and drawn
     indices pidx [P]: (out, accept_len, acc_margin, draw_margin)."""
@@ -281,9 +300,9 @@ def verify_proposal(Z, path, cand, q, pidx, T: float, seed: int, b: int = 0):
 
 
 def sample_verify_many(Z, S, ids, T: float, seed0: int, n: int, b: int = 0,
-                       nthreads: int | None = None):
-    """Sampled traversal + its verification for seeds seed0..seed0+n-1 on a fixed lattice:
-    (paths [n, P], out [n, L], accept_len [n])."""
+                       nthreads: int | None = None, joint: bool = False):
+    """Sampled traversal (joint: the joint path draw) + its verification for seeds
+    seed0..seed0+n-1 on a fixed lattice: (paths [n, P], out [n, L], accept_len [n])."""
     Z = _c(Z)
     L, V = Z.shape
     S = _c(S, np.float64)
@@ -294,8 +313,9 @@ def sample_verify_many(Z, S, ids, T: float, seed0: int, n: int, b: int = 0,
     acc = np.empty(n, np.int32)
     _check(_load().orc_sample_verify_many(_dtype_code(Z), _ptr(Z), L, V, _ptr(S), _ptr(ids), K,
                                           float(T), ctypes.c_uint64(seed0), int(n), int(b),
-                                          nthreads or default_threads(), _ptr(paths), _ptr(out),
-                                          _ptr(acc)), "sample_verify_many")
+                                          nthreads or default_threads(), int(bool(joint)),
+                                          _ptr(paths), _ptr(out), _ptr(acc)),
+           "sample_verify_many")
     return paths, out, acc
 
 

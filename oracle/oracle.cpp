@@ -23,6 +23,9 @@
  *   orc_pair_scores .......... one-hot closed forms, linearity, A = 0 gives U
  *   orc_path_viterbi ......... brute force over all K^(L-1) paths
  *   orc_path_greedy .......... hand-worked golden lattice; A = 0 gives top-1
+ *   orc_path_sample_joint .... brute force over all K^P paths: the product of the drawn
+ *                              conditionals is the path's exact probability; chi-square of
+ *                              drawn paths; T -> 0 gives the Viterbi path
  *   orc_verify_greedy ........ equality with target-argmax decoding
  *   orc_verify_sampling ...... chi-square of emitted-token marginals against
  *                              the target softmax (1e6 draws; and redraws over a
@@ -610,6 +613,62 @@ int orc_path_sample(int P, int K, const double* S, const int32_t* ids, double T,
   return 0;
 }
 
+/* Joint path draw, [Blog] §"A lightweight path selector" (sampling draws from the same
+ * scores), read as a draw of the whole path from the distribution the scores define over the
+ * lattice: P(x_1..x_P) proportional to exp(sum_t S_t(x_{t-1}, x_t) / T), x_0 the last
+ * verified token. Its conditionals come from backward messages
+ *   log beta_P(c) = 0,  log beta_t(a) = log sum_c exp(S_{t+1}(a, c) / T + log beta_{t+1}(c)),
+ * q_t(c | x_{t-1}) = exp(S_t(x_{t-1}, c) / T + log beta_t(c)) / (the same summed over c),
+ * and x_t is drawn left to right from them, one uniform per position (counter (0, t, b, 3),
+ * word 0) against the cumulative q in candidate order (if rounding leaves no candidate above
+ * it, the last one with mass). Outputs as orc_path_sample: the path, its candidate indices,
+ * q [P][K] (each position's conditional given the drawn predecessor), the summed scores and
+ * the smallest distance of a uniform to a cumulative boundary. T > 0. */
+int orc_path_sample_joint(int P, int K, const double* S, const int32_t* ids, double T,
+                          uint64_t seed, int64_t b, int32_t* path, int32_t* pidx, double* q,
+                          double* score, double* margin) {
+  if (P < 1 || K < 1 || !(T > 0.0)) return -1;
+  std::vector<double> lb(static_cast<size_t>(P) * K, 0.0);  // log beta_t, position t = p + 1
+  for (int p = P - 2; p >= 0; --p) {
+    for (int a = 0; a < K; ++a) {
+      const double* row = S + (static_cast<int64_t>(p + 1) * K + a) * K;
+      double m = -kInf;
+      for (int c = 0; c < K; ++c) m = std::max(m, row[c] / T + lb[(p + 1) * K + c]);
+      double z = 0.0;
+      for (int c = 0; c < K; ++c) z += std::exp(row[c] / T + lb[(p + 1) * K + c] - m);
+      lb[p * K + a] = m + std::log(z);
+    }
+  }
+  int a = 0;
+  double total = 0.0, mg = kInf;
+  for (int p = 0; p < P; ++p) {
+    const double* row = S + (static_cast<int64_t>(p) * K + a) * K;
+    double m = -kInf;
+    for (int c = 0; c < K; ++c) m = std::max(m, row[c] / T + lb[p * K + c]);
+    double z = 0.0;
+    for (int c = 0; c < K; ++c) z += std::exp(row[c] / T + lb[p * K + c] - m);
+    double* qp = q + static_cast<int64_t>(p) * K;
+    for (int c = 0; c < K; ++c) qp[c] = std::exp(row[c] / T + lb[p * K + c] - m) / z;
+    const double u = uniform_path(seed, b, p + 1);
+    int pick = -1, last = 0;
+    double cum = 0.0;
+    for (int c = 0; c < K; ++c) {
+      cum += qp[c];
+      if (qp[c] > 0.0) last = c;
+      if (c + 1 < K) mg = std::min(mg, std::fabs(cum - u));
+      if (pick < 0 && cum > u) pick = c;
+    }
+    if (pick < 0) pick = last;
+    path[p] = ids[static_cast<int64_t>(p) * K + pick];
+    pidx[p] = pick;
+    total += row[pick];
+    a = pick;
+  }
+  *score = total;
+  *margin = mg;
+  return 0;
+}
+
 /* Speculative-sampling verification of a sampled proposal, [Blog] §"A lightweight path
  * selector" (rejection sampling recovers the exact target distribution): for t = 1..L-1,
  * with p = softmax(Z[t-1]/T) and q = q_t (K candidates cand[t-1][*], the drawn one at index
@@ -654,12 +713,12 @@ int orc_verify_proposal(int zdtype, const void* Z, int L, int64_t V, const int32
   return 0;
 }
 
-/* The sampled traversal and its verification run once per seed in [seed0, seed0 + n) on
- * a fixed lattice (S [P][K][K], ids [P][K]) and target rows Z [L][V], for the distribution
- * tests: paths [n][P], out [n][L], accept_len [n]. */
+/* The sampled traversal (joint != 0: the joint path draw) and its verification run once per
+ * seed in [seed0, seed0 + n) on a fixed lattice (S [P][K][K], ids [P][K]) and target rows
+ * Z [L][V], for the distribution tests: paths [n][P], out [n][L], accept_len [n]. */
 int orc_sample_verify_many(int zdtype, const void* Z, int L, int64_t V, const double* S,
                            const int32_t* ids, int K, double T, uint64_t seed0, int64_t n,
-                           int64_t b, int nthreads, int32_t* paths, int32_t* out,
+                           int64_t b, int nthreads, int joint, int32_t* paths, int32_t* out,
                            int32_t* accept_len) {
   if (L < 2 || V < 2 || K < 1 || !(T > 0.0) || n < 0) return -1;
   const int P = L - 1;
@@ -671,8 +730,10 @@ int orc_sample_verify_many(int zdtype, const void* Z, int L, int64_t V, const do
     std::vector<double> q(static_cast<size_t>(P) * K);
     double score, pm, am, gm;
     const uint64_t seed = seed0 + static_cast<uint64_t>(i);
-    int rc = orc_path_sample(P, K, S, ids, T, seed, b, paths + i * P, pidx.data(), q.data(),
-                             &score, &pm);
+    int rc = joint ? orc_path_sample_joint(P, K, S, ids, T, seed, b, paths + i * P, pidx.data(),
+                                           q.data(), &score, &pm)
+                   : orc_path_sample(P, K, S, ids, T, seed, b, paths + i * P, pidx.data(),
+                                     q.data(), &score, &pm);
     if (rc == 0)
       rc = orc_verify_proposal(zdtype, Z, L, V, paths + i * P, ids, q.data(), pidx.data(), K, T,
                                seed, b, out + i * L, accept_len + i, &am, &gm);
@@ -705,9 +766,9 @@ void orc_philox4x64(const uint64_t* ctr, const uint64_t* key, uint64_t* out) {
  * scores -> path -> verify. Inputs: h [B][L][d], W [d][V], Wg [r][d],
  * A and Bt [V][r], x0 [B], Z [B][L][V]. Outputs are indexed by list position
  * q = 0..nreq-1. Wq / w_scale non-null: the LM head is E4M3 (orc_logits_e4m3) instead of W.
- * path_mode 0 = greedy traversal, 1 = Viterbi, 2 = sampled traversal
- * (verified against its own proposal); T <= 0 selects greedy verification (and, for
- * path_mode 2, the greedy traversal). */
+ * path_mode 0 = greedy traversal, 1 = Viterbi, 2 = sampled traversal, 3 = joint path draw
+ * (2 and 3 verified against their own proposal); T <= 0 selects greedy verification (and,
+ * for path_mode 2, the greedy traversal; for path_mode 3, Viterbi, the draw's T -> 0 limit). */
 int orc_select_verify(int dtype, int zdtype, const void* h, const void* W, const void* Wg,
                       const void* A, const void* Bt, const int32_t* x0, const void* Z,
                       int64_t B, int L, int64_t V, int64_t d, int64_t r, int K, int path_mode,
@@ -742,13 +803,16 @@ int orc_select_verify(int dtype, int zdtype, const void* h, const void* W, const
     if (rc == 0) rc = orc_topk(u.data(), P, V, K, ids, U, topk_gap + q * P);
     if (rc == 0) rc = orc_gate(dtype, h, Wg, d, r, rows.data(), P, g);
     if (rc == 0) rc = orc_pair_scores(dtype, A, Bt, r, P, K, ids, U, g, x0[b], Sq);
-    const bool sampled = path_mode == 2 && T > 0.0;
+    const bool sampled = (path_mode == 2 || path_mode == 3) && T > 0.0;
     std::vector<double> qprop(static_cast<size_t>(P) * K);
     if (rc == 0) {
-      if (sampled)
+      if (sampled && path_mode == 3)
+        rc = orc_path_sample_joint(P, K, Sq, ids, T, seed, b, path + q * P, pidx.data(),
+                                   qprop.data(), path_score + q, path_margin + q);
+      else if (sampled)
         rc = orc_path_sample(P, K, Sq, ids, T, seed, b, path + q * P, pidx.data(), qprop.data(),
                              path_score + q, path_margin + q);
-      else if (path_mode == 1)
+      else if (path_mode == 1 || path_mode == 3)
         rc = orc_path_viterbi(P, K, Sq, ids, path + q * P, pidx.data(), path_score + q, path_margin + q);
       else
         rc = orc_path_greedy(P, K, Sq, ids, path + q * P, pidx.data(), path_score + q, path_margin + q);

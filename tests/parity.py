@@ -185,16 +185,18 @@ def oracle_step(orc, npd, spec, head, mode, T, seed, x0=None, Z=None) -> dict:
               "path_score": np.empty(B), "path_margin": np.empty(B),
               "out_tokens": np.empty((B, spec.L), np.int32), "accept_len": np.empty(B, np.int32),
               "acc_margin": np.full(B, np.inf), "draw_margin": np.full(B, np.inf)})
-    sampled = mode == binding.DFS_PATH_SAMPLE and T > 0
+    sampled = mode in (binding.DFS_PATH_SAMPLE, binding.DFS_PATH_SAMPLE_JOINT) and T > 0
     for b in range(B):
         ids = head["cand_ids"][b]
         S = orc.pair_scores(npd["A"], npd["Bt"], ids, head["cand_U"][b], head["gate"][b], int(x0[b]))
         o["S"][b] = S
         if sampled:
-            path, pidx, q, score, margin = orc.path_sample(S, ids, T, seed, b)
+            draw = orc.path_sample_joint if mode == binding.DFS_PATH_SAMPLE_JOINT else orc.path_sample
+            path, pidx, q, score, margin = draw(S, ids, T, seed, b)
             out, acc, am, dm = orc.verify_proposal(Z[b], path, ids, q, pidx, T, seed, b)
         else:
-            fn = orc.path_viterbi if mode == binding.DFS_PATH_VITERBI else orc.path_greedy
+            viterbi = mode in (binding.DFS_PATH_VITERBI, binding.DFS_PATH_SAMPLE_JOINT)
+            fn = orc.path_viterbi if viterbi else orc.path_greedy
             path, _, score, margin = fn(S, ids)
             if T > 0:
                 out, acc, am, dm = orc.verify_sampling(Z[b], path, T, seed, b)

@@ -56,7 +56,8 @@ def test_select_verify_request_subset(orc):
         np.testing.assert_array_equal(sub[key], full[key][[2, 0]])
 
 
-@pytest.mark.parametrize("mode,T", [(0, 0.0), (1, 0.0), (0, 0.7), (1, 1.3), (2, 0.7)])
+@pytest.mark.parametrize("mode,T", [(0, 0.0), (1, 0.0), (0, 0.7), (1, 1.3), (2, 0.7), (3, 0.7),
+                                    (3, 0.0)])
 def test_stagewise_oracle_step_equals_select_verify(orc, mode, T):
     """The GPU tests compose the oracle's step from its stages on a head computed once per
     workload (tests/parity.py: oracle_head, oracle_step); that composition must equal the
