@@ -278,6 +278,7 @@ def run_ours(args):
     # the same step with the LM head given quantised to E4M3 (one power-of-two scale per
     # vocabulary entry; rows quantised per call): half the LM-head bytes
     Wq, w_scale = wl.quantize_lmhead_e4m3(data["W"])
+    Wq = binding.dfs_pack_e4m3_head(Wq)  # the head packed once, as a loader would
 
     def step_q(i):
         binding.dfs_select_verify_e4m3(dims, hs[i % nrot], Wq, w_scale, data["Wg"], data["A"],

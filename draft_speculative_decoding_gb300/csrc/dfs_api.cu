@@ -116,6 +116,11 @@ T* at(void* ws, size_t off) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
 int check_ptrs(std::initializer_list<const void*> req, std::initializer_list<const void*> opt) {
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return DFS_ERR_INVALID;
@@ -451,7 +456,7 @@ int dfs_select_verify(const dfs_dims* dims, const void* hidden, const void* W_vo
   int rc = prepare(dims, ws, ws_bytes, &L);
   if (rc != DFS_OK) return rc;
   if (path_mode != DFS_PATH_GREEDY && path_mode != DFS_PATH_VITERBI &&
-      path_mode != DFS_PATH_SAMPLE)
+      path_mode != DFS_PATH_SAMPLE && path_mode != DFS_PATH_SAMPLE_JOINT)
     return DFS_ERR_INVALID;
   if (!(temperature >= 0.f) || temperature != temperature) return DFS_ERR_INVALID;
   if ((rc = check_ptrs({hidden, W_vocab, W_g, A, Btab, last_verified, target_logits, path,
@@ -499,8 +504,8 @@ int dfs_quantize_rows_e4m3(const dfs_dims* dims, const void* hidden, void* q, fl
 namespace {
 
 // Shape and pointer checks of the E4M3 LM head: bf16 hidden states (quantised per row by
-// the call), d a multiple of 128 (one stage is 128 bytes of k), Wq [V, d] E4M3 and w_scale
-// [V] fp32, 16-byte aligned.
+// the call), d a multiple of 128 (one stage is 128 bytes of k), Wq the packed E4M3 head
+// (dfs_pack_e4m3_head) and w_scale [V] fp32, 16-byte aligned.
 int check_e4m3(const dfs_dims* dims, const void* Wq, const float* w_scale) {
   if (dims->dtype != DFS_BF16 || dims->d % 128 != 0) return DFS_ERR_UNSUPPORTED;
   return check_ptrs({Wq, w_scale}, {});
@@ -559,6 +564,21 @@ cudaError_t run_lmhead_e4m3(const dfs_dims& d, const Layout& L, void* ws, const 
 
 extern "C" {
 
+size_t dfs_e4m3_head_bytes(int V, int d) {
+  if (V < 1 || d < 128 || d % 128 != 0) return 0;
+  return dfs::e4m3_head_bytes(V, d);
+}
+
+int dfs_pack_e4m3_head(int V, int d, const void* Wq, void* Wq_packed, void* stream) {
+  if (V < 1 || d < 128) return DFS_ERR_INVALID;
+  if (d % 128 != 0 || V > dfs::kMaxZChunks * dfs::kZChunk) return DFS_ERR_UNSUPPORTED;
+  const int rc = check_ptrs({Wq, Wq_packed}, {});
+  if (rc != DFS_OK) return rc;
+  if (overlaps(Wq, static_cast<size_t>(V) * d, Wq_packed, dfs::e4m3_head_bytes(V, d)))
+    return DFS_ERR_INVALID;
+  return cuda_rc(dfs::launch_pack_e4m3_head(Wq, V, d, Wq_packed, static_cast<cudaStream_t>(stream)));
+}
+
 int dfs_lmhead_topk_e4m3(const dfs_dims* dims, const void* hidden, const void* Wq,
                          const float* w_scale, int32_t* cand_ids, float* cand_U, void* ws,
                          size_t ws_bytes, void* stream) {
@@ -590,7 +610,7 @@ int dfs_select_verify_e4m3(const dfs_dims* dims, const void* hidden, const void*
   if (rc != DFS_OK) return rc;
   if ((rc = check_e4m3(dims, Wq, w_scale)) != DFS_OK) return rc;
   if (path_mode != DFS_PATH_GREEDY && path_mode != DFS_PATH_VITERBI &&
-      path_mode != DFS_PATH_SAMPLE)
+      path_mode != DFS_PATH_SAMPLE && path_mode != DFS_PATH_SAMPLE_JOINT)
     return DFS_ERR_INVALID;
   if (!(temperature >= 0.f) || temperature != temperature) return DFS_ERR_INVALID;
   if ((rc = check_ptrs({hidden, W_g, A, Btab, last_verified, target_logits, path, out_tokens,
@@ -636,10 +656,6 @@ int check_conv(int B, int L, int d) {
 // The error word, then the correction GEMM's per-split partial sums.
 size_t conv_ws_bytes(int B, int L, int d) { return kAlign + align_up(dfs::conv2tap_partial_bytes(B, L, d)); }
 
-bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
-  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-  return x < y + nb && y < x + na;
-}
 
 }  // namespace
 

@@ -43,7 +43,7 @@ struct LmheadLaunch {
   // head given as E4M3 bytes [V, d] with one fp32 scale per vocabulary entry
   const void* hq;        // [rows_total, d] E4M3
   const float* h_scale;  // [rows_total]
-  const void* Wq;        // [V, d] E4M3
+  const void* Wq;        // E4M3 head, packed: [ceil(V/128)][d/128][128][128] bytes
   const float* w_scale;  // [V]
   // Target-logit row statistics computed by the kernel's spare warps (z_rows = 0: none).
   const void* Z;       // [z_rows, V]
@@ -93,6 +93,11 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s);
 // statistics; launched as a programmatic dependent of launch_quantize_rows_e4m3. Partial
 // lists: one per CTA pair (G / 2 per row).
 cudaError_t launch_lmhead_e4m3(const LmheadLaunch& a, cudaStream_t s);
+// Bytes of the packed E4M3 head, and the packing of a row-major Wq [V, d] into it (each 128
+// vocabulary rows x 128 k bytes one contiguous tile; tiles ordered by vocabulary block, then
+// k block; rows past V zero).
+size_t e4m3_head_bytes(int V, int d);
+cudaError_t launch_pack_e4m3_head(const void* Wq, int V, int d, void* out, cudaStream_t s);
 // Rows of h [rows, d] bf16 quantised to E4M3 with per-row power-of-two scales.
 cudaError_t launch_quantize_rows_e4m3(const void* h, int rows, int d, void* q, float* scale,
                                       cudaStream_t s);

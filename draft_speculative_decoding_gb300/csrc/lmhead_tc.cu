@@ -500,7 +500,9 @@ struct PairCfg {
   static_assert(kAccCols * kNBuf <= kTmemCols, "TMEM");
 };
 
-// kE4M3: the operands are E4M3 (the quantised rows and the quantised head Wq [V, d], both
+// kE4M3: the operands are E4M3 (the quantised rows and the quantised head, tiled as
+// dfs_pack_e4m3_head lays it out: each 128 vocabulary rows x 128 k bytes one contiguous
+// 16 KB tile, both
 // K-major 128-byte rows, 128 k per stage, kind::f8f6f4 with K = 32 per instruction), and
 // the epilogue scales column v by w_scale[v] and the row by h_scale (no gate tiles).
 template <int S, bool kE4M3>
@@ -582,7 +584,8 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
           const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
           const uint32_t sw = smem_u32(ring + size_t(stage) * Cfg::kStage);
           if (q8) {  // 128 vocabulary rows x 128 k bytes (K-major), and the quantised rows
-            tma_load_2d_pair(sw, &p.tm_w, fb, kb * 128, n0, pol_stream);
+            // tile (n0 / 128, kb) of the packed head: 16 KB contiguous in memory
+            tma_load_2d_pair(sw, &p.tm_w, fb, 0, ((n0 >> 7) * KB + kb) * 128, pol_stream);
             tma_load_2d_pair(sw + Cfg::kHalfBytes, &p.tm_hq, fb, kb * 128,
                              p.row0 + static_cast<int>(rank) * 128, pol_keep);
           } else {
@@ -1310,6 +1313,27 @@ __global__ void __launch_bounds__(256) k_quantize_rows_e4m3(const uint16_t* __re
   }
 }
 
+// ------------------------------------------------------------------ head packing
+// One block per 128 x 128-byte tile (vb, kb) of the E4M3 head: rows 128 vb .. of Wq [V, d]
+// (row-major bytes), k bytes 128 kb .., written as one contiguous 16 KB tile, row after row;
+// rows past V are zeros.
+__global__ void __launch_bounds__(256) k_pack_e4m3_head(const uint8_t* __restrict__ Wq, int V,
+                                                         int d, uint8_t* __restrict__ out) {
+  const int KB = d / 128;
+  const int vb = blockIdx.x / KB, kb = blockIdx.x - vb * KB;
+  uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(blockIdx.x) * 16384);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = threadIdx.x + 256 * i;  // 16-byte piece: row e / 8, bytes 16 (e % 8) ..
+    const int row = vb * 128 + (e >> 3);
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (row < V)
+      x = __ldg(reinterpret_cast<const uint4*>(Wq + static_cast<size_t>(row) * d + kb * 128) +
+                (e & 7));
+    dst[e] = x;
+  }
+}
+
 // ------------------------------------------------------------------ host side
 namespace {
 
@@ -1569,6 +1593,19 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
   return cudaSuccess;
 }
 
+size_t e4m3_head_bytes(int V, int d) {
+  return static_cast<size_t>((V + 127) / 128) * 128 * static_cast<size_t>(d);
+}
+
+cudaError_t launch_pack_e4m3_head(const void* Wq, int V, int d, void* out, cudaStream_t s) {
+  const int tiles = ((V + 127) / 128) * (d / 128);
+  k_pack_e4m3_head<<<tiles, 256, 0, s>>>(static_cast<const uint8_t*>(Wq), V, d,
+                                          static_cast<uint8_t*>(out));
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launches(1);
+  return e;
+}
+
 cudaError_t launch_quantize_rows_e4m3(const void* h, int rows, int d, void* q, float* scale,
                                       cudaStream_t s) {
   k_quantize_rows_e4m3<<<rows, 256, 0, s>>>(static_cast<const uint16_t*>(h), d,
@@ -1582,7 +1619,10 @@ cudaError_t launch_lmhead_e4m3(const LmheadLaunch& a, cudaStream_t s) {
   LmheadParams prm;
   memset(&prm, 0, sizeof(prm));
   if (!encode_u8_2d(&prm.tm_hq, a.hq, a.d, a.rows_total, 128, 128)) return cudaErrorInvalidValue;
-  if (!encode_u8_2d(&prm.tm_w, a.Wq, a.d, a.V, 128, 128)) return cudaErrorInvalidValue;
+  // the packed head as rows of 128 bytes: tile (vb, kb) is rows (vb * d / 128 + kb) * 128 ..
+  if (!encode_u8_2d(&prm.tm_w, a.Wq, 128, static_cast<uint64_t>(e4m3_head_bytes(a.V, a.d) / 128),
+                    128, 128))
+    return cudaErrorInvalidValue;
   // gate tiles stay bf16: the bf16 rows and W_g (128 W_g rows per CTA of a pair)
   if (!encode_bf16_2d(&prm.tm_h, a.hidden, a.d, a.rows_total, 64, 128)) return cudaErrorInvalidValue;
   prm.h_box_bytes = 128u * 128u;

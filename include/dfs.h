@@ -65,9 +65,15 @@ typedef enum {
  * CUDA cores (exact fp32 products, for small checkable cases). */
 typedef enum { DFS_BF16 = 0, DFS_FP32 = 1 } dfs_dtype;
 
-/* DFS_PATH_SAMPLE ("A lightweight path selector": sampling draws from the same scores)
- * is the fused call's sampled traversal; see dfs_select_verify. */
-typedef enum { DFS_PATH_GREEDY = 0, DFS_PATH_VITERBI = 1, DFS_PATH_SAMPLE = 2 } dfs_path_mode;
+/* DFS_PATH_SAMPLE and DFS_PATH_SAMPLE_JOINT ("A lightweight path selector": sampling
+ * draws from the same scores) are the fused call's sampled traversal and joint path draw;
+ * see dfs_select_verify. */
+typedef enum {
+  DFS_PATH_GREEDY = 0,
+  DFS_PATH_VITERBI = 1,
+  DFS_PATH_SAMPLE = 2,
+  DFS_PATH_SAMPLE_JOINT = 3
+} dfs_path_mode;
 
 typedef struct {
   int B;      /* requests in the batch, >= 1                                 */
@@ -202,7 +208,14 @@ int dfs_verify_noalloc(const dfs_dims* dims, const int32_t* path, const void* ta
  *   max(0, p_{t-1} - q_t) renormalised (dfs_verify's draw with these weights); when all are
  *   accepted a bonus draw from p_{L-1}.
  *   path_score_opt is then the summed scores of the drawn path. With temperature 0 the
- *   mode is DFS_PATH_GREEDY. (dfs_path_select does not take it: it has no seed.) */
+ *   mode is DFS_PATH_GREEDY. (dfs_path_select does not take it: it has no seed.)
+ * path_mode DFS_PATH_SAMPLE_JOINT with temperature > 0: the whole path is drawn from
+ *   P(x_1..x_{L-1}) proportional to exp(sum_t S_t(x_{t-1}, x_t) / T), left to right from
+ *   its conditionals q_t(c | x_{t-1}) proportional to exp(S_t(x_{t-1}, c) / T + log beta_t(c)),
+ *   with log beta_{L-1} = 0 and log beta_t(a) = log sum_c exp(S_{t+1}(a, c) / T +
+ *   log beta_{t+1}(c)) (same counters and draw as DFS_PATH_SAMPLE), and verified by
+ *   speculative sampling against those conditionals, as above. With temperature 0 the mode
+ *   is DFS_PATH_VITERBI (the draw's T -> 0 limit). */
 int dfs_select_verify(const dfs_dims* dims, const void* hidden, const void* W_vocab,
                       const void* W_g, const void* A, const void* Btab,
                       const int32_t* last_verified, const void* target_logits, int path_mode,
@@ -218,10 +231,21 @@ int dfs_select_verify(const dfs_dims* dims, const void* hidden, const void* W_vo
  * a power-of-two scale (exact to apply), so the product runs on the 8-bit tensor cores:
  *   u_t[v] = s_h[t] * w_scale[v] * sum_k E4M3(hq[t][k]) * E4M3(Wq[v][k])
  * Everything after the LM head (gate, pair scores, path, verification) is the bf16 step's.
- *   Wq      [V, d] E4M3 bytes (vocabulary-major: each entry's d weights contiguous)
+ *   Wq      the head as E4M3 bytes, packed by dfs_pack_e4m3_head (dfs_e4m3_head_bytes)
  *   w_scale [V] fp32
  *   dims: dtype DFS_BF16 (hidden states, W_g, A, B), d a multiple of 128; Wq and w_scale
  *   16-byte aligned, else DFS_ERR_UNSUPPORTED / DFS_ERR_INVALID. */
+
+/* The packed form of an E4M3 head: Wq [V, d] (row-major bytes, each vocabulary entry's d
+ * weights contiguous, as a quantised checkpoint stores it) cut into tiles of 128 vocabulary
+ * rows x 128 k bytes, each tile 16 KB contiguous (its 128 rows one after another), tiles
+ * ordered by vocabulary block, then k block; rows past V are zeros. The LM head then reads
+ * every stage of the head as one contiguous 16 KB block.
+ * dfs_e4m3_head_bytes: the packed size, ceil(V / 128) * 128 * d (0 for d not a positive
+ * multiple of 128). dfs_pack_e4m3_head: one kernel on `stream` from Wq (device, 16-byte
+ * aligned) into Wq_packed (device, that many bytes, not overlapping Wq). Do it once per head. */
+size_t dfs_e4m3_head_bytes(int V, int d);
+int dfs_pack_e4m3_head(int V, int d, const void* Wq, void* Wq_packed, void* stream);
 
 /* The row quantisation alone: hidden [B, L, d] bf16 -> q [B*L, d] E4M3 bytes and
  * scale [B*L] fp32, per row the smallest power of two 2^e with max|h| <= 448 * 2^e (448 is

@@ -63,7 +63,8 @@ def test_lmhead_topk_e4m3(lib, orc, spec):
     npd = np_inputs(data)
     dims = dims_for(spec)
     ws = binding.alloc_workspace(dims)
-    ids, U = binding.dfs_lmhead_topk_e4m3(dims, data["h"], data["Wq"], data["w_scale"], ws)
+    Wp = binding.dfs_pack_e4m3_head(data["Wq"])
+    ids, U = binding.dfs_lmhead_topk_e4m3(dims, data["h"], Wp, data["w_scale"], ws)
     torch.cuda.synchronize()
     assert binding.dfs_get_device_error(ws) == binding.DFS_OK
     o_ids, o_U, o_gap = _oracle_topk(orc, npd, data, spec)
@@ -74,7 +75,8 @@ def test_lmhead_topk_e4m3(lib, orc, spec):
 def _run_e4m3(data, spec, mode, T, seed):
     dims = dims_for(spec)
     ws = binding.alloc_workspace(dims)
-    res = binding.dfs_select_verify_e4m3(dims, data["h"], data["Wq"], data["w_scale"], data["Wg"],
+    Wp = binding.dfs_pack_e4m3_head(data["Wq"])
+    res = binding.dfs_select_verify_e4m3(dims, data["h"], Wp, data["w_scale"], data["Wg"],
                                          data["A"], data["Bt"], data["x0"], data["Z"], mode, T,
                                          seed, ws, want_intermediates=True)
     torch.cuda.synchronize()
@@ -112,3 +114,19 @@ def test_fused_e4m3_full_size(lib, orc):
         excluded = _compare(g, o, spec, range(spec.B), T,
                             name=f"{spec.name} e4m3 mode={mode} T={T}")
         assert excluded <= max(1, spec.B // 4)
+
+
+@pytest.mark.parametrize("V,d", [(1000, 256), (4096, 128), (151936, 640)])
+def test_pack_e4m3_head_layout(lib, V, d):
+    """The packed head: tile (vb, kb) holds rows 128 vb .. 128 vb + 127 of Wq (zeros past V),
+    bytes 128 kb .. 128 kb + 127 of each, as 16 KB contiguous; tiles by vb, then kb."""
+    g = torch.Generator(device="cuda").manual_seed(V + d)
+    Wq = torch.randint(0, 256, (V, d), generator=g, device="cuda", dtype=torch.uint8)
+    got = binding.dfs_pack_e4m3_head(Wq)
+    torch.cuda.synchronize()
+    nvb, nkb = -(-V // 128), d // 128
+    assert got.numel() == nvb * 128 * d
+    pad = torch.zeros(nvb * 128, d, dtype=torch.uint8, device="cuda")
+    pad[:V] = Wq
+    want = pad.view(nvb, 128, nkb, 128).permute(0, 2, 1, 3).reshape(-1)
+    assert torch.equal(got, want)
