@@ -787,14 +787,6 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
 // At the end the odd CTA's lists (its 128 vocabulary entries per tile) are read by the
 // leader through distributed shared memory and merged by (value desc, id asc) into one
 // partial list per row and pair, the layout the tail reads.
-// After its first kVtWarmTiles vocabulary tiles a CTA of k_lmhead_vt no longer turns every
-// row around: each row's list has an entry threshold by then (its 16th value), and only
-// entries above it are queued in the round buffer, per row and epilogue warp (at most
-// kVtCap each). A later tile's entries have larger ids than every listed member, so an entry
-// equal to the threshold never enters, and the strict test misses nothing.
-constexpr int kVtWarmTiles = 3;
-constexpr int kVtCap = 7;
-
 template <int S>
 struct VtCfg {
   static constexpr int kABytes = 128 * 128;  // 128 vocabulary entries (or W_g rows) x 64 k
@@ -818,7 +810,6 @@ struct VtCfg {
   static constexpr size_t kSmemMax = smem(kMaxStage);
   static_assert(kSmemMax <= 232448, "shared memory");
   static_assert(kXBytes >= 2 * 128 * 2 * kK * 4, "the peer's lists fit the round buffer");
-  static_assert(kXBytes >= 2048 + 256 * 4 * kVtCap * 8, "thresholds, counts and queues fit it");
   static_assert(kXBytes % 16 == 0, "the barriers follow 16-byte aligned");
 };
 
@@ -838,25 +829,15 @@ __device__ __forceinline__ void top16_insert_ranked(Top16& t, float x, int id) {
   t.i[0] = ge[0] ? t.i[0] : id;
 }
 
-// The round buffer of k_lmhead_vt while it filters: thr [256] fp32 (entry threshold per
-// drafted row; +inf past N), cnt [4][256] uint8 (entries queued by each epilogue warp this
-// tile), cand [256][4][kVtCap] (value, id) pairs.
-__device__ __forceinline__ float* vt_thr(float* xbuf) { return xbuf; }
-__device__ __forceinline__ uint8_t* vt_cnt(float* xbuf) {
-  return reinterpret_cast<uint8_t*>(xbuf + 256);
-}
-__device__ __forceinline__ float2* vt_cand(float* xbuf) {
-  return reinterpret_cast<float2*>(xbuf + 512);
-}
-
 // The tile's accumulator turned around through the round buffer, four 32-row chunks per
 // round: all four epilogue warps store their lane quarter of the round's chunks as
 // [row][vocabulary] rows, then warp q ranks chunk q, one row per thread, 128 consecutive
-// entries in increasing id order. Rows with want0 / want1 false are not offered.
+// entries in increasing id order. (Measured: a per-row threshold filter with queued
+// candidates instead of this, after three such tiles, ran slower per tile on these warps.)
 template <class Cfg>
 __device__ __forceinline__ void vt_rank_turned(float* xbuf, uint32_t tbase, int nchunk, int q,
                                                int lane, int vbase, int V, Top16& top0,
-                                               Top16& top1, bool want0, bool want1) {
+                                               Top16& top1) {
 #pragma unroll
   for (int rd = 0; rd < 2; ++rd) {
     if (4 * rd < nchunk) {
@@ -873,7 +854,7 @@ __device__ __forceinline__ void vt_rank_turned(float* xbuf, uint32_t tbase, int 
         }
       }
       named_bar_sync(2, 128);
-      if (4 * rd + q < nchunk && (rd == 0 ? want0 : want1)) {  // row 32 (4 rd + q) + lane
+      if (4 * rd + q < nchunk) {  // row 32 (4 rd + q) + lane
         Top16& top = rd == 0 ? top0 : top1;
         const float* xrow = xbuf + (q * 32 + lane) * Cfg::kXStride;
 #pragma unroll 1
@@ -888,76 +869,6 @@ __device__ __forceinline__ void vt_rank_turned(float* xbuf, uint32_t tbase, int 
       named_bar_sync(2, 128);  // the round's reads are done before the next stores
     }
   }
-}
-
-// Each thread holds vocabulary entry v of the tile (its TMEM lane) for every drafted row:
-// the entries above their row's threshold are queued on that row in this warp's queue, at
-// the entry's rank among the warp's lanes (one ballot per row of a chunk; no atomics). A
-// count past kVtCap is recorded as is, and the row is redone by vt_rank_turned.
-__device__ __forceinline__ void vt_filter_push(float* xbuf, uint32_t tbase, int nchunk, int q,
-                                               int lane, int v, int V) {
-  const float* thr = vt_thr(xbuf);
-  uint8_t* cnt = vt_cnt(xbuf) + q * 256;
-  float2* cand = vt_cand(xbuf);
-  const uint32_t below = (1u << lane) - 1u;
-#pragma unroll 1
-  for (int c = 0; c < nchunk; ++c) {
-    uint32_t rr[32];
-    tmem_ld_32x32b_x32(tbase + c * 32, rr);
-    tmem_ld_wait();
-    uint32_t mask = 0;
-    const float4* t4 = reinterpret_cast<const float4*>(thr + c * 32);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float4 t = t4[u];
-      mask |= (__uint_as_float(rr[4 * u]) > t.x ? 1u : 0u) << (4 * u);
-      mask |= (__uint_as_float(rr[4 * u + 1]) > t.y ? 1u : 0u) << (4 * u + 1);
-      mask |= (__uint_as_float(rr[4 * u + 2]) > t.z ? 1u : 0u) << (4 * u + 2);
-      mask |= (__uint_as_float(rr[4 * u + 3]) > t.w ? 1u : 0u) << (4 * u + 3);
-    }
-    if (v >= V) mask = 0;  // past the vocabulary: not a token
-    uint32_t mine = 0;     // queued on row 32 c + lane by this warp
-    if (__reduce_or_sync(0xffffffffu, mask) != 0u) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const uint32_t bj = __ballot_sync(0xffffffffu, (mask >> j) & 1u);
-        if (lane == j) mine = __popc(bj);
-        if ((mask >> j) & 1u) {
-          const int pos = __popc(bj & below);
-          if (pos < kVtCap)
-            cand[((c * 32 + j) * 4 + q) * kVtCap + pos] =
-                make_float2(__uint_as_float(rr[j]), __int_as_float(v));
-        }
-      }
-    }
-    cnt[c * 32 + lane] = static_cast<uint8_t>(mine < 255u ? mine : 255u);
-  }
-}
-
-// Row col's queued entries (all four warps') into its list (value desc, id asc, in any order
-// of arrival); false when a queue overflowed (nothing inserted: the row is redone).
-__device__ __forceinline__ bool vt_drain(float* xbuf, int col, int N, Top16& top) {
-  if (col >= N) return true;
-  const uint8_t* cnt = vt_cnt(xbuf);
-  int n[4];
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    n[w] = cnt[w * 256 + col];
-    if (n[w] > kVtCap) return false;
-  }
-  const float2* cand = vt_cand(xbuf) + col * 4 * kVtCap;
-#pragma unroll
-  for (int w = 0; w < 4; ++w)
-    for (int i = 0; i < n[w]; ++i) {
-      const float2 e = cand[w * kVtCap + i];
-      top16_insert_ranked(top, e.x, __float_as_int(e.y));
-    }
-  return true;
-}
-
-// Row col's threshold: its list's 16th value (+inf for a column past N).
-__device__ __forceinline__ void vt_publish(float* xbuf, int col, int N, const Top16& top) {
-  vt_thr(xbuf)[col] = col < N ? top.v[kK - 1] : INFINITY;
 }
 
 template <int S>
@@ -1135,7 +1046,6 @@ __global__ void __launch_bounds__(VtCfg<S>::kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    int n_seen = 0;  // vocabulary tiles ranked so far
     for (int tile = cid; tile < n_tiles; tile += ncl) {
       const PairTile pt = pair_tile(tile, ncl, p.n_gate_tiles, n_tiles);
       const bool w_ok = mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, p.err, abort_flag, p.wait_limit_ns);
@@ -1149,22 +1059,7 @@ __global__ void __launch_bounds__(VtCfg<S>::kThreads, 1)
                              static_cast<uint32_t>(acc * Cfg::kAccCols);
       const int vbase = pt.n0 + static_cast<int>(rank) * 128;  // this CTA's first M entry
       if (pt.vocab) {
-        const int col0 = q * 32 + lane, col1 = 128 + q * 32 + lane;  // this thread's rows
-        bool redo0 = true, redo1 = true;  // rows still to be offered the tile's entries
-        if (n_seen >= kVtWarmTiles) {
-          vt_filter_push(xbuf, tbase, nchunk, q, lane, vbase + q * 32 + lane, p.V);
-          named_bar_sync(2, 128);  // every queued entry has landed
-          redo0 = !vt_drain(xbuf, col0, N, top0);
-          redo1 = !vt_drain(xbuf, col1, N, top1);
-        }
-        // the warm-up tiles, and any row whose queue overflowed, go through the turned-around
-        // accumulator (the barrier also ends every read of the queues)
-        if (!named_bar_and(2, 128, !(redo0 || redo1)))
-          vt_rank_turned<Cfg>(xbuf, tbase, nchunk, q, lane, vbase, p.V, top0, top1, redo0, redo1);
-        vt_publish(xbuf, col0, N, top0);
-        vt_publish(xbuf, col1, N, top1);
-        named_bar_sync(2, 128);  // thresholds visible to every warp
-        ++n_seen;
+        vt_rank_turned<Cfg>(xbuf, tbase, nchunk, q, lane, vbase, p.V, top0, top1);
       } else {
         // gate tile: lane = unit j of g (a W_g row), column = drafted row; sigmoid, and the
         // 32 lanes of a store write 32 consecutive units of one row

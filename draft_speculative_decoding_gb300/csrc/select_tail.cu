@@ -108,6 +108,13 @@ __device__ __forceinline__ void staged_copy(const Seg (&seg)[kNSeg]) {
   }
 }
 
+// Device-scope acquire-release add (returns the old value).
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // ------------------------------------------------------------------ packed keys
 // (value desc, id asc) as one unsigned 64-bit key: larger key = ranks first.
 __device__ __forceinline__ unsigned long long pack_key(float v, int id) {
@@ -437,29 +444,34 @@ __device__ float pair_scores_block(const TailLaunch& a, float* P, float* Q, cons
 // Sampled traversal (mode 2) by the whole block: from the last verified token, x_t is drawn
 // from q_t(c) = softmax_c(S_t(x_{t-1}, c) / T) over the 16 candidates by one uniform (Philox
 // stream 3) against the cumulative q in candidate order; if rounding leaves no candidate
-// above it, the last one with mass. Every (position p, predecessor a) row's q and draw are
-// computed first, one row per thread, the row's q kept in place of its scores; then thread 0 walks
-// from predecessor 0 and the drawn rows' q are copied out. Writes path_tok[P], pidx[P] and
-// q[P][16]; returns the path score in thread 0. Contains block barriers.
+// above it, the last one with mass. With backward messages logb (the joint path draw, mode
+// 3) the weights are S_t(x_{t-1}, c) / T + logb[t][c]. Every (position p, predecessor a)
+// row's q and draw are computed first, one row per thread, the row's q kept in place of its
+// scores; then thread 0 walks from predecessor 0 and the drawn rows' q are copied out.
+// Writes path_tok[P], pidx[P] and q[P][16]; returns the path score in thread 0. Contains
+// block barriers.
 __device__ float path_sample_block(float* S, const int* ids, int P, float inv_T, uint64_t seed,
                                    int b, int* path_tok, int* pidx, float* q, float* sdraw,
-                                   float* upath, unsigned char* draw) {
+                                   float* upath, unsigned char* draw,
+                                   const float* logb = nullptr) {
   if (threadIdx.x < P) upath[threadIdx.x] = uniform_path(seed, b, threadIdx.x + 1);
   __syncthreads();
   for (int x = threadIdx.x; x < P * kK; x += blockDim.x) {
     float* row = S + x * kK;
-    float v[kK];
+    const float* lb = logb != nullptr ? logb + (x >> 4) * kK : nullptr;
+    float v[kK], w[kK];
     float m = -INFINITY;
 #pragma unroll
     for (int c = 0; c < kK; ++c) {
       v[c] = row[c];
-      m = fmaxf(m, v[c] * inv_T);
+      w[c] = v[c] * inv_T + (lb != nullptr ? lb[c] : 0.f);
+      m = fmaxf(m, w[c]);
     }
     float z = 0.f;
     float e[kK];
 #pragma unroll
     for (int c = 0; c < kK; ++c) {
-      e[c] = expf(v[c] * inv_T - m);
+      e[c] = expf(w[c] - m);
       z += e[c];
     }
     const float u = upath[x >> 4];
@@ -501,6 +513,27 @@ __device__ float path_sample_block(float* S, const int* ids, int P, float inv_T,
   }
   __syncthreads();
   return total;
+}
+
+// Backward messages of the joint path draw (mode 3) by the whole block (256 threads):
+// logb[P-1][c] = 0 and logb[p][a] = log sum_c exp(S_{p+1}(a, c) / T + logb[p+1][c]), one
+// (a, c) term per thread, the log-sum-exp over c across a half-warp. Contains barriers.
+__device__ void backward_messages_block(const float* S, int P, float inv_T, float* logb) {
+  static_assert(kTailThreads == kK * kK, "one (a, c) term per thread");
+  const int a = threadIdx.x >> 4, c = threadIdx.x & 15;
+  if (threadIdx.x < kK) logb[(P - 1) * kK + threadIdx.x] = 0.f;
+  __syncthreads();
+  for (int p = P - 2; p >= 0; --p) {
+    const float x = S[((p + 1) * kK + a) * kK + c] * inv_T + logb[(p + 1) * kK + c];
+    float m = x;
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float e = expf(x - m);
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) e += __shfl_xor_sync(0xffffffffu, e, off);
+    if (c == 0) logb[p * kK + a] = m + logf(e);
+    __syncthreads();
+  }
 }
 
 // Greedy traversal by the whole block: the best successor of every (position, predecessor)
@@ -884,6 +917,7 @@ struct TailSmem {
   float* qprop;                  // sampled traversal: [P][16] proposal distributions
   float* sdraw;                  // [P][16] score of the drawn successor of each (p, a)
   float* upath;                  // [P] path-draw uniforms
+  float* logb;                   // joint path draw: [P][16] backward messages (log beta)
   int* pidx;                     // [16] drawn candidate indices
   float* rstat;                  // [L][4] the request's published row statistics
   MergeSmem* ms;                 // top-16 merge scratch
@@ -902,6 +936,7 @@ __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
   n += sizeof(VerifySmem) + 16;
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
+  n += static_cast<size_t>(kMaxL) * kK * 4 + 16;
   n += kMaxL * 16 + 16;
   n += sizeof(MergeSmem) + 16;
   n += 32;
@@ -940,6 +975,7 @@ __device__ TailSmem carve(uint8_t* base, int G, int r) {
   s.pidx = reinterpret_cast<int*>(take(kMaxL * 4));
   s.sdraw = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
   s.upath = reinterpret_cast<float*>(take(kMaxL * 4));
+  s.logb = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
   s.rstat = reinterpret_cast<float*>(take(kMaxL * 16));
   s.ms = reinterpret_cast<MergeSmem*>(take(sizeof(MergeSmem)));
   s.bar = reinterpret_cast<uint64_t*>(take(16));
@@ -961,15 +997,21 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
   staged_copy<5, 3>(seg);
   __syncthreads();
   // path mode 2 at T > 0: the sampled traversal, verified against its own proposal; at
-  // T = 0 it is the greedy traversal
-  const bool sampled = a.path_mode == 2 && a.T > 0.f;
-  if (!sampled && a.path_mode != 1) {  // greedy (mode 2 at T = 0 included)
+  // T = 0 it is the greedy traversal. Mode 3 at T > 0: the joint path draw (the same
+  // traversal with backward messages), verified against its own conditionals; at T = 0 it
+  // is Viterbi, its T -> 0 limit.
+  const bool sampled = (a.path_mode == 2 || a.path_mode == 3) && a.T > 0.f;
+  const bool viterbi = a.path_mode == 1 || (a.path_mode == 3 && !sampled);
+  if (!sampled && !viterbi) {  // greedy (mode 2 at T = 0 included)
     const float score = path_greedy_block(sm.S_all, sm.ids_all, P, sm.path_tok, sm.bp);
     if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
     if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
   } else if (sampled) {
-    const float score = path_sample_block(sm.S_all, sm.ids_all, P, 1.0f / a.T, a.seed, b,
-                                          sm.path_tok, sm.pidx, sm.qprop, sm.sdraw, sm.upath, sm.bp);
+    const float inv_T = 1.0f / a.T;
+    if (a.path_mode == 3) backward_messages_block(sm.S_all, P, inv_T, sm.logb);
+    const float score = path_sample_block(sm.S_all, sm.ids_all, P, inv_T, a.seed, b,
+                                          sm.path_tok, sm.pidx, sm.qprop, sm.sdraw, sm.upath, sm.bp,
+                                          a.path_mode == 3 ? sm.logb : nullptr);
     if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
     if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
   } else if (threadIdx.x < 32) {
@@ -1039,12 +1081,13 @@ __global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_consta
   int pair;
   const float s = pair_scores_block(a, sm.P, sm.Q, sm.g, sm.prev_tok, sm.cand_id, sm.cand_U, pair);
   a.S[(static_cast<size_t>(b) * P + (t - 1)) * kK * kK + pair] = s;
-  __threadfence();
+  // hand-off: the block's writes (candidates, pair scores, row statistics) are ordered before
+  // thread 0's device-scope release by the barrier; the last block's acquire, then its
+  // barrier, orders the other blocks' writes before its reads
   __syncthreads();
-  if (threadIdx.x == 0) *sm.flag = (atomicAdd(a.counters + b, 1) == P - 1);
+  if (threadIdx.x == 0) *sm.flag = (atomic_add_acq_rel_gpu(a.counters + b, 1) == P - 1);
   __syncthreads();
   if (!*sm.flag) return;
-  __threadfence();
   finish_request(a, sm, b);
   if (threadIdx.x == 0) a.counters[b] = 0;
 }

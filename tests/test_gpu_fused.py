@@ -91,7 +91,7 @@ def _invariants(g, spec, npd, T):
 
 @pytest.mark.parametrize("spec", SMALL, ids=lambda s: s.name)
 @pytest.mark.parametrize("mode", [binding.DFS_PATH_GREEDY, binding.DFS_PATH_VITERBI,
-                                  binding.DFS_PATH_SAMPLE])
+                                  binding.DFS_PATH_SAMPLE, binding.DFS_PATH_SAMPLE_JOINT])
 @pytest.mark.parametrize("T", [0.0, 0.8])
 def test_fused_small(lib, orc, spec, mode, T):
     data = wl.generate(spec, "cuda")
@@ -178,19 +178,20 @@ def full_size():
 
 
 def _full_size_legs(spec):
-    """(path mode, T, seed) of a workload: every path mode and temperature it lists, and the
-    sampled traversal at each T > 0 with two seeds."""
+    """(path mode, T, seed) of a workload: every path mode and temperature it lists, the
+    sampled traversal at each T > 0 with two seeds, and the joint path draw at each T > 0."""
     code = {"greedy": binding.DFS_PATH_GREEDY, "viterbi": binding.DFS_PATH_VITERBI}
     legs = [(code[m], T, spec.seed) for m in spec.path_modes for T in spec.temperatures]
     legs += [(binding.DFS_PATH_SAMPLE, T, s) for T in spec.temperatures if T > 0
              for s in (spec.seed, spec.seed + 17)]
+    legs += [(binding.DFS_PATH_SAMPLE_JOINT, T, spec.seed + 5) for T in spec.temperatures if T > 0]
     return legs
 
 
 @pytest.mark.parametrize("spec", FULL, ids=lambda s: s.name)
 def test_fused_full_size_every_request(lib, orc, full_size, spec, monkeypatch):
     data, npd, head = full_size(orc, spec)
-    names = {0: "greedy", 1: "viterbi", 2: "sampled"}
+    names = {0: "greedy", 1: "viterbi", 2: "sampled", 3: "joint"}
     # the throughput workload also with the drafted-rows LM head forced (8 vocabulary tiles
     # per CTA pair: its threshold filter runs after the warm-up tiles)
     variants = ("0", "6") if spec is wl.THROUGHPUT else ("0",)

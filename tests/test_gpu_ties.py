@@ -114,10 +114,9 @@ def test_fused_candidates_with_ties(lib, B, L, V, variant, monkeypatch):
 @pytest.mark.parametrize("variant", ["5", "6"])
 def test_lmhead_logits_increasing_with_id(lib, orc, variant, monkeypatch):
     """Logits that grow with the token id, equal within each run of three consecutive ids
-    (every later tile beats every list: the drafted-rows kernel's per-row queues overflow on
-    each tile after its warm-up and the tile is ranked through the turned-around accumulator
-    instead). The top-16 is five whole runs and the lowest id of the sixth: exact ties inside
-    it and at its 16/17 boundary, as the oracle gives them."""
+    (every later tile beats every list, so every list is rebuilt on every tile). The top-16
+    is five whole runs and the lowest id of the sixth: exact ties inside it and at its 16/17
+    boundary, as the oracle gives them."""
     monkeypatch.setenv("DFS_LMHEAD_VARIANT", variant)
     B, L, V, d = 32, 8, 65528, 128
     g = torch.Generator().manual_seed(5)
