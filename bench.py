@@ -274,6 +274,11 @@ def run_ours(args):
     ms_prop, _, _ = timed(args.sampling_temperature, max(10, args.steps // 2), args.warmup,
                           path_mode=binding.DFS_PATH_SAMPLE)
     accept_prop = outs[2].float().mean().item()
+    # the joint path draw (the whole path from the distribution the scores define over the
+    # lattice) verified against its own conditionals
+    ms_joint, _, _ = timed(args.sampling_temperature, max(10, args.steps // 2), args.warmup,
+                           path_mode=binding.DFS_PATH_SAMPLE_JOINT)
+    accept_joint = outs[2].float().mean().item()
 
     # the same step with the LM head given quantised to E4M3 (one power-of-two scale per
     # vocabulary entry; rows quantised per call): half the LM-head bytes
@@ -515,6 +520,7 @@ def run_ours(args):
     ms_max = replicas.max_over_ranks(ms_greedy)
     value_samp = replicas.job_throughput(spec.B, ms_samp / 1e3)
     value_prop = replicas.job_throughput(spec.B, ms_prop / 1e3)
+    value_joint = replicas.job_throughput(spec.B, ms_joint / 1e3)
     value_graph = replicas.job_throughput(spec.B, ms_graph / 1e3)
     value_q = replicas.job_throughput(spec.B, ms_q / 1e3)
     q_bytes = spec.d * spec.V + spec.B * spec.L * spec.V * 2  # E4M3 head + target logits
@@ -587,7 +593,10 @@ def run_ours(args):
                          "path": args.path_mode,
                          "sampled_path": {"value": round(value_prop, 1), "unit": UNIT,
                                           "ms_per_step": round(ms_prop, 4),
-                                          "mean_accept_len": round(accept_prop, 3)}},
+                                          "mean_accept_len": round(accept_prop, 3)},
+                         "joint_path": {"value": round(value_joint, 1), "unit": UNIT,
+                                        "ms_per_step": round(ms_joint, 4),
+                                        "mean_accept_len": round(accept_joint, 3)}},
             "e4m3_head": {"value": round(value_q, 1), "unit": UNIT,
                           "ms_per_step": round(ms_q, 4),
                           "hbm_roofline_frac_step": round(q_bytes / (ms_q * 1e-3) / 1e9 /

@@ -255,6 +255,9 @@ __global__ void __launch_bounds__(LmCfg<MT, NT, NBUF, SW, SH>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // Launched as a programmatic dependent: the set-up above overlaps the previous kernel on
+  // the stream; nothing below touches global memory before that kernel has completed.
+  grid_dependency_wait();
   // Every CTA of this persistent grid is resident now: let the dependent tail kernel launch
   // onto SMs as they free up (it waits for this grid's completion before reading).
   grid_dependents_launch();
@@ -550,6 +553,11 @@ __global__ void __launch_bounds__(PairCfg<S>::kThreads, 1)
   cluster_sync();  // both CTAs' barriers are initialised before either signals the other's
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // bf16: launched as a programmatic dependent of whatever precedes it on the stream; the
+  // set-up above overlaps that kernel, nothing below touches global memory before it has
+  // completed. E4M3: the dependent of the row quantisation; the roles that read its output
+  // wait for it below, the target-row statistics do not.
+  if (!kE4M3) grid_dependency_wait();
   grid_dependents_launch();
 
   const int n_tiles = p.n_vocab_tiles + p.n_gate_tiles;
@@ -921,6 +929,7 @@ __global__ void __launch_bounds__(VtCfg<S>::kThreads, 1)
   cluster_sync();  // both CTAs' barriers are initialised before either signals the other's
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  grid_dependency_wait();  // programmatic dependent: the set-up above overlaps the previous kernel
   grid_dependents_launch();
 
   const int n_tiles = p.n_vocab_tiles + p.n_gate_tiles;
@@ -1311,13 +1320,15 @@ cudaError_t launch_vt(const LmheadParams& prm, int grid, cudaStream_t s) {
   cfg.blockDim = dim3(Cfg::kThreads);
   cfg.dynamicSmemBytes = Cfg::smem(prm.stage_bytes);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
   if (e == cudaSuccess) note_launches(1);
   return e;
@@ -1334,8 +1345,17 @@ cudaError_t launch_cfg(const LmheadParams& prm, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(prm);
-  const cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }
@@ -1481,7 +1501,7 @@ cudaError_t launch_lmhead_tc(const LmheadLaunch& a, cudaStream_t s) {
                         64, static_cast<uint32_t>(a.gate ? (rs ? NT / 2 : NT) : 128)))
       return cudaErrorInvalidValue;
     const int grid = a.vocab ? a.G : (prm.n_gate_tiles > 0 ? prm.n_gate_tiles : 1) * (rs ? 2 : 1);
-    const cudaError_t e = rs ? launch_pair<7, false>(prm, grid, s)
+    const cudaError_t e = rs ? launch_pair<7, false>(prm, grid, s, true)
                              : launch_cfg<1, 256, 2, 5, 4>(prm, grid, s);
     if (e != cudaSuccess) return e;
   }

@@ -1040,6 +1040,9 @@ __global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_consta
     fence_barrier_init();
   }
   __syncthreads();
+  // the next step's LM-head kernel (a programmatic dependent) may set up on SMs this grid
+  // leaves free; it waits for this grid's completion before touching memory
+  grid_dependents_launch();
   grid_dependency_wait();  // the LM-head kernel's results (launched as its dependent)
   // the gate row and the partial top-16 lists of positions t and t-1: bulk copies
   const size_t lst = static_cast<size_t>(a.G) * kK;
