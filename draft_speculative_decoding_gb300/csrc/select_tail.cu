@@ -127,9 +127,9 @@ __device__ __forceinline__ unsigned long long pack_key(float v, int id) {
 // ------------------------------------------------------------------ target rows
 // One block of 128 threads reduces kZChunk (4096) elements of one row of Z: each thread
 // holds 4 groups of 8 consecutive elements, the groups 1024 elements apart. Block (c, y)
-// takes chunk c of rows y, y + gridDim.y, ... (any number of rows with at most 65535 blocks
-// in the second grid dimension).
-template <bool kSoft>
+// takes chunk c of row y; with kStrided, of rows y, y + gridDim.y, ... (more rows than the
+// 65535 blocks of the second grid dimension; the one-row form measured faster where it fits).
+template <bool kSoft, bool kStrided>
 __global__ void __launch_bounds__(128) k_zreduce(const void* Z, int is_bf16, int rows, int V,
                                                  int nchunk, float inv_T, float* zmax, int* zarg,
                                                  float* zsum, int* zero_ptr, int zero_count) {
@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(128) k_zreduce(const void* Z, int is_bf16, int
         if (kSoft) zsum[o] = st.s;
       }
     }
+    if (!kStrided) break;
     __syncthreads();  // ws is rewritten by the next row
   }
 }
@@ -1219,13 +1220,12 @@ cudaError_t allow_smem() {
 }  // namespace
 
 cudaError_t launch_zreduce(const ZReduceLaunch& a, cudaStream_t s) {
-  dim3 grid(a.nchunk, a.rows < 65535 ? a.rows : 65535);
-  if (a.inv_T > 0.f)
-    k_zreduce<true><<<grid, 128, 0, s>>>(a.Z, a.zdtype == 0, a.rows, a.V, a.nchunk, a.inv_T,
-                                         a.zmax, a.zarg, a.zsum, a.zero_ptr, a.zero_count);
-  else
-    k_zreduce<false><<<grid, 128, 0, s>>>(a.Z, a.zdtype == 0, a.rows, a.V, a.nchunk, 0.f,
-                                          a.zmax, a.zarg, a.zsum, a.zero_ptr, a.zero_count);
+  const bool strided = a.rows > 65535;
+  dim3 grid(a.nchunk, strided ? 65535 : a.rows);
+  auto kern = a.inv_T > 0.f ? (strided ? k_zreduce<true, true> : k_zreduce<true, false>)
+                            : (strided ? k_zreduce<false, true> : k_zreduce<false, false>);
+  kern<<<grid, 128, 0, s>>>(a.Z, a.zdtype == 0, a.rows, a.V, a.nchunk, a.inv_T, a.zmax, a.zarg,
+                           a.zsum, a.zero_ptr, a.zero_count);
   return counted(cudaGetLastError());
 }
 
