@@ -212,16 +212,34 @@ __device__ __forceinline__ int warp_best_lane(bool has, float v, int id) {
   return __ffs(w) - 1;
 }
 
-// Block-wide top 16 (value desc, id asc) of nm <= 2 sets of G <= 256 sorted lists of 16.
-// Ids are unique across lists (the vocabulary tiles partition V) and the only repeated
-// entries are the (-inf, INT_MAX) fillers, so the packed key orders them totally.
-// 1. The 16 lists with the best heads: no entry of any other list can be in the top 16,
-//    since each of those 16 heads ranks before that list's head, which ranks before the
-//    rest of its list. Heads are ranked by counting (ties of filler heads by list index).
-// 2. A merge tree over those 16 lists: a half-warp merges two sorted lists into their top
-//    16 (the elementwise better of A[l] and B[15-l] is bitonic, four half-cleaner steps sort
-//    it), 16 -> 8 -> 4 -> 2 -> 1 lists per set.
+// Top 16 (value desc, id asc) of a set of G <= 256 sorted lists of 16, by warps m and m + 2
+// (set m). The lists are staged as they are written: entry n of list j at place j * 16 + n.
+// Ids are unique across lists (the vocabulary tiles partition V); the only repeated entries
+// are the (-inf, INT_MAX) fillers, which merge_key tells apart by their place, below every
+// real entry of equal value. So the keys of a set are distinct.
+// 1. The lists are taken in groups of 2^lg consecutive lists, at most kMaxGroups groups (one
+//    per lane of the two warps); a group's head is its best list head. Group heads are ranked
+//    by counting (broadcast shared-memory loads). Only the 16 groups with the best heads can
+//    hold a top-16 entry (each of those heads ranks before any other group's head, which
+//    ranks before every other entry of that group), and theta, the 16th best group head, is
+//    a lower bound on the 16th best key overall (16 distinct entries reach it).
+// 2. Candidates, by warp m alone: the entries >= theta of those groups' lists (no other
+//    entry reaches theta; in a sorted list they are a prefix), placed by a warp scan of the
+//    prefix lengths, with their values and ids. The top 16 are among them. Logits without order across the vocabulary
+//    tiles leave a few more than 16; logits that rise or fall with the id can leave hundreds.
+// 3. Up to kCandMax candidates: each one's rank among them by counting; ranks 0..15 are the
+//    result. More: merge_exact, by warps 0..3, takes over.
+constexpr int kCandMax = 64;
+constexpr int kMaxGroups = 40;
 struct MergeSmem {
+  unsigned long long gk[2][kMaxGroups];  // group heads
+  unsigned long long ck[2][kCandMax + 2];  // candidate keys (one zero pad)
+  unsigned long long theta[2];           // 16th best group head
+  float cv[2][kCandMax];                // candidate values
+  int ci[2][kCandMax];                  // candidate ids
+  int gsel[2][kK];                     // groups by head rank
+  int ncand[2];
+  // merge_exact
   unsigned long long hk[2][kMaxLists];  // head keys
   int sel[2][kK];                       // lists by head rank
   float v1[16][kK];                     // tree levels: 16, 4 lists (both sets)
@@ -231,6 +249,142 @@ struct MergeSmem {
 };
 
 __device__ __forceinline__ void bar_sync_warps0to3() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// warps m and m + 2, the two warps of set m
+__device__ __forceinline__ void bar_sync_set(int m) {
+  if (m == 0)
+    asm volatile("bar.sync 3, 64;" ::: "memory");
+  else
+    asm volatile("bar.sync 4, 64;" ::: "memory");
+}
+
+// pack_key, except that a filler (id INT_MAX) takes the low word 0x7fffffff - pos: distinct
+// for every place pos, and below the low word ~id of any real entry.
+__device__ __forceinline__ unsigned long long merge_key(float v, int id, int pos) {
+  const unsigned long long k = pack_key(v, id);
+  return id == kIntMax ? ((k & 0xffffffff00000000ull) | static_cast<uint32_t>(0x7fffffff - pos)) : k;
+}
+
+// Set m's step 1, by its two warps (h = 0: warp m, h = 1: warp m + 2), each taking half of
+// the groups, one per lane; ends with gsel and theta in shared memory for warp m.
+__device__ __forceinline__ void merge_rank_groups(const float* sv, const int* si, int m, int h, int G,
+                                                  MergeSmem& ms) {
+  const int lane = threadIdx.x & 31;
+  int lg = 0;
+  while ((kMaxGroups << lg) < G) ++lg;
+  const int gs = 1 << lg, ng = (G + gs - 1) >> lg, half = (ng + 1) >> 1;
+  const int g = h * half + lane;
+  const bool valid = lane < half && g < ng;
+  unsigned long long k = 0;  // zero (below every key) past the last group
+  if (valid) {
+    for (int d = 0; d < gs; ++d) {
+      const int j = (g << lg) + d;
+      if (j < G) {
+        const unsigned long long x = merge_key(sv[j * kK], si[j * kK], j * kK);
+        k = x > k ? x : k;
+      }
+    }
+  }
+  if (lane < half) ms.gk[m][g] = k;
+  if (h == 0 && lane < kK) ms.gsel[m][lane] = -1;
+  if (h == 0 && lane == 0) ms.theta[m] = 0;  // fewer than 16 groups: every entry is a candidate
+  bar_sync_set(m);
+  if (valid) {
+    const ulonglong2* g2 = reinterpret_cast<const ulonglong2*>(ms.gk[m]);
+    int rank = 0;
+#pragma unroll 4
+    for (int i = 0; i < half; ++i) {
+      const ulonglong2 o = g2[i];  // broadcast
+      rank += (o.x > k) + (o.y > k);
+    }
+    if (rank < kK) ms.gsel[m][rank] = g;
+    if (rank == kK - 1) ms.theta[m] = k;
+  }
+  bar_sync_set(m);
+}
+
+// Set m's steps 2 and 3, by warp m alone. Returns the candidate count (the same in every
+// lane); when it is at most kCandMax, outv/outi hold the top 16 and every lane of the warp
+// sees them.
+__device__ __forceinline__ int merge_candidates_warp(const float* sv, const int* si, int m, int G,
+                                                     MergeSmem& ms, float* outv, int* outi) {
+  const int lane = threadIdx.x & 31;
+  int lg = 0;
+  while ((kMaxGroups << lg) < G) ++lg;
+  const int gs = 1 << lg;
+  const unsigned long long theta = ms.theta[m];
+  // 2. candidates: the lane takes selected lists lane, lane + 32, ... (16 * 2^lg <= 128); the
+  // keys of the first four entries of its first list are kept for the writes
+  const int nsl = kK << lg;
+  int len[4], jl[4];
+  unsigned long long kf[4];
+  int total = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int s = lane + 32 * i;
+    len[i] = 0;
+    jl[i] = 0;
+    if (s < nsl) {
+      const int g = ms.gsel[m][s >> lg];
+      const int j = (g << lg) + (s & (gs - 1));
+      jl[i] = j;
+      if (g >= 0 && j < G) {  // the first four entries at once, the rest one by one
+        int n = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const unsigned long long x = merge_key(sv[j * kK + e], si[j * kK + e], j * kK + e);
+          if (i == 0) kf[e] = x;
+          n += x >= theta;
+        }
+        if (n == 4)
+          while (n < kK && merge_key(sv[j * kK + n], si[j * kK + n], j * kK + n) >= theta) ++n;
+        len[i] = n;
+      }
+    }
+    total += len[i];
+  }
+  int incl = total;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  const int c = __shfl_sync(0xffffffffu, incl, 31);
+  if (c > kCandMax) return c;
+  int q = incl - total;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = jl[i];
+    for (int n = 0; n < len[i]; ++n, ++q) {
+      const unsigned long long kn = n == 0 ? kf[0] : n == 1 ? kf[1] : n == 2 ? kf[2] : kf[3];
+      ms.ck[m][q] = (i == 0 && n < 4) ? kn : merge_key(sv[j * kK + n], si[j * kK + n], j * kK + n);
+      ms.cv[m][q] = sv[j * kK + n];
+      ms.ci[m][q] = si[j * kK + n];
+    }
+  }
+  if (lane == 0 && (c & 1)) ms.ck[m][c] = 0;  // pads the last pair: below every key
+  __syncwarp();
+  // 3. ranks among the candidates
+  const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(ms.ck[m]);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int x = lane + 32 * h;
+    if (x < c) {
+      const unsigned long long k = ms.ck[m][x];
+      int rank = 0;
+#pragma unroll 4
+      for (int i = 0; i < (c + 1) / 2; ++i) {
+        const ulonglong2 o = c2[i];  // broadcast
+        rank += (o.x > k) + (o.y > k);
+      }
+      if (rank < kK) {
+        outv[rank] = ms.cv[m][x];
+        outi[rank] = ms.ci[m][x];
+      }
+    }
+  }
+  __syncwarp();
+  return c;
+}
 
 // Two sorted lists (element l16 of A and of B in lane l16 of this half-warp) merged into
 // their top 16, sorted, in (av, ai). All 32 lanes of the warp call it.
@@ -254,52 +408,47 @@ __device__ __forceinline__ void merge2_halfwarp(float& av, int& ai, float bv, in
   }
 }
 
-// Steps 1 and the first tree level, by the whole block; ends with the level's lists in
-// ms.v1/ms.i1 (set m's list p at m * 8 + p) and a block barrier.
-__device__ void merge_begin(const float* sv0, const int* si0, const float* sv1, const int* si1,
-                            int nm, int G, MergeSmem& ms) {
-  const int n = nm * G;
-  for (int x = threadIdx.x; x < n; x += kTailThreads) {
+// The exact merge, for sets with more than kCandMax candidates, by warps 0..3 (they sync
+// among themselves): every head ranked by counting, then a merge tree over the 16 lists with
+// the best heads: a half-warp merges two sorted lists into their top 16 (the elementwise
+// better of A[l] and B[15-l] is bitonic, four half-cleaner steps sort it), 16 -> 8 -> 4 -> 2
+// -> 1 lists per set. Set m's top 16 go to outv[m]/outi[m] where wm (w0, w1) is set.
+__device__ __noinline__ void merge_exact(const float* sv0, const int* si0, const float* sv1, const int* si1,
+                                         int nm, int G, MergeSmem& ms, float* outv0, int* outi0,
+                                         float* outv1, int* outi1, bool w0, bool w1) {
+  const int tid = threadIdx.x;
+  for (int x = tid; x < nm * G; x += 128) {
     const int m = x >= G, j = x - m * G;
-    ms.hk[m][j] = pack_key((m ? sv1 : sv0)[j * kK], (m ? si1 : si0)[j * kK]);
+    ms.hk[m][j] = merge_key((m ? sv1 : sv0)[j * kK], (m ? si1 : si0)[j * kK], j * kK);
   }
-  if (threadIdx.x < 2 * kK) ms.sel[threadIdx.x >> 4][threadIdx.x & 15] = -1;
-  __syncthreads();
-  for (int x = threadIdx.x; x < n; x += kTailThreads) {
+  if (tid < 2 * kK) ms.sel[tid >> 4][tid & 15] = -1;
+  bar_sync_warps0to3();
+  for (int x = tid; x < nm * G; x += 128) {
     const int m = x >= G, j = x - m * G;
     const unsigned long long k = ms.hk[m][j];
     int rank = 0;
-#pragma unroll 8
-    for (int i = 0; i < G; ++i) {
-      const unsigned long long o = ms.hk[m][i];
-      rank += (o > k) || (o == k && i < j);
-    }
+    for (int i = 0; i < G; ++i) rank += ms.hk[m][i] > k;
     if (rank < kK) ms.sel[m][rank] = j;
   }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, l16 = lane & 15;
-  const int q = warp * 2 + (lane >> 4);  // merge q of 16: set q >> 3, lists 2p, 2p+1
-  const int m = q >> 3, p = q & 7;
-  const float* sv = m ? sv1 : sv0;
-  const int* si = m ? si1 : si0;
-  const int la = m < nm ? ms.sel[m][2 * p] : -1, lb = m < nm ? ms.sel[m][2 * p + 1] : -1;
-  float av = la >= 0 ? sv[la * kK + l16] : -INFINITY;
-  int ai = la >= 0 ? si[la * kK + l16] : kIntMax;
-  const float bv = lb >= 0 ? sv[lb * kK + l16] : -INFINITY;
-  const int bi = lb >= 0 ? si[lb * kK + l16] : kIntMax;
-  merge2_halfwarp(av, ai, bv, bi);
-  ms.v1[q][l16] = av;
-  ms.i1[q][l16] = ai;
-  __syncthreads();
-}
-
-// The remaining tree levels, by warps 0..3 only (they sync among themselves); the top 16
-// of set m go to outv[m]/outi[m]. The caller joins all warps with a block barrier after.
-__device__ void merge_finish(int nm, MergeSmem& ms, float* outv0, int* outi0, float* outv1,
-                             int* outi1) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, l16 = lane & 15;
+  bar_sync_warps0to3();
+  const int warp = tid >> 5, lane = tid & 31, l16 = lane & 15;
   const int h = lane >> 4;
-  {  // 16 -> 8 lists: merge q = 2 warp + h (q < 8), set q >> 2
+#pragma unroll 1
+  for (int rep = 0; rep < 2; ++rep) {  // 16 -> 8 lists per set: merge q, lists 2p, 2p+1
+    const int q = rep * 8 + warp * 2 + h, m = q >> 3, p = q & 7;
+    const float* sv = m ? sv1 : sv0;
+    const int* si = m ? si1 : si0;
+    const int la = m < nm ? ms.sel[m][2 * p] : -1, lb = m < nm ? ms.sel[m][2 * p + 1] : -1;
+    float av = la >= 0 ? sv[la * kK + l16] : -INFINITY;
+    int ai = la >= 0 ? si[la * kK + l16] : kIntMax;
+    const float bv = lb >= 0 ? sv[lb * kK + l16] : -INFINITY;
+    const int bi = lb >= 0 ? si[lb * kK + l16] : kIntMax;
+    merge2_halfwarp(av, ai, bv, bi);
+    ms.v1[q][l16] = av;
+    ms.i1[q][l16] = ai;
+  }
+  bar_sync_warps0to3();
+  {  // 8 -> 4 lists per set: merge q = 2 warp + h (q < 8), set q >> 2
     const int q = warp * 2 + h, m = q >> 2, p = q & 3;
     float av = ms.v1[m * 8 + 2 * p][l16];
     int ai = ms.i1[m * 8 + 2 * p][l16];
@@ -308,7 +457,7 @@ __device__ void merge_finish(int nm, MergeSmem& ms, float* outv0, int* outi0, fl
     ms.i2[q][l16] = ai;
   }
   bar_sync_warps0to3();
-  if (warp < 2) {  // 8 -> 4 lists: merge q = 2 warp + h (q < 4), set q >> 1
+  if (warp < 2) {  // 4 -> 2 lists per set: merge q = 2 warp + h (q < 4), set q >> 1
     const int q = warp * 2 + h, m = q >> 1, p = q & 1;
     float av = ms.v2[m * 4 + 2 * p][l16];
     int ai = ms.i2[m * 4 + 2 * p][l16];
@@ -317,89 +466,178 @@ __device__ void merge_finish(int nm, MergeSmem& ms, float* outv0, int* outi0, fl
     ms.i1[q][l16] = ai;
   }
   bar_sync_warps0to3();
-  if (warp == 0) {  // 4 -> 2 lists: half h is set h
+  if (warp == 0) {  // 2 -> 1 list per set: half h is set h
     float av = ms.v1[2 * h][l16];
     int ai = ms.i1[2 * h][l16];
     merge2_halfwarp(av, ai, ms.v1[2 * h + 1][l16], ms.i1[2 * h + 1][l16]);
-    if (h < nm) {
+    if (h < nm && (h ? w1 : w0)) {
       (h ? outv1 : outv0)[l16] = av;
       (h ? outi1 : outi0)[l16] = ai;
     }
   }
+  bar_sync_warps0to3();
 }
 
 // ------------------------------------------------------------------ pair scores
 // S_t(a, c) = U_t(c) + sum_j A(a)_j g_j B(c)_j for the 16 x 16 pairs of one position.
-// prev_tok[a] is the a-th predecessor token (all x0 for position 1); cur_tok/cur_U the
-// position's candidates; g (the gate row, shared memory) is already in place. P and Q are
-// [16][r+4] fp32 scratch rows. Warp w gathers table rows 4w..4w+3 (0..15: A rows of the
-// predecessors, scaled by g; 16..31: B rows of the candidates), one 16-byte chunk per lane
-// per step. Then thread (blk = tid / 16, ks = tid % 16) accumulates a 4 x 4 block of pairs
-// (a in 4 (blk / 4) + 0..3, c in 4 (blk % 4) + 0..3) over the float4 chunks ks, ks + 16, ...
-// of the rank, and the 16 lanes of each half-warp reduce-scatter the block so that lane ks
-// ends with pair (4 (blk / 4) + ks / 4, 4 (blk % 4) + ks % 4). Returns that pair's score and
-// its index a * 16 + c in `pair`.
-__device__ float pair_scores_block(const TailLaunch& a, float* P, float* Q, const float* g,
-                                   const int* prev_tok, const int* cur_tok, const float* cur_U,
-                                   int& pair) {
+// bf16 tables with r a multiple of 16 take the tensor-core path (gather_rows_bulk,
+// pair_dot_mma, below); the others the SIMT path: first one warp gathers 16 table rows into
+// fp32 shared rows dst[16][r+4],
+// the A rows of the predecessors scaled by the gate g (isA), or the B rows of the
+// candidates; lane l takes the 16-byte chunks l, l + 32, ... of every row, eight rows'
+// loads in flight at a time. tok == nullptr: every row is token tok_all (position 1, where
+// every predecessor is the last verified token). A token outside the vocabulary reads as a
+// zero row.
+__device__ __forceinline__ void gather_rows_warp(const TailLaunch& a, const int* tok, int tok_all, bool isA,
+                                              float* dst, const float* g) {
+  const int lane = threadIdx.x & 31;
   const int r = a.r, rs = r + 4;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int is_bf16 = a.dtype == 0;
   const int per_row = r * (is_bf16 ? 2 : 4) / 16;  // 16-byte chunks per row: <= 128
   const size_t row_bytes = static_cast<size_t>(r) * (is_bf16 ? 2 : 4);
-  uint4 raw[4][4];
+  const char* tab = static_cast<const char*>(isA ? a.A : a.Bt);
+  for (int ch = lane; ch < per_row; ch += 32) {
+#pragma unroll 1
+    for (int i0 = 0; i0 < kK; i0 += 8) {  // eight rows' loads in flight at a time
+      uint4 raw[8];
 #pragma unroll
-  for (int rr = 0; rr < 4; ++rr) {
-    const int row = warp * 4 + rr;
-    const int tok = row < 16 ? prev_tok[row] : cur_tok[row - 16];
-    const bool ok = tok >= 0 && tok < a.V;  // an id outside the vocabulary: zero embedding
-    const uint4* base = reinterpret_cast<const uint4*>(static_cast<const char*>(row < 16 ? a.A : a.Bt) +
-                                                       static_cast<size_t>(ok ? tok : 0) * row_bytes);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int ch = lane + 32 * c;
-      raw[rr][c] = (ok && ch < per_row) ? __ldg(base + ch) : make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-#pragma unroll
-  for (int rr = 0; rr < 4; ++rr) {
-    const int row = warp * 4 + rr;
-    const bool isP = row < 16;
-    float* dst = isP ? P + row * rs : Q + (row - 16) * rs;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int ch = lane + 32 * c;
-      if (ch >= per_row) continue;
-      const uint32_t w[4] = {raw[rr][c].x, raw[rr][c].y, raw[rr][c].z, raw[rr][c].w};
+      for (int i = 0; i < 8; ++i) {
+        const int t = tok ? tok[i0 + i] : tok_all;
+        raw[i] = (t >= 0 && t < a.V)
+                     ? __ldg(reinterpret_cast<const uint4*>(tab + static_cast<size_t>(t) * row_bytes) + ch)
+                     : make_uint4(0u, 0u, 0u, 0u);
+      }
       if (is_bf16) {
         const int e0 = ch * 8;
-        float x[8];
+        float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
+        if (isA) {
+          g0 = *reinterpret_cast<const float4*>(g + e0);
+          g1 = *reinterpret_cast<const float4*>(g + e0 + 4);
+        }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          x[2 * j] = bf16_bits_to_float(w[j] & 0xFFFFu);
-          x[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+          float x[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            x[2 * j] = bf16_bits_to_float(w[j] & 0xFFFFu);
+            x[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+          }
+          float* d = dst + (i0 + i) * rs + e0;
+          *reinterpret_cast<float4*>(d) = make_float4(x[0] * g0.x, x[1] * g0.y, x[2] * g0.z, x[3] * g0.w);
+          *reinterpret_cast<float4*>(d + 4) = make_float4(x[4] * g1.x, x[5] * g1.y, x[6] * g1.z, x[7] * g1.w);
         }
-        if (isP) {
-          const float4 g0 = *reinterpret_cast<const float4*>(g + e0);
-          const float4 g1 = *reinterpret_cast<const float4*>(g + e0 + 4);
-          x[0] *= g0.x; x[1] *= g0.y; x[2] *= g0.z; x[3] *= g0.w;
-          x[4] *= g1.x; x[5] *= g1.y; x[6] *= g1.z; x[7] *= g1.w;
-        }
-        *reinterpret_cast<float4*>(dst + e0) = make_float4(x[0], x[1], x[2], x[3]);
-        *reinterpret_cast<float4*>(dst + e0 + 4) = make_float4(x[4], x[5], x[6], x[7]);
       } else {
         const int e0 = ch * 4;
-        float4 x = make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]),
-                               __uint_as_float(w[3]));
-        if (isP) {
-          const float4 gg = *reinterpret_cast<const float4*>(g + e0);
-          x.x *= gg.x; x.y *= gg.y; x.z *= gg.z; x.w *= gg.w;
-        }
-        *reinterpret_cast<float4*>(dst + e0) = x;
+        float4 gg = make_float4(1.f, 1.f, 1.f, 1.f);
+        if (isA) gg = *reinterpret_cast<const float4*>(g + e0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float4*>(dst + (i0 + i) * rs + e0) =
+              make_float4(__uint_as_float(raw[i].x) * gg.x, __uint_as_float(raw[i].y) * gg.y,
+                          __uint_as_float(raw[i].z) * gg.z, __uint_as_float(raw[i].w) * gg.w);
       }
     }
   }
+}
+
+// The rows for the tensor-core products (bf16 tables, r a multiple of 16): one warp gathers
+// 16 rows of `table` as they are (bf16) into dst[16][r + 8] by bulk copies completing on
+// the mbarrier bar (lane i copies row i; the 16-byte pad per row keeps the MMA fragment
+// loads free of bank conflicts). tok == nullptr: every row is token tok_all. A token
+// outside the vocabulary gets a zero row, written by its lane (visible after a block
+// barrier). The barrier's one arrival is lane 0's, with the bytes of the copied rows.
+__device__ __forceinline__ void gather_rows_bulk(const TailLaunch& a, const int* tok, int tok_all,
+                                                 const void* table, uint16_t* dst, uint32_t bar) {
+  const int lane = threadIdx.x & 31;
+  const int rowb = a.r * 2, rsb = (a.r + 8) * 2;
+  int t = -1;
+  if (lane < kK) {
+    const int x = tok ? tok[lane] : tok_all;
+    t = (x >= 0 && x < a.V) ? x : -1;
+  }
+  const unsigned ok = __ballot_sync(0xffffffffu, t >= 0);
+  if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(ok) * rowb));
+  __syncwarp();
+  char* row = reinterpret_cast<char*>(dst) + lane * rsb;
+  if (t >= 0) {
+    bulk_load(smem_u32(row), static_cast<const char*>(table) + static_cast<size_t>(t) * rowb,
+              static_cast<uint32_t>(rowb), bar);
+  } else if (lane < kK) {
+    for (int o = 0; o < rowb; o += 16) *reinterpret_cast<uint4*>(row + o) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// D += A (16 x 16, bf16, row-major fragment) * B (16 x 8, bf16, column fragment), fp32.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The products on the tensor cores: the 16 x 16 scores are one 16 x 16 x r product of the
+// gated A rows (A g) and the B rows, both gathered as bf16 rows of stride r + 8. B enters
+// the MMA as it is. Each A g value is formed in fp32 and split into bf16 hi + lo (hi =
+// A g rounded, lo = the rest rounded), so (A g) B^T = hi B^T + lo B^T with about 16
+// significant bits of A g (against the 24 of an fp32 product), every bf16 product exact
+// and the sums in fp32. Warp w takes the k-steps of 16 w, w + 8, ...: two m16n8k16 MMAs
+// (hi, lo) per step and half of the 16 candidates; the eight warps' partial tiles are summed
+// through red[8][256] (shared memory). Returns the score of pair tid (a = tid / 16,
+// c = tid % 16) in `pair`. Contains a block barrier.
+__device__ float pair_dot_mma(int r, const uint16_t* Ab, const uint16_t* Bb, const float* g,
+                              const float* cur_U, float* red, int& pair) {
+  const int rsb = r + 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  for (int k0 = warp * 16; k0 < r; k0 += 8 * 16) {
+    uint32_t ahi[4], alo[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // a0..a3: rows gq, gq + 8; columns k0 + 2 tq, + 8
+      const int col = k0 + 8 * (q >> 1) + 2 * tq;
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(Ab + (gq + 8 * (q & 1)) * rsb + col);
+      const float2 gg = *reinterpret_cast<const float2*>(g + col);
+      const float x0 = bf16_bits_to_float(w & 0xFFFFu) * gg.x, x1 = bf16_bits_to_float(w >> 16) * gg.y;
+      const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+      const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+      ahi[q] = *reinterpret_cast<const uint32_t*>(&h);
+      alo[q] = *reinterpret_cast<const uint32_t*>(&l);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {  // candidates 8 nt .. 8 nt + 7
+      const uint16_t* brow = Bb + (8 * nt + gq) * rsb + k0 + 2 * tq;
+      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(brow);
+      const uint32_t b1 = *reinterpret_cast<const uint32_t*>(brow + 8);
+      mma_bf16_16816(d[nt], ahi, b0, b1);
+      mma_bf16_16816(d[nt], alo, b0, b1);
+    }
+  }
+  // d[nt]: rows gq (0, 1) and gq + 8 (2, 3), columns 8 nt + 2 tq (+1)
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    float* rw = red + warp * 256 + 8 * nt + 2 * tq;
+    *reinterpret_cast<float2*>(rw + gq * 16) = make_float2(d[nt][0], d[nt][1]);
+    *reinterpret_cast<float2*>(rw + (gq + 8) * 16) = make_float2(d[nt][2], d[nt][3]);
+  }
   __syncthreads();
+  const int t = threadIdx.x;
+  float acc = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) acc += red[w * 256 + t];
+  pair = t;
+  return cur_U[t & 15] + acc;
+}
+
+// Then the SIMT products, by the whole block once P (the gated A rows) and Q (the B rows) are
+// in place: thread (blk = tid / 16, ks = tid % 16) accumulates a 4 x 4 block of pairs (a in
+// 4 (blk / 4) + 0..3, c in 4 (blk % 4) + 0..3) over the float4 chunks ks, ks + 16, ... of
+// the rank, and the 16 lanes of each half-warp reduce-scatter the block so that lane ks ends
+// with pair (4 (blk / 4) + ks / 4, 4 (blk % 4) + ks % 4). Returns that pair's score and its
+// index a * 16 + c in `pair`.
+__device__ float pair_dot_block(int r, const float* P, const float* Q, const float* cur_U, int& pair) {
+  const int rs = r + 4;
   const int ks = threadIdx.x & 15, blk = threadIdx.x >> 4;
   const int a0 = 4 * (blk >> 2), c0 = 4 * (blk & 3);
   float acc[16];
@@ -907,7 +1145,6 @@ struct TailSmem {
   float* g;                      // gate row [r]
   float* cand_U; int* cand_id;   // merged candidates of t   [16]
   float* prev_U; int* prev_id;   // merged candidates of t-1 [16]
-  int* prev_tok;                 // predecessor tokens [16]
   float* P; float* Q;            // [16][r+4]
   float* S_all; int* ids_all;    // last block: [P][16][16], [P][16]
   unsigned char* bp;             // [16][16]
@@ -922,7 +1159,8 @@ struct TailSmem {
   int* pidx;                     // [16] drawn candidate indices
   float* rstat;                  // [L][4] the request's published row statistics
   MergeSmem* ms;                 // top-16 merge scratch
-  uint64_t* bar;                 // bulk-copy completion of the staged lists
+  uint64_t* bar;                 // bulk-copy completion: [0] the staged lists and gate row,
+                                 // [1] set 0's B rows, [2] set 1's A rows (tensor-core path)
   int* abort;                    // set when a bounded wait gave up
 };
 
@@ -940,7 +1178,7 @@ __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16;
   n += kMaxL * 16 + 16;
   n += sizeof(MergeSmem) + 16;
-  n += 32;
+  n += 48;
   return n + 256;
 }
 
@@ -962,7 +1200,6 @@ __device__ TailSmem carve(uint8_t* base, int G, int r) {
   s.cand_id = reinterpret_cast<int*>(take(64));
   s.prev_U = reinterpret_cast<float*>(take(64));
   s.prev_id = reinterpret_cast<int*>(take(64));
-  s.prev_tok = reinterpret_cast<int*>(take(64));
   s.P = reinterpret_cast<float*>(take(16 * static_cast<size_t>(r + 4) * 4));
   s.Q = reinterpret_cast<float*>(take(16 * static_cast<size_t>(r + 4) * 4));
   s.S_all = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * kK * 4));
@@ -979,9 +1216,32 @@ __device__ TailSmem carve(uint8_t* base, int G, int r) {
   s.logb = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
   s.rstat = reinterpret_cast<float*>(take(kMaxL * 16));
   s.ms = reinterpret_cast<MergeSmem*>(take(sizeof(MergeSmem)));
-  s.bar = reinterpret_cast<uint64_t*>(take(16));
+  s.bar = reinterpret_cast<uint64_t*>(take(32));
   s.abort = reinterpret_cast<int*>(take(16));
   return s;
+}
+
+// Set m's rows for the pair scores, by warp m: set 0's candidates' B rows (into Q), set 1's
+// predecessors' A rows (into P; every one the last verified token x0 when has_prev is false).
+// mma: bf16 rows by bulk copies completing on bar[1 + m]; otherwise fp32 rows, A scaled by g.
+__device__ __forceinline__ void gather_set_rows(const TailLaunch& a, const TailSmem& sm, int m, bool has_prev,
+                                                int x0, bool mma) {
+  const int* tok = m ? (has_prev ? sm.prev_id : nullptr) : sm.cand_id;
+  if (mma)
+    gather_rows_bulk(a, tok, x0, m ? a.A : a.Bt, reinterpret_cast<uint16_t*>(m ? sm.P : sm.Q),
+                     smem_u32(sm.bar + 1 + m));
+  else
+    gather_rows_warp(a, tok, x0, m == 1, m ? sm.P : sm.Q, sm.g);
+}
+
+// The 16 x 16 scores once the rows are in place (after a block barrier); every thread first
+// observes the bulk copies' completion on the tensor-core path.
+__device__ __forceinline__ float pair_scores(const TailLaunch& a, const TailSmem& sm, bool mma, int& pair) {
+  if (!mma) return pair_dot_block(a.r, sm.P, sm.Q, sm.cand_U, pair);
+  mbar_wait_bounded(smem_u32(sm.bar + 1), 0, a.err, sm.abort);
+  mbar_wait_bounded(smem_u32(sm.bar + 2), 0, a.err, sm.abort);
+  return pair_dot_mma(a.r, reinterpret_cast<const uint16_t*>(sm.P), reinterpret_cast<const uint16_t*>(sm.Q),
+                      sm.g, sm.cand_U, sm.S_all, pair);
 }
 
 // Path and verification of request b, run by the block that completes it. The scores and
@@ -1030,17 +1290,18 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
 // ------------------------------------------------------------------ kernels
 // Fused tail: block (t-1, b). Merges the candidates of positions t (and t-1), scores the
 // 16 x 16 pairs of position t, and the last block of request b runs path + verification.
-__global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_constant__ TailLaunch a) {
+__global__ void __launch_bounds__(kTailThreads, 2) k_tail_fused(const __grid_constant__ TailLaunch a) {
   extern __shared__ __align__(16) uint8_t tail_smem[];
   const int t = blockIdx.x + 1, b = blockIdx.y, L = a.L, P = L - 1;
   TailSmem sm = carve(tail_smem, a.G, a.r);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(sm.bar), 1);
+    for (int k = 0; k < 3; ++k) mbar_init(smem_u32(sm.bar + k), 1);
     *sm.abort = 0;
     fence_barrier_init();
   }
   __syncthreads();
+  const bool mma = a.dtype == 0 && a.r % 16 == 0;  // tensor-core products (bf16 rows)
   // the next step's LM-head kernel (a programmatic dependent) may set up on SMs this grid
   // leaves free; it waits for this grid's completion before touching memory
   grid_dependents_launch();
@@ -1048,42 +1309,60 @@ __global__ void __launch_bounds__(kTailThreads) k_tail_fused(const __grid_consta
   // the gate row and the partial top-16 lists of positions t and t-1: bulk copies
   const size_t lst = static_cast<size_t>(a.G) * kK;
   const size_t rc = static_cast<size_t>(b) * L + t;
+  const int nm = t >= 2 ? 2 : 1;
   if (threadIdx.x == 0) {
     const uint32_t bar = smem_u32(sm.bar);
     const uint32_t lb = static_cast<uint32_t>(lst * 4);
-    mbar_arrive_expect_tx(bar, a.r * 4 + (t >= 2 ? 4 : 2) * lb);
+    mbar_arrive_expect_tx(bar, a.r * 4 + 2 * nm * lb);
     bulk_load(smem_u32(sm.g), a.gate + rc * a.r, a.r * 4, bar);
     bulk_load(smem_u32(sm.lv_cur), a.part_val + rc * lst, lb, bar);
     bulk_load(smem_u32(sm.li_cur), a.part_idx + rc * lst, lb, bar);
-    if (t >= 2) {
+    if (nm == 2) {
       bulk_load(smem_u32(sm.lv_prev), a.part_val + (rc - 1) * lst, lb, bar);
       bulk_load(smem_u32(sm.li_prev), a.part_idx + (rc - 1) * lst, lb, bar);
     }
   }
-  // a wait that runs out leaves the error word set; the block runs on (every later index is
-  // bounds-checked) and the host reads DFS_ERR_TIMEOUT
-  mbar_wait_bounded(smem_u32(sm.bar), 0, a.err, sm.abort);
-  // the candidates of position t (and of t-1, the predecessors), merged by the block
-  const int nm = t >= 2 ? 2 : 1;
-  merge_begin(sm.lv_cur, sm.li_cur, sm.lv_prev, sm.li_prev, nm, a.G, *sm.ms);
   if (warp < 4) {
-    merge_finish(nm, *sm.ms, sm.cand_U, sm.cand_id, sm.prev_U, sm.prev_id);
+    // a wait that runs out leaves the error word set; the block runs on (every later index
+    // is bounds-checked) and the host reads DFS_ERR_TIMEOUT
+    mbar_wait_bounded(smem_u32(sm.bar), 0, a.err, sm.abort);
+    // set 0 (warps 0 and 2): the candidates of position t, then warp 0 gathers their B rows;
+    // set 1 (warps 1 and 3): the candidates of position t-1 (the predecessors), then warp 1
+    // gathers their A rows scaled by the gate (at position 1 the predecessor is the last
+    // verified token)
+    const int m = warp & 1;
+    if (m < nm)
+      merge_rank_groups(m ? sm.lv_prev : sm.lv_cur, m ? sm.li_prev : sm.li_cur, m, warp >> 1, a.G, *sm.ms);
+    if (warp < 2) {
+      int c = 0;
+      if (m < nm)
+        c = merge_candidates_warp(m ? sm.lv_prev : sm.lv_cur, m ? sm.li_prev : sm.li_cur, m, a.G, *sm.ms,
+                                  m ? sm.prev_U : sm.cand_U, m ? sm.prev_id : sm.cand_id);
+      if ((threadIdx.x & 31) == 0) sm.ms->ncand[m] = c;
+      if (c <= kCandMax) gather_set_rows(a, sm, m, t >= 2, a.x0[b], mma);
+    }
+    bar_sync_warps0to3();
+    const bool over0 = sm.ms->ncand[0] > kCandMax, over1 = sm.ms->ncand[1] > kCandMax;
+    if (over0 || over1) {  // too many candidates: the exact merge, then those rows
+      merge_exact(sm.lv_cur, sm.li_cur, sm.lv_prev, sm.li_prev, nm, a.G, *sm.ms, sm.cand_U,
+                  sm.cand_id, sm.prev_U, sm.prev_id, over0, over1);
+      if (warp == 0 && over0) gather_set_rows(a, sm, 0, true, 0, mma);
+      if (warp == 1 && over1) gather_set_rows(a, sm, 1, true, 0, mma);
+    }
   } else {
-    // meanwhile: the statistics of target row t-1 (and of the bonus row L-1 for the last
-    // position), published for the request's last block
-    if (warp == 4) row_stat_publish(a, b * L + t - 1, a.rstat + (static_cast<size_t>(b) * L + t - 1) * 4);
-    if (warp == 5 && t == P) row_stat_publish(a, b * L + L - 1, a.rstat + (static_cast<size_t>(b) * L + L - 1) * 4);
+    // meanwhile, warps 6 and 7: the statistics of target row t-1 (and of the bonus row L-1
+    // for the last position), published for the request's last block
+    if (warp == 6) row_stat_publish(a, b * L + t - 1, a.rstat + (static_cast<size_t>(b) * L + t - 1) * 4);
+    if (warp == 7 && t == P) row_stat_publish(a, b * L + L - 1, a.rstat + (static_cast<size_t>(b) * L + L - 1) * 4);
   }
   __syncthreads();
   if (threadIdx.x < kK) {
-    sm.prev_tok[threadIdx.x] = t >= 2 ? sm.prev_id[threadIdx.x] : a.x0[b];
     const size_t o = (static_cast<size_t>(b) * P + (t - 1)) * kK + threadIdx.x;
     a.cand_ids[o] = sm.cand_id[threadIdx.x];
     a.cand_U[o] = sm.cand_U[threadIdx.x];
   }
-  __syncthreads();
   int pair;
-  const float s = pair_scores_block(a, sm.P, sm.Q, sm.g, sm.prev_tok, sm.cand_id, sm.cand_U, pair);
+  const float s = pair_scores(a, sm, mma, pair);
   a.S[(static_cast<size_t>(b) * P + (t - 1)) * kK * kK + pair] = s;
   // hand-off: the block's writes (candidates, pair scores, row statistics) are ordered before
   // thread 0's device-scope release by the barrier; the last block's acquire, then its
@@ -1118,8 +1397,18 @@ __global__ void __launch_bounds__(kTailThreads) k_merge(const __grid_constant__ 
       {reinterpret_cast<const uint4*>(a.part_idx + rc * lst), reinterpret_cast<uint4*>(sm.li_cur), a.G * kK / 4}};
   staged_copy<8, 2>(seg);
   __syncthreads();
-  merge_begin(sm.lv_cur, sm.li_cur, nullptr, nullptr, 1, a.G, *sm.ms);
-  if (threadIdx.x < 128) merge_finish(1, *sm.ms, sm.cand_U, sm.cand_id, nullptr, nullptr);
+  if (threadIdx.x < 128) {
+    const int warp = threadIdx.x >> 5;
+    if (warp == 0 || warp == 2) merge_rank_groups(sm.lv_cur, sm.li_cur, 0, warp >> 1, a.G, *sm.ms);
+    if (warp == 0) {
+      const int c = merge_candidates_warp(sm.lv_cur, sm.li_cur, 0, a.G, *sm.ms, sm.cand_U, sm.cand_id);
+      if (threadIdx.x == 0) sm.ms->ncand[0] = c;
+    }
+    bar_sync_warps0to3();
+    if (sm.ms->ncand[0] > kCandMax)
+      merge_exact(sm.lv_cur, sm.li_cur, nullptr, nullptr, 1, a.G, *sm.ms, sm.cand_U, sm.cand_id,
+                  nullptr, nullptr, true, false);
+  }
   __syncthreads();
   if (threadIdx.x < kK) {
     const size_t o = (static_cast<size_t>(b) * P + (t - 1)) * kK + threadIdx.x;
@@ -1133,6 +1422,12 @@ __global__ void __launch_bounds__(kTailThreads) k_pair(const __grid_constant__ T
   extern __shared__ __align__(16) uint8_t tail_smem[];
   const int t = blockIdx.x + 1, b = blockIdx.y, L = a.L, P = L - 1;
   TailSmem sm = carve(tail_smem, 1, a.r);
+  const bool mma = a.dtype == 0 && a.r % 16 == 0;  // tensor-core products (bf16 rows)
+  if (threadIdx.x == 0) {
+    for (int k = 1; k < 3; ++k) mbar_init(smem_u32(sm.bar + k), 1);
+    *sm.abort = 0;
+    fence_barrier_init();
+  }
   const Seg seg[1] = {{reinterpret_cast<const uint4*>(a.gate + (static_cast<size_t>(b) * L + t) * a.r),
                        reinterpret_cast<uint4*>(sm.g), a.r / 4}};
   staged_copy<1, 1>(seg);
@@ -1140,11 +1435,13 @@ __global__ void __launch_bounds__(kTailThreads) k_pair(const __grid_constant__ T
     const size_t o = (static_cast<size_t>(b) * P + (t - 1)) * kK + threadIdx.x;
     sm.cand_id[threadIdx.x] = a.cand_ids[o];
     sm.cand_U[threadIdx.x] = a.cand_U[o];
-    sm.prev_tok[threadIdx.x] = t >= 2 ? a.cand_ids[o - kK] : a.x0[b];
+    sm.prev_id[threadIdx.x] = t >= 2 ? a.cand_ids[o - kK] : a.x0[b];
   }
   __syncthreads();
+  if (threadIdx.x < 64) gather_set_rows(a, sm, threadIdx.x >> 5, true, 0, mma);
+  __syncthreads();
   int pair;
-  const float s = pair_scores_block(a, sm.P, sm.Q, sm.g, sm.prev_tok, sm.cand_id, sm.cand_U, pair);
+  const float s = pair_scores(a, sm, mma, pair);
   a.S[(static_cast<size_t>(b) * P + (t - 1)) * kK * kK + pair] = s;
 }
 

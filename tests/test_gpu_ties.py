@@ -111,14 +111,8 @@ def test_fused_candidates_with_ties(lib, B, L, V, variant, monkeypatch):
         assert ids[i].tolist() == want, f"row {i}"
 
 
-@pytest.mark.parametrize("variant", ["5", "6"])
-def test_lmhead_logits_increasing_with_id(lib, orc, variant, monkeypatch):
-    """Logits that grow with the token id, equal within each run of three consecutive ids
-    (every later tile beats every list, so every list is rebuilt on every tile). The top-16
-    is five whole runs and the lowest id of the sixth: exact ties inside it and at its 16/17
-    boundary, as the oracle gives them."""
-    monkeypatch.setenv("DFS_LMHEAD_VARIANT", variant)
-    B, L, V, d = 32, 8, 65528, 128
+def _ramp_inputs(B, L, V, d):
+    """Logits that grow with the token id, equal within each run of three consecutive ids."""
     g = torch.Generator().manual_seed(5)
     h = (torch.randn(B, L, d, generator=g) * 0.01).to(torch.bfloat16)
     h[..., d - 1] = 16.0
@@ -129,6 +123,29 @@ def test_lmhead_logits_increasing_with_id(lib, orc, variant, monkeypatch):
     W = torch.zeros(d, V, dtype=torch.bfloat16)
     W[d - 1] = hi
     W[d - 2] = lo
+    return h, W
+
+
+def _ramp_expected(V):
+    """Five whole runs at the top and the lowest id of the sixth (lower id first in a run)."""
+    top = V - 1 - (V - 1) % 3  # the first id of the highest run
+    want = [top + k for k in range(V - top)]
+    base = top
+    while len(want) < 16:
+        base -= 3
+        want += [base + k for k in range(min(3, 16 - len(want)))]
+    return want
+
+
+@pytest.mark.parametrize("variant", ["5", "6"])
+def test_lmhead_logits_increasing_with_id(lib, orc, variant, monkeypatch):
+    """Logits that grow with the token id, equal within each run of three consecutive ids
+    (every later tile beats every list, so every list is rebuilt on every tile). The top-16
+    is five whole runs and the lowest id of the sixth: exact ties inside it and at its 16/17
+    boundary, as the oracle gives them."""
+    monkeypatch.setenv("DFS_LMHEAD_VARIANT", variant)
+    B, L, V, d = 32, 8, 65528, 128
+    h, W = _ramp_inputs(B, L, V, d)
     rows = np.array([b * L + t for b in range(B) for t in range(1, L)])
     o_ids, o_U, _ = orc.topk(orc.logits(wl.to_numpy_bits(h), wl.to_numpy_bits(W), rows), 16)
     dims = binding.make_dims(B, L, V, d, 8, binding.DFS_BF16, binding.DFS_BF16)
@@ -138,13 +155,34 @@ def test_lmhead_logits_increasing_with_id(lib, orc, variant, monkeypatch):
     assert binding.dfs_get_device_error(ws) == binding.DFS_OK
     ids = to_cpu(ids).reshape(-1, 16)
     U = to_cpu(U).reshape(-1, 16)
-    top = V - 1 - (V - 1) % 3  # the first id of the highest run
-    want = [top + k for k in range(V - top)]
-    base = top
-    while len(want) < 16:
-        base -= 3
-        want += [base + k for k in range(min(3, 16 - len(want)))]
+    want = _ramp_expected(V)
     assert all(o_ids[i].tolist() == want for i in range(len(rows)))
     for i in range(len(rows)):
         assert ids[i].tolist() == o_ids[i].tolist(), f"row {i}"
         assert np.all(close(U[i], o_U[i]))
+
+
+@pytest.mark.parametrize("B,variant", [(4, "0"), (32, "5"), (32, "6")])
+def test_fused_candidates_logits_increasing_with_id(lib, B, variant, monkeypatch):
+    """The fused call's merge on the same ramp. The 16 lists with the best heads then hold
+    far more entries above the 16th best head than its candidate buffer takes, so the merge
+    takes its tree path; generic logits (the other tests) take the candidate ranks."""
+    monkeypatch.setenv("DFS_LMHEAD_VARIANT", variant)
+    L, V, d, r = 8, 65528, 128, 16
+    h, W = _ramp_inputs(B, L, V, d)
+    g = torch.Generator().manual_seed(13)
+    Wg = (torch.randn(r, d, generator=g) / math.sqrt(d)).to(torch.bfloat16).cuda()
+    A = (torch.randn(V, r, generator=g) / math.sqrt(r)).to(torch.bfloat16).cuda()
+    Bt = (torch.randn(V, r, generator=g) / math.sqrt(r)).to(torch.bfloat16).cuda()
+    x0 = torch.randint(0, V, (B,), generator=g, dtype=torch.int32).cuda()
+    Z = torch.randn(B, L, V, generator=g).to(torch.bfloat16).cuda()
+    dims = binding.make_dims(B, L, V, d, r, binding.DFS_BF16, binding.DFS_BF16)
+    ws = binding.alloc_workspace(dims)
+    res = binding.dfs_select_verify(dims, h.cuda(), W.cuda(), Wg, A, Bt, x0, Z,
+                                    binding.DFS_PATH_GREEDY, 0.0, 1, ws, want_intermediates=True)
+    torch.cuda.synchronize()
+    assert binding.dfs_get_device_error(ws) == binding.DFS_OK
+    ids = to_cpu(res["cand_ids"]).reshape(-1, 16)
+    want = _ramp_expected(V)
+    for i in range(ids.shape[0]):
+        assert ids[i].tolist() == want, f"row {i}"
