@@ -52,6 +52,7 @@ struct Layout {
   size_t logits;
   size_t hq, h_scale;  // E4M3 LM head: quantised rows and their scales
   size_t rstat;        // fused tail: target-row statistics [B*L][4]
+  size_t succ;         // fused tail, greedy path: best successors [B][L-1][16] (int2)
   size_t total;
   int G, nchunk;
 };
@@ -99,6 +100,7 @@ bool make_layout(const dfs_dims& d, Layout* L) {
   L->hq = take(d.dtype == DFS_BF16 ? rows * static_cast<size_t>(d.d) : 0);
   L->h_scale = take(4 * rows);
   L->rstat = take(16 * rows);
+  L->succ = take(8 * d.B * P * kK);
   L->total = off;
   return true;
 }
@@ -168,6 +170,7 @@ dfs::TailLaunch tail_args(const dfs_dims& d, const Layout& L, void* ws) {
   t.counters = at<int>(ws, L.counters);
   t.err = at<int>(ws, L.err);
   t.rstat = at<float>(ws, L.rstat);
+  t.succ = at<int2>(ws, L.succ);
   return t;
 }
 

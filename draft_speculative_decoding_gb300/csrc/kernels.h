@@ -163,6 +163,8 @@ struct TailLaunch {
   int* err;
   float* rstat;              // fused tail: [B*L][4] target-row statistics (max, argmax bits,
                              // log-sum-exp), published by the position blocks
+  int2* succ;                // fused tail, greedy path: [B][L-1][16] each predecessor's best
+                             // successor (candidate index, score bits), from the position blocks
 };
 // Fused tail for dfs_select_verify: (L-1) x B blocks; the last block of each request
 // selects its path and verifies it.

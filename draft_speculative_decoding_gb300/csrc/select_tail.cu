@@ -265,8 +265,10 @@ __device__ __forceinline__ unsigned long long merge_key(float v, int id, int pos
 }
 
 // Set m's step 1, by its two warps (h = 0: warp m, h = 1: warp m + 2), each taking half of
-// the groups, one per lane; ends with gsel and theta in shared memory for warp m.
-__device__ __forceinline__ void merge_rank_groups(const float* sv, const int* si, int m, int h, int G,
+// the groups, one per lane; ends with gsel and theta in shared memory for warp m. The heads
+// are read from the lists gv/gi [G][16] in global memory (through L2), so that the fused
+// kernel ranks them while the lists' bulk copy to shared memory is still in flight.
+__device__ __forceinline__ void merge_rank_groups(const float* gv, const int* gi, int m, int h, int G,
                                                   MergeSmem& ms) {
   const int lane = threadIdx.x & 31;
   int lg = 0;
@@ -279,7 +281,7 @@ __device__ __forceinline__ void merge_rank_groups(const float* sv, const int* si
     for (int d = 0; d < gs; ++d) {
       const int j = (g << lg) + d;
       if (j < G) {
-        const unsigned long long x = merge_key(sv[j * kK], si[j * kK], j * kK);
+        const unsigned long long x = merge_key(__ldcg(gv + j * kK), __ldcg(gi + j * kK), j * kK);
         k = x > k ? x : k;
       }
     }
@@ -775,43 +777,6 @@ __device__ void backward_messages_block(const float* S, int P, float inv_T, floa
   }
 }
 
-// Greedy traversal by the whole block: the best successor of every (position, predecessor)
-// pair, best[p][a] = argmax_c S_p(a, c) (value desc, id asc; candidate 0 when no score is
-// orderable), one pair per thread into `best`, then thread 0 walks x_t = best[t][x_{t-1}]
-// from the last verified token (predecessor 0). Writes path_tok[P] (shared); returns the
-// path score in thread 0. Contains block barriers.
-__device__ float path_greedy_block(const float* S, const int* ids, int P, int* path_tok,
-                                   unsigned char* best) {
-  for (int x = threadIdx.x; x < P * kK; x += blockDim.x) {
-    const int p = x >> 4;
-    const float* row = S + x * kK;  // S_p(a, .), a = x % 16
-    unsigned long long bk = 0ull;
-    int bc = 0;
-#pragma unroll
-    for (int c = 0; c < kK; ++c) {
-      const unsigned long long k = pack_key(row[c], ids[p * kK + c]);
-      if (k > bk) {
-        bk = k;
-        bc = c;
-      }
-    }
-    best[x] = static_cast<unsigned char>((bk >> 32) == 0ull ? 0 : bc);
-  }
-  __syncthreads();
-  float total = 0.f;
-  if (threadIdx.x == 0) {
-    int a = 0;
-    for (int p = 0; p < P; ++p) {
-      const int c = best[p * kK + a];
-      total += S[(p * kK + a) * kK + c];
-      path_tok[p] = ids[p * kK + c];
-      a = c;
-    }
-  }
-  __syncthreads();
-  return total;
-}
-
 // One warp; S [P][16][16], ids [P][16] and delta [16] in shared memory. Writes
 // path_tok[P] (shared) and returns the path score in every lane.
 __device__ float path_warp(const float* S, const int* ids, int P, int mode, int* path_tok,
@@ -1244,13 +1209,22 @@ __device__ __forceinline__ float pair_scores(const TailLaunch& a, const TailSmem
                       sm.g, sm.cand_U, sm.S_all, pair);
 }
 
+// The greedy traversal: path mode 0, and mode 2 (the sampled traversal) at T = 0.
+__device__ __forceinline__ bool greedy_path(const TailLaunch& a) {
+  return a.path_mode == 0 || (a.path_mode == 2 && !(a.T > 0.f));
+}
+
 // Path and verification of request b, run by the block that completes it. The scores and
 // candidates of every position are read back from global memory in one round trip.
 __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
   const int P = a.L - 1;
+  const bool greedy = greedy_path(a);
+  // the greedy traversal needs only the position blocks' successor table (in place of S_all)
   const Seg seg[3] = {
-      {reinterpret_cast<const uint4*>(a.S + static_cast<size_t>(b) * P * kK * kK),
-       reinterpret_cast<uint4*>(sm.S_all), P * kK * kK / 4},
+      greedy ? Seg{reinterpret_cast<const uint4*>(a.succ + static_cast<size_t>(b) * P * kK),
+                   reinterpret_cast<uint4*>(sm.S_all), P * kK / 2}
+             : Seg{reinterpret_cast<const uint4*>(a.S + static_cast<size_t>(b) * P * kK * kK),
+                   reinterpret_cast<uint4*>(sm.S_all), P * kK * kK / 4},
       {reinterpret_cast<const uint4*>(a.cand_ids + static_cast<size_t>(b) * P * kK),
        reinterpret_cast<uint4*>(sm.ids_all), P * kK / 4},
       {reinterpret_cast<const uint4*>(a.rstat + static_cast<size_t>(b) * a.L * 4),
@@ -1262,11 +1236,21 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
   // traversal with backward messages), verified against its own conditionals; at T = 0 it
   // is Viterbi, its T -> 0 limit.
   const bool sampled = (a.path_mode == 2 || a.path_mode == 3) && a.T > 0.f;
-  const bool viterbi = a.path_mode == 1 || (a.path_mode == 3 && !sampled);
-  if (!sampled && !viterbi) {  // greedy (mode 2 at T = 0 included)
-    const float score = path_greedy_block(sm.S_all, sm.ids_all, P, sm.path_tok, sm.bp);
+  if (greedy) {  // (mode 2 at T = 0 included): a walk of P table lookups from predecessor 0
+    if (threadIdx.x == 0) {
+      const int2* succ = reinterpret_cast<const int2*>(sm.S_all);
+      float total = 0.f;
+      int pa = 0;
+      for (int p = 0; p < P; ++p) {
+        const int2 e = succ[p * kK + pa];
+        total += __int_as_float(e.y);
+        sm.path_tok[p] = sm.ids_all[p * kK + e.x];
+        pa = e.x;
+      }
+      if (a.path_score) a.path_score[b] = total;
+    }
+    __syncthreads();
     if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
-    if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
   } else if (sampled) {
     const float inv_T = 1.0f / a.T;
     if (a.path_mode == 3) backward_messages_block(sm.S_all, P, inv_T, sm.logb);
@@ -1323,16 +1307,16 @@ __global__ void __launch_bounds__(kTailThreads, 2) k_tail_fused(const __grid_con
     }
   }
   if (warp < 4) {
-    // a wait that runs out leaves the error word set; the block runs on (every later index
-    // is bounds-checked) and the host reads DFS_ERR_TIMEOUT
-    mbar_wait_bounded(smem_u32(sm.bar), 0, a.err, sm.abort);
     // set 0 (warps 0 and 2): the candidates of position t, then warp 0 gathers their B rows;
     // set 1 (warps 1 and 3): the candidates of position t-1 (the predecessors), then warp 1
     // gathers their A rows scaled by the gate (at position 1 the predecessor is the last
-    // verified token)
+    // verified token). The group heads are ranked from L2 while the bulk copies land.
     const int m = warp & 1;
     if (m < nm)
-      merge_rank_groups(m ? sm.lv_prev : sm.lv_cur, m ? sm.li_prev : sm.li_cur, m, warp >> 1, a.G, *sm.ms);
+      merge_rank_groups(a.part_val + (rc - m) * lst, a.part_idx + (rc - m) * lst, m, warp >> 1, a.G, *sm.ms);
+    // a wait that runs out leaves the error word set; the block runs on (every later index
+    // is bounds-checked) and the host reads DFS_ERR_TIMEOUT
+    mbar_wait_bounded(smem_u32(sm.bar), 0, a.err, sm.abort);
     if (warp < 2) {
       int c = 0;
       if (m < nm)
@@ -1364,6 +1348,53 @@ __global__ void __launch_bounds__(kTailThreads, 2) k_tail_fused(const __grid_con
   int pair;
   const float s = pair_scores(a, sm, mma, pair);
   a.S[(static_cast<size_t>(b) * P + (t - 1)) * kK * kK + pair] = s;
+  if (greedy_path(a)) {
+    // the greedy traversal's table for this position: each predecessor's best successor
+    // (score desc, id asc; the same choice as path_warp's greedy steps), for the last block's walk
+    const size_t o = (static_cast<size_t>(b) * P + (t - 1)) * kK;
+    if (mma) {
+      // pair = tid: half-warp a holds row a, lane c its pair (a, c); a shuffle argmax
+      const int c = threadIdx.x & 15;
+      unsigned long long bk = pack_key(s, sm.cand_id[c]);
+      int bc = c;
+      float bv = s;
+#pragma unroll
+      for (int d = 8; d > 0; d >>= 1) {
+        const unsigned long long ok = __shfl_xor_sync(0xffffffffu, bk, d);
+        const int oc = __shfl_xor_sync(0xffffffffu, bc, d);
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+        if (ok > bk || (ok == bk && oc < bc)) {
+          bk = ok;
+          bc = oc;
+          bv = ov;
+        }
+      }
+      const float s0 = __shfl_sync(0xffffffffu, s, threadIdx.x & 16);  // the row's first pair
+      if ((bk >> 32) == 0ull) {  // no candidate ranks above the empty key: the first one
+        bc = 0;
+        bv = s0;
+      }
+      if (c == 0) a.succ[o + (threadIdx.x >> 4)] = make_int2(bc, __float_as_int(bv));
+    } else {
+      sm.qprop[pair] = s;  // free in the position blocks
+      __syncthreads();
+      if (threadIdx.x < kK) {
+        const float* row = sm.qprop + threadIdx.x * kK;
+        unsigned long long bk = 0ull;
+        int bc = 0;
+#pragma unroll
+        for (int c = 0; c < kK; ++c) {
+          const unsigned long long k = pack_key(row[c], sm.cand_id[c]);
+          if (k > bk) {
+            bk = k;
+            bc = c;
+          }
+        }
+        if ((bk >> 32) == 0ull) bc = 0;
+        a.succ[o + threadIdx.x] = make_int2(bc, __float_as_int(row[bc]));
+      }
+    }
+  }
   // hand-off: the block's writes (candidates, pair scores, row statistics) are ordered before
   // thread 0's device-scope release by the barrier; the last block's acquire, then its
   // barrier, orders the other blocks' writes before its reads
@@ -1399,7 +1430,8 @@ __global__ void __launch_bounds__(kTailThreads) k_merge(const __grid_constant__ 
   __syncthreads();
   if (threadIdx.x < 128) {
     const int warp = threadIdx.x >> 5;
-    if (warp == 0 || warp == 2) merge_rank_groups(sm.lv_cur, sm.li_cur, 0, warp >> 1, a.G, *sm.ms);
+    if (warp == 0 || warp == 2)
+      merge_rank_groups(a.part_val + rc * lst, a.part_idx + rc * lst, 0, warp >> 1, a.G, *sm.ms);
     if (warp == 0) {
       const int c = merge_candidates_warp(sm.lv_cur, sm.li_cur, 0, a.G, *sm.ms, sm.cand_U, sm.cand_id);
       if (threadIdx.x == 0) sm.ms->ncand[0] = c;
