@@ -51,7 +51,8 @@ struct Layout {
   size_t cand_ids, cand_U, S, path;
   size_t logits;
   size_t hq, h_scale;  // E4M3 LM head: quantised rows and their scales
-  size_t rstat;        // fused tail: target-row statistics [B*L][4]
+  size_t rstat;        // fused tail: target-row statistics and uniforms [B*L][8]
+  size_t zc;           // fused tail at T > 0: the candidates' target logits [B][L-1][16]
   size_t succ;         // fused tail, greedy path: best successors [B][L-1][16] (int2)
   size_t total;
   int G, nchunk;
@@ -99,7 +100,8 @@ bool make_layout(const dfs_dims& d, Layout* L) {
   L->logits = take(d.dtype == DFS_FP32 ? 4 * rows * d.V : 0);
   L->hq = take(d.dtype == DFS_BF16 ? rows * static_cast<size_t>(d.d) : 0);
   L->h_scale = take(4 * rows);
-  L->rstat = take(16 * rows);
+  L->rstat = take(32 * rows);
+  L->zc = take(4 * d.B * P * kK);
   L->succ = take(8 * d.B * P * kK);
   L->total = off;
   return true;
@@ -170,6 +172,7 @@ dfs::TailLaunch tail_args(const dfs_dims& d, const Layout& L, void* ws) {
   t.counters = at<int>(ws, L.counters);
   t.err = at<int>(ws, L.err);
   t.rstat = at<float>(ws, L.rstat);
+  t.zc = at<float>(ws, L.zc);
   t.succ = at<int2>(ws, L.succ);
   return t;
 }

@@ -161,8 +161,11 @@ struct TailLaunch {
   int* accept_len;           // [B]
   int* counters;             // [B]
   int* err;
-  float* rstat;              // fused tail: [B*L][4] target-row statistics (max, argmax bits,
-                             // log-sum-exp), published by the position blocks
+  float* rstat;              // fused tail: [B*L][8] target-row statistics (max, argmax bits,
+                             // log-sum-exp) and, at T > 0, the row's acceptance and redraw
+                             // uniforms, published by the position blocks
+  float* zc;                 // fused tail at T > 0: [B][L-1][16] each candidate's target logit
+                             // in its verifying row (-inf outside the vocabulary)
   int2* succ;                // fused tail, greedy path: [B][L-1][16] each predecessor's best
                              // successor (candidate index, score bits), from the position blocks
 };

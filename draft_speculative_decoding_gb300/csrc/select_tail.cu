@@ -780,7 +780,7 @@ __device__ void backward_messages_block(const float* S, int P, float inv_T, floa
 // One warp; S [P][16][16], ids [P][16] and delta [16] in shared memory. Writes
 // path_tok[P] (shared) and returns the path score in every lane.
 __device__ float path_warp(const float* S, const int* ids, int P, int mode, int* path_tok,
-                           unsigned char* bp, float* delta) {
+                           unsigned char* bp, float* delta, int* pidx = nullptr) {
   const int lane = threadIdx.x & 31;
   const bool act = lane < kK;
   if (mode == 0) {
@@ -793,7 +793,10 @@ __device__ float path_warp(const float* S, const int* ids, int P, int mode, int*
       int c = warp_best_lane(act, v, act ? ids[p * kK + lane] : kIntMax);
       c = c < 0 ? 0 : c;  // no orderable score at all (NaN row): take candidate 0
       total += __shfl_sync(0xffffffffu, v, c);
-      if (lane == 0) path_tok[p] = ids[p * kK + c];
+      if (lane == 0) {
+        path_tok[p] = ids[p * kK + c];
+        if (pidx) pidx[p] = c;
+      }
       a = c;
     }
     __syncwarp();
@@ -834,6 +837,7 @@ __device__ float path_warp(const float* S, const int* ids, int P, int mode, int*
     int cur = c;
     for (int p = P - 1; p >= 0; --p) {
       path_tok[p] = ids[p * kK + cur];
+      if (pidx) pidx[p] = cur;
       if (p > 0) cur = bp[p * kK + cur];
     }
   }
@@ -872,20 +876,33 @@ struct VerifySmem {
 // and a candidate's weight is scaled by max(0, 1 - q/p). Without one the proposal is the
 // path itself (q = 1 on x_t).
 // Statistics of target row `row` (max, argmax, log of the sum of exp), by one warp.
+// The statistics of target row `row` (b = row / L, n = row % L) for the request's last block:
+// dst[0..2] = max, argmax bits, log-sum-exp; at T > 0 also dst[3] = the acceptance uniform of
+// the draft the row verifies (n < L - 1) and dst[4] = the row's redraw uniform (both at
+// counter position n + 1), so that the last block draws no Philox numbers itself.
 __device__ void row_stat_publish(const TailLaunch& a, int row, float* dst) {
   const RowStat st = row_stat_warp(a, row);
   if ((threadIdx.x & 31) == 0) {
     dst[0] = st.m;
     dst[1] = __int_as_float(st.i);
     dst[2] = a.T > 0.f ? logf(st.s) : 0.f;
+    if (a.T > 0.f) {
+      const int b = row / a.L, n = row - b * a.L;
+      dst[3] = n < a.L - 1 ? uniform_accept(a.seed, b, n + 1) : 0.f;
+      dst[4] = uniform_redraw(a.seed, b, n + 1);
+    }
   }
 }
 
 // stats != nullptr: the request's L row statistics were published (rstat layout) and staged
 // into shared memory already; otherwise they are computed here.
+// zc (with stats): the target logit of every candidate in its verifying row, [P][16], and
+// path_pidx [P] the path's candidate index at each position; then no target logit is read
+// from Z here except the redraw's chunk.
 __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, VerifySmem& vs,
                              const float* prop_q = nullptr, const int* prop_cand = nullptr,
-                             const int* prop_pidx = nullptr, const float* stats = nullptr) {
+                             const int* prop_pidx = nullptr, const float* stats = nullptr,
+                             const float* zc = nullptr, const int* path_pidx = nullptr) {
   const int L = a.L, P = L - 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool soft = a.T > 0.f;
@@ -893,9 +910,9 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
   const int is_bf16 = a.zdtype == 0;
   if (stats != nullptr) {
     if (threadIdx.x < L) {
-      vs.rm[threadIdx.x] = stats[threadIdx.x * 4];
-      vs.ry[threadIdx.x] = __float_as_int(stats[threadIdx.x * 4 + 1]);
-      vs.rl[threadIdx.x] = stats[threadIdx.x * 4 + 2];
+      vs.rm[threadIdx.x] = stats[threadIdx.x * 8];
+      vs.ry[threadIdx.x] = __float_as_int(stats[threadIdx.x * 8 + 1]);
+      vs.rl[threadIdx.x] = stats[threadIdx.x * 8 + 2];
     }
   } else {
     for (int i = warp; i < L; i += blockDim.x >> 5) {
@@ -917,15 +934,17 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
         ok = x == vs.ry[lane];
       } else {
         const bool in_vocab = x >= 0 && x < a.V;  // an out-of-vocabulary proposal has p = 0
-        const float z = in_vocab ? load1(a.Z, is_bf16, (static_cast<size_t>(b) * L + lane) * a.V + x)
-                                 : -INFINITY;
+        const float z = zc != nullptr ? zc[lane * kK + path_pidx[lane]]  // -inf outside V
+                                      : in_vocab ? load1(a.Z, is_bf16, (static_cast<size_t>(b) * L + lane) * a.V + x)
+                                                 : -INFINITY;
         vs.zx[lane] = z;
         const float p = expf((z - vs.rm[lane]) * inv_T - vs.rl[lane]);
         const float qx = prop_q ? prop_q[lane * kK + prop_pidx[lane]] : 1.0f;
-        ok = uniform_accept(a.seed, b, lane + 1) < p / qx;
+        const float ua = stats != nullptr ? stats[lane * 8 + 3] : uniform_accept(a.seed, b, lane + 1);
+        ok = ua < p / qx;
       }
     }
-    if (soft && lane < L) vs.ur[lane] = uniform_redraw(a.seed, b, lane + 1);
+    if (soft && lane < L) vs.ur[lane] = stats != nullptr ? stats[lane * 8 + 4] : uniform_redraw(a.seed, b, lane + 1);
     const unsigned fail = __ballot_sync(0xffffffffu, lane < P && !ok);
     const int n = fail ? __ffs(fail) - 1 : P;  // accepted drafts
     if (lane < L && (lane != n || !soft))
@@ -955,7 +974,7 @@ __device__ void verify_block(const TailLaunch& a, int b, const int* path_tok, Ve
       ck = prop_cand[n * kK + lane];
       const float qk = prop_q[n * kK + lane];
       if (ck >= 0 && ck < a.V) {
-        const float zk = load1(a.Z, is_bf16, grow * a.V + ck);
+        const float zk = zc != nullptr ? zc[n * kK + lane] : load1(a.Z, is_bf16, grow * a.V + ck);
         const float pk = expf((zk - M) * inv_T - vs.rl[n]);
         take = fminf(pk, qk) * expf(vs.rl[n]);
         cfac = qk < pk ? 1.f - qk / pk : 0.f;
@@ -1122,7 +1141,8 @@ struct TailSmem {
   float* upath;                  // [P] path-draw uniforms
   float* logb;                   // joint path draw: [P][16] backward messages (log beta)
   int* pidx;                     // [16] drawn candidate indices
-  float* rstat;                  // [L][4] the request's published row statistics
+  float* rstat;                  // [L][8] the request's published row statistics and uniforms
+  float* zc_all;                 // [P][16] the candidates' target logits (T > 0)
   MergeSmem* ms;                 // top-16 merge scratch
   uint64_t* bar;                 // bulk-copy completion: [0] the staged lists and gate row,
                                  // [1] set 0's B rows, [2] set 1's A rows (tensor-core path)
@@ -1141,7 +1161,7 @@ __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16;
-  n += kMaxL * 16 + 16;
+  n += kMaxL * 32 + 16 + kMaxL * kK * 4 + 16;
   n += sizeof(MergeSmem) + 16;
   n += 48;
   return n + 256;
@@ -1179,7 +1199,8 @@ __device__ TailSmem carve(uint8_t* base, int G, int r) {
   s.sdraw = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
   s.upath = reinterpret_cast<float*>(take(kMaxL * 4));
   s.logb = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
-  s.rstat = reinterpret_cast<float*>(take(kMaxL * 16));
+  s.rstat = reinterpret_cast<float*>(take(kMaxL * 32));
+  s.zc_all = reinterpret_cast<float*>(take(kMaxL * kK * 4));
   s.ms = reinterpret_cast<MergeSmem*>(take(sizeof(MergeSmem)));
   s.bar = reinterpret_cast<uint64_t*>(take(32));
   s.abort = reinterpret_cast<int*>(take(16));
@@ -1220,16 +1241,19 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
   const int P = a.L - 1;
   const bool greedy = greedy_path(a);
   // the greedy traversal needs only the position blocks' successor table (in place of S_all)
-  const Seg seg[3] = {
+  const Seg seg[4] = {
       greedy ? Seg{reinterpret_cast<const uint4*>(a.succ + static_cast<size_t>(b) * P * kK),
                    reinterpret_cast<uint4*>(sm.S_all), P * kK / 2}
              : Seg{reinterpret_cast<const uint4*>(a.S + static_cast<size_t>(b) * P * kK * kK),
                    reinterpret_cast<uint4*>(sm.S_all), P * kK * kK / 4},
       {reinterpret_cast<const uint4*>(a.cand_ids + static_cast<size_t>(b) * P * kK),
        reinterpret_cast<uint4*>(sm.ids_all), P * kK / 4},
-      {reinterpret_cast<const uint4*>(a.rstat + static_cast<size_t>(b) * a.L * 4),
-       reinterpret_cast<uint4*>(sm.rstat), a.L}};
-  staged_copy<5, 3>(seg);
+      {reinterpret_cast<const uint4*>(a.rstat + static_cast<size_t>(b) * a.L * 8),
+       reinterpret_cast<uint4*>(sm.rstat), 2 * a.L},
+      // at T > 0 the candidates' target logits, published by the position blocks
+      {reinterpret_cast<const uint4*>(a.zc + static_cast<size_t>(b) * P * kK),
+       reinterpret_cast<uint4*>(sm.zc_all), a.T > 0.f ? P * kK / 4 : 0}};
+  staged_copy<5, 4>(seg);
   __syncthreads();
   // path mode 2 at T > 0: the sampled traversal, verified against its own proposal; at
   // T = 0 it is the greedy traversal. Mode 3 at T > 0: the joint path draw (the same
@@ -1245,6 +1269,7 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
         const int2 e = succ[p * kK + pa];
         total += __int_as_float(e.y);
         sm.path_tok[p] = sm.ids_all[p * kK + e.x];
+        sm.pidx[p] = e.x;
         pa = e.x;
       }
       if (a.path_score) a.path_score[b] = total;
@@ -1260,15 +1285,15 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
     if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
     if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
   } else if (threadIdx.x < 32) {
-    const float score = path_warp(sm.S_all, sm.ids_all, P, 1, sm.path_tok, sm.bp, sm.delta);
+    const float score = path_warp(sm.S_all, sm.ids_all, P, 1, sm.path_tok, sm.bp, sm.delta, sm.pidx);
     if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
     if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
   }
   __syncthreads();
   if (sampled)
-    verify_block(a, b, sm.path_tok, *sm.vs, sm.qprop, sm.ids_all, sm.pidx, sm.rstat);
+    verify_block(a, b, sm.path_tok, *sm.vs, sm.qprop, sm.ids_all, sm.pidx, sm.rstat, sm.zc_all, sm.pidx);
   else
-    verify_block(a, b, sm.path_tok, *sm.vs, nullptr, nullptr, nullptr, sm.rstat);
+    verify_block(a, b, sm.path_tok, *sm.vs, nullptr, nullptr, nullptr, sm.rstat, sm.zc_all, sm.pidx);
 }
 
 // ------------------------------------------------------------------ kernels
@@ -1336,8 +1361,8 @@ __global__ void __launch_bounds__(kTailThreads, 2) k_tail_fused(const __grid_con
   } else {
     // meanwhile, warps 6 and 7: the statistics of target row t-1 (and of the bonus row L-1
     // for the last position), published for the request's last block
-    if (warp == 6) row_stat_publish(a, b * L + t - 1, a.rstat + (static_cast<size_t>(b) * L + t - 1) * 4);
-    if (warp == 7 && t == P) row_stat_publish(a, b * L + L - 1, a.rstat + (static_cast<size_t>(b) * L + L - 1) * 4);
+    if (warp == 6) row_stat_publish(a, b * L + t - 1, a.rstat + (static_cast<size_t>(b) * L + t - 1) * 8);
+    if (warp == 7 && t == P) row_stat_publish(a, b * L + L - 1, a.rstat + (static_cast<size_t>(b) * L + L - 1) * 8);
   }
   __syncthreads();
   if (threadIdx.x < kK) {
@@ -1345,9 +1370,21 @@ __global__ void __launch_bounds__(kTailThreads, 2) k_tail_fused(const __grid_con
     a.cand_ids[o] = sm.cand_id[threadIdx.x];
     a.cand_U[o] = sm.cand_U[threadIdx.x];
   }
+  // at T > 0, the target logit of each candidate in row t-1 (the row that verifies position
+  // t), for the last block's acceptance tests and residuals: loaded now, stored after the
+  // pair scores so that the load's latency hides behind them
+  const bool soft = a.T > 0.f;
+  float zcand = -INFINITY;
+  if (soft && warp == 5 && (threadIdx.x & 31) < kK) {
+    const int c = sm.cand_id[threadIdx.x & 31];
+    if (c >= 0 && c < a.V)
+      zcand = load1(a.Z, a.zdtype == 0, (static_cast<size_t>(b) * L + t - 1) * a.V + c);
+  }
   int pair;
   const float s = pair_scores(a, sm, mma, pair);
   a.S[(static_cast<size_t>(b) * P + (t - 1)) * kK * kK + pair] = s;
+  if (soft && warp == 5 && (threadIdx.x & 31) < kK)
+    a.zc[(static_cast<size_t>(b) * P + (t - 1)) * kK + (threadIdx.x & 31)] = zcand;
   if (greedy_path(a)) {
     // the greedy traversal's table for this position: each predecessor's best successor
     // (score desc, id asc; the same choice as path_warp's greedy steps), for the last block's walk
