@@ -70,8 +70,18 @@ int check_dims(const dfs_dims* d) {
   return DFS_OK;
 }
 
+// Test hook, read on each call (the workspace layout follows it): DFS_DEBUG_LMHEAD_CTAS = an
+// even number from 2 to the SM count runs the persistent LM-head kernels on that many CTAs,
+// so that rows get fewer partial lists for the tail to merge; unset or out of range, one CTA
+// per SM.
+int lmhead_ctas(int sms) {
+  const char* s = std::getenv("DFS_DEBUG_LMHEAD_CTAS");
+  const int v = s ? std::atoi(s) : 0;
+  return (v >= 2 && v <= sms && v % 2 == 0) ? v : sms;
+}
+
 bool make_layout(const dfs_dims& d, Layout* L) {
-  const int sms = device_sm_count();
+  const int sms = lmhead_ctas(device_sm_count());
   if (sms <= 0) return false;
   // one list per CTA of the persistent LM-head grid: even, so CTA pairs tile it
   L->G = d.dtype == DFS_BF16 ? ((sms < dfs::kMaxLists ? sms : dfs::kMaxLists) / 2) * 2 : 1;

@@ -104,6 +104,34 @@ def test_fused_small(lib, orc, spec, mode, T):
     _invariants(g, spec, npd, T)
 
 
+# Fewer LM-head CTAs, so fewer partial lists per row: the tail's merge takes groups of 1, 2 and
+# 4 lists, fewer than 16 groups (every entry a candidate) and the exact merge past 64
+# candidates. Up to 128 rows the list count is the CTA count, above it half.
+LIST_COUNTS = [
+    (SMALL[1], 4),    # 4 lists: fewer than 16 groups, 64 candidates (the buffer's size)
+    (SMALL[1], 6),    # 6 lists: 96 candidates, the exact merge
+    (SMALL[1], 24),   # groups of one list
+    (SMALL[1], 100),  # groups of four lists
+    (SMALL[2], 16),   # CTA pairs: 8 lists, the exact merge
+    (SMALL[2], 60),   # 30 lists, groups of one
+    (SMALL[2], 120),  # 60 lists, groups of two
+]
+
+
+@pytest.mark.parametrize("spec,ctas", LIST_COUNTS, ids=lambda x: getattr(x, "name", str(x)))
+@pytest.mark.parametrize("mode,T", [(binding.DFS_PATH_GREEDY, 0.0), (binding.DFS_PATH_SAMPLE, 0.8)])
+def test_fused_merge_list_counts(lib, orc, spec, ctas, mode, T, monkeypatch):
+    monkeypatch.setenv("DFS_DEBUG_LMHEAD_CTAS", str(ctas))
+    data = wl.generate(spec, "cuda")
+    npd = np_inputs(data)
+    g = _run(data, spec, mode, T, seed=spec.seed + 200)
+    o = orc.select_verify(npd["h"], npd["W"], npd["Wg"], npd["A"], npd["Bt"], npd["x0"], npd["Z"],
+                          path_mode=mode, temperature=T, seed=spec.seed + 200)
+    diverged = _compare(g, o, spec, list(range(spec.B)), T)
+    assert diverged <= max(1, spec.B // 8)
+    _invariants(g, spec, npd, T)
+
+
 def test_fused_is_deterministic(lib):
     spec = SMALL[2]
     data = wl.generate(spec, "cuda")
