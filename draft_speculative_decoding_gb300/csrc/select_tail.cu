@@ -1261,21 +1261,35 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
   // is Viterbi, its T -> 0 limit.
   const bool sampled = (a.path_mode == 2 || a.path_mode == 3) && a.T > 0.f;
   if (greedy) {  // (mode 2 at T = 0 included): a walk of P table lookups from predecessor 0
-    if (threadIdx.x == 0) {
-      const int2* succ = reinterpret_cast<const int2*>(sm.S_all);
-      float total = 0.f;
-      int pa = 0;
-      for (int p = 0; p < P; ++p) {
-        const int2 e = succ[p * kK + pa];
-        total += __int_as_float(e.y);
-        sm.path_tok[p] = sm.ids_all[p * kK + e.x];
-        sm.pidx[p] = e.x;
-        pa = e.x;
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      if (lane == 0) {
+        const int2* succ = reinterpret_cast<const int2*>(sm.S_all);
+        float total = 0.f;
+        int pa = 0;
+        for (int p = 0; p < P; ++p) {
+          const int2 e = succ[p * kK + pa];
+          total += __int_as_float(e.y);
+          sm.path_tok[p] = sm.ids_all[p * kK + e.x];
+          sm.pidx[p] = e.x;
+          pa = e.x;
+        }
+        if (a.path_score) a.path_score[b] = total;
       }
-      if (a.path_score) a.path_score[b] = total;
+      __syncwarp();
+      if (lane < P) a.path[static_cast<size_t>(b) * P + lane] = sm.path_tok[lane];
+      if (!(a.T > 0.f)) {
+        // greedy verification, by this warp alone: draft p is accepted while it is the argmax
+        // of target row p (the position blocks published the rows' statistics)
+        const int ry = lane < a.L ? __float_as_int(sm.rstat[lane * 8 + 1]) : 0;
+        const unsigned fail = __ballot_sync(0xffffffffu, lane < P && sm.path_tok[lane] != ry);
+        const int n = fail ? __ffs(fail) - 1 : P;  // accepted drafts
+        int* out = a.out_tokens + static_cast<size_t>(b) * a.L;
+        if (lane < a.L) out[lane] = lane < n ? sm.path_tok[lane] : (lane == n ? ry : -1);
+        if (lane == 0) a.accept_len[b] = n + 1;
+      }
     }
-    __syncthreads();
-    if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
+    if (!(a.T > 0.f)) return;  // the request is done
   } else if (sampled) {
     const float inv_T = 1.0f / a.T;
     if (a.path_mode == 3) backward_messages_block(sm.S_all, P, inv_T, sm.logb);
