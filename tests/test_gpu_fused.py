@@ -35,6 +35,10 @@ SMALL = [
     wl.TINY.with_(name="vt_32x9", dtype="bf16", B=32, L=9, V=3000, d=128, r=256, seed=39,
                   zipf=True),
     wl.TINY.with_(name="vt_64x5", dtype="bf16", B=64, L=5, V=2600, d=128, r=64, seed=40),
+    # one draft position (every tail block merges one set; a one-step walk); and a rank that
+    # is not a multiple of 16, so the tail's pair scores take the SIMT path on bf16 tables
+    wl.TINY.with_(name="fused_L2", dtype="bf16", B=8, L=2, V=3000, d=128, r=32, seed=41),
+    wl.TINY.with_(name="fused_r24", dtype="bf16", B=6, L=5, V=2600, d=128, r=24, seed=42),
 ]
 
 
