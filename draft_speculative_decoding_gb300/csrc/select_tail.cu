@@ -278,11 +278,24 @@ __device__ __forceinline__ void merge_rank_groups(const float* gv, const int* gi
   const bool valid = lane < half && g < ng;
   unsigned long long k = 0;  // zero (below every key) past the last group
   if (valid) {
-    for (int d = 0; d < gs; ++d) {
-      const int j = (g << lg) + d;
-      if (j < G) {
-        const unsigned long long x = merge_key(__ldcg(gv + j * kK), __ldcg(gi + j * kK), j * kK);
-        k = x > k ? x : k;
+    // four heads' loads in flight at once (one L2 round trip for groups of up to four lists)
+    for (int d0 = 0; d0 < gs; d0 += 4) {
+      float hv[4];
+      int hi[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = (g << lg) + d0 + e;
+        const bool in = d0 + e < gs && j < G;
+        hv[e] = in ? __ldcg(gv + j * kK) : 0.f;
+        hi[e] = in ? __ldcg(gi + j * kK) : 0;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = (g << lg) + d0 + e;
+        if (d0 + e < gs && j < G) {
+          const unsigned long long x = merge_key(hv[e], hi[e], j * kK);
+          k = x > k ? x : k;
+        }
       }
     }
   }
