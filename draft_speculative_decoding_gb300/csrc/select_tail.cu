@@ -790,71 +790,75 @@ __device__ void backward_messages_block(const float* S, int P, float inv_T, floa
   }
 }
 
-// One warp; S [P][16][16], ids [P][16] and delta [16] in shared memory. Writes
-// path_tok[P] (shared) and returns the path score in every lane.
-__device__ float path_warp(const float* S, const int* ids, int P, int mode, int* path_tok,
-                           unsigned char* bp, float* delta, int* pidx = nullptr) {
+// Greedy traversal by one warp (dfs_path_select): x_t = argmax_c S_t(x_{t-1}, c) by (score
+// desc, id asc). S [P][16][16] and ids [P][16] in shared memory; writes path_tok[P] (shared)
+// and returns the path score in every lane.
+__device__ float path_greedy_warp(const float* S, const int* ids, int P, int* path_tok) {
   const int lane = threadIdx.x & 31;
   const bool act = lane < kK;
-  if (mode == 0) {
-    // greedy: x_t = argmax_c S_t(x_{t-1}, c)
-    int a = 0;
-    float total = 0.f;
+  int a = 0;
+  float total = 0.f;
 #pragma unroll 1
-    for (int p = 0; p < P; ++p) {
-      const float v = act ? S[(p * kK + a) * kK + lane] : -INFINITY;
-      int c = warp_best_lane(act, v, act ? ids[p * kK + lane] : kIntMax);
-      c = c < 0 ? 0 : c;  // no orderable score at all (NaN row): take candidate 0
-      total += __shfl_sync(0xffffffffu, v, c);
-      if (lane == 0) {
-        path_tok[p] = ids[p * kK + c];
-        if (pidx) pidx[p] = c;
-      }
-      a = c;
-    }
-    __syncwarp();
-    return total;
+  for (int p = 0; p < P; ++p) {
+    const float v = act ? S[(p * kK + a) * kK + lane] : -INFINITY;
+    int c = warp_best_lane(act, v, act ? ids[p * kK + lane] : kIntMax);
+    c = c < 0 ? 0 : c;  // no orderable score at all (NaN row): take candidate 0
+    total += __shfl_sync(0xffffffffu, v, c);
+    if (lane == 0) path_tok[p] = ids[p * kK + c];
+    a = c;
   }
-  // Viterbi: delta_1(c) = S_1(x0, c); delta_t(c) = max_a delta_{t-1}(a) + S_t(a, c)
-  if (act) delta[lane] = S[lane];
   __syncwarp();
+  return total;
+}
+
+// Viterbi by the whole block (256 threads): delta_1(c) = S_1(x0, c), delta_t(c) = max_a
+// delta_{t-1}(a) + S_t(a, c), then the best final candidate (score desc, id asc) and the
+// back-pointers. Thread (c, a) = (tid / 16, tid % 16) forms delta_{t-1}(a) + S_t(a, c), and
+// the 16 threads of c (a half-warp) keep the best by (score desc, predecessor id asc) with a
+// shuffle butterfly; of equal keys the lowest a wins. delta2 [2][16] alternates between
+// positions, so one barrier per position suffices.
+__device__ float path_viterbi_block(const float* S, const int* ids, int P, int* path_tok,
+                                    unsigned char* bp, float* delta2, int* pidx) {
+  const int tid = threadIdx.x, lane = tid & 31, c = tid >> 4, aa = tid & 15;
+  if (tid < kK) delta2[tid] = S[tid];
+  __syncthreads();
 #pragma unroll 1
   for (int p = 1; p < P; ++p) {
-    float bv = -INFINITY;
-    int ba = 0;
-    unsigned long long bk = 0ull;
-    if (act) {
+    const float* dcur = delta2 + ((p - 1) & 1) * kK;
+    float* dnext = delta2 + (p & 1) * kK;
+    const float v = dcur[aa] + S[(p * kK + aa) * kK + c];
+    const unsigned long long k = pack_key(v, ids[(p - 1) * kK + aa]);
+    unsigned long long m = k;
 #pragma unroll
-      for (int aa = 0; aa < kK; ++aa) {
-        const float v = delta[aa] + S[(p * kK + aa) * kK + lane];
-        const unsigned long long k = pack_key(v, ids[(p - 1) * kK + aa]);
-        if (k > bk) {
-          bk = k;
-          bv = v;
-          ba = aa;
-        }
+    for (int off = 8; off > 0; off >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, m, off);
+      m = o > m ? o : m;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, k == m) & (0xffffu << (lane & 16));
+    if (lane == __ffs(hit) - 1) {
+      dnext[c] = v;
+      bp[p * kK + c] = static_cast<unsigned char>(aa);
+    }
+    __syncthreads();
+  }
+  float score = 0.f;
+  if (tid < 32) {
+    const bool act = lane < kK;
+    const float* dl = delta2 + ((P - 1) & 1) * kK;
+    const float v = act ? dl[lane] : -INFINITY;
+    int cb = warp_best_lane(act, v, act ? ids[(P - 1) * kK + lane] : kIntMax);
+    cb = cb < 0 ? 0 : cb;
+    score = __shfl_sync(0xffffffffu, v, cb);
+    if (lane == 0) {
+      int cur = cb;
+      for (int p = P - 1; p >= 0; --p) {
+        path_tok[p] = ids[p * kK + cur];
+        if (pidx) pidx[p] = cur;
+        if (p > 0) cur = bp[p * kK + cur];
       }
     }
     __syncwarp();
-    if (act) {
-      delta[lane] = bv;
-      bp[p * kK + lane] = static_cast<unsigned char>(ba);
-    }
-    __syncwarp();
   }
-  const float v = act ? delta[lane] : -INFINITY;
-  int c = warp_best_lane(act, v, act ? ids[(P - 1) * kK + lane] : kIntMax);
-  c = c < 0 ? 0 : c;
-  const float score = __shfl_sync(0xffffffffu, v, c);
-  if (lane == 0) {
-    int cur = c;
-    for (int p = P - 1; p >= 0; --p) {
-      path_tok[p] = ids[p * kK + cur];
-      if (pidx) pidx[p] = cur;
-      if (p > 0) cur = bp[p * kK + cur];
-    }
-  }
-  __syncwarp();
   return score;
 }
 
@@ -1145,7 +1149,7 @@ struct TailSmem {
   float* P; float* Q;            // [16][r+4]
   float* S_all; int* ids_all;    // last block: [P][16][16], [P][16]
   unsigned char* bp;             // [16][16]
-  float* delta;                  // [16]
+  float* delta;                  // [2][16] Viterbi scores, alternating between positions
   int* path_tok;                 // [16]
   int* flag;
   VerifySmem* vs;
@@ -1169,7 +1173,7 @@ __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
   n += 5 * 80;
   n += 2 * (16 * static_cast<size_t>(r + 4) * 4 + 16);
   n += static_cast<size_t>(kMaxL) * kK * kK * 4 + kMaxL * kK * 4 + 32;
-  n += kMaxL * kK + 16 + 80 + 80 + 16;
+  n += kMaxL * kK + 16 + 144 + 80 + 16;
   n += sizeof(VerifySmem) + 16;
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
@@ -1203,7 +1207,7 @@ __device__ TailSmem carve(uint8_t* base, int G, int r) {
   s.S_all = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * kK * 4));
   s.ids_all = reinterpret_cast<int*>(take(kMaxL * kK * 4));
   s.bp = take(kMaxL * kK);
-  s.delta = reinterpret_cast<float*>(take(64));
+  s.delta = reinterpret_cast<float*>(take(128));
   s.path_tok = reinterpret_cast<int*>(take(64));
   s.flag = reinterpret_cast<int*>(take(16));
   s.vs = reinterpret_cast<VerifySmem*>(take(sizeof(VerifySmem)));
@@ -1311,8 +1315,8 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
                                           a.path_mode == 3 ? sm.logb : nullptr);
     if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
     if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
-  } else if (threadIdx.x < 32) {
-    const float score = path_warp(sm.S_all, sm.ids_all, P, 1, sm.path_tok, sm.bp, sm.delta, sm.pidx);
+  } else {
+    const float score = path_viterbi_block(sm.S_all, sm.ids_all, P, sm.path_tok, sm.bp, sm.delta, sm.pidx);
     if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
     if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
   }
@@ -1414,7 +1418,7 @@ __global__ void __launch_bounds__(kTailThreads, 2) k_tail_fused(const __grid_con
     a.zc[(static_cast<size_t>(b) * P + (t - 1)) * kK + (threadIdx.x & 31)] = zcand;
   if (greedy_path(a)) {
     // the greedy traversal's table for this position: each predecessor's best successor
-    // (score desc, id asc; the same choice as path_warp's greedy steps), for the last block's walk
+    // (score desc, id asc; the same choice as path_greedy_warp's steps), for the last block's walk
     const size_t o = (static_cast<size_t>(b) * P + (t - 1)) * kK;
     if (mma) {
       // pair = tid: half-warp a holds row a, lane c its pair (a, c); a shuffle argmax
@@ -1541,12 +1545,13 @@ __global__ void __launch_bounds__(kTailThreads) k_pair(const __grid_constant__ T
   a.S[(static_cast<size_t>(b) * P + (t - 1)) * kK * kK + pair] = s;
 }
 
-// dfs_path_select: one block per request; four warps stage the scores, one selects.
-__global__ void __launch_bounds__(128) k_path(const __grid_constant__ TailLaunch a) {
+// dfs_path_select: one block per request; the block stages the scores, then one warp walks
+// the greedy path, or the whole block runs Viterbi (the fused tail's code for both).
+__global__ void __launch_bounds__(kTailThreads) k_path(const __grid_constant__ TailLaunch a) {
   __shared__ __align__(16) float S_all[kMaxL * kK * kK];
   __shared__ __align__(16) int ids_all[kMaxL * kK];
   __shared__ unsigned char bp[kMaxL * kK];
-  __shared__ float delta[kK];
+  __shared__ float delta[2 * kK];
   __shared__ int path_tok[kMaxL];
   const int b = blockIdx.x, P = a.L - 1;
   const Seg seg[2] = {
@@ -1554,10 +1559,15 @@ __global__ void __launch_bounds__(128) k_path(const __grid_constant__ TailLaunch
        reinterpret_cast<uint4*>(S_all), P * kK * kK / 4},
       {reinterpret_cast<const uint4*>(a.cand_ids + static_cast<size_t>(b) * P * kK),
        reinterpret_cast<uint4*>(ids_all), P * kK / 4}};
-  staged_copy<8, 2>(seg);  // up to 15 * 68 chunks over 128 threads
+  staged_copy<4, 2>(seg);  // up to 15 * 68 chunks over 256 threads
   __syncthreads();
-  if (threadIdx.x >= 32) return;
-  const float score = path_warp(S_all, ids_all, P, a.path_mode, path_tok, bp, delta);
+  float score;
+  if (a.path_mode == 0) {
+    if (threadIdx.x >= 32) return;
+    score = path_greedy_warp(S_all, ids_all, P, path_tok);
+  } else {
+    score = path_viterbi_block(S_all, ids_all, P, path_tok, bp, delta, nullptr);
+  }
   if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = path_tok[threadIdx.x];
   if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
 }
@@ -1652,7 +1662,7 @@ cudaError_t launch_pair(const TailLaunch& a, cudaStream_t s) {
 }
 
 cudaError_t launch_path(const TailLaunch& a, cudaStream_t s) {
-  k_path<<<a.B, 128, 0, s>>>(a);
+  k_path<<<a.B, kTailThreads, 0, s>>>(a);
   return counted(cudaGetLastError());
 }
 
