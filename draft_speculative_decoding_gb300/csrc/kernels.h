@@ -162,8 +162,8 @@ struct TailLaunch {
   int* counters;             // [B]
   int* err;
   float* rstat;              // fused tail: [B*L][8] target-row statistics (max, argmax bits,
-                             // log-sum-exp) and, at T > 0, the row's acceptance and redraw
-                             // uniforms, published by the position blocks
+                             // log-sum-exp) and, at T > 0, the row's acceptance, redraw and
+                             // (drawn paths) path uniforms, published by the position blocks
   float* zc;                 // fused tail at T > 0: [B][L-1][16] each candidate's target logit
                              // in its verifying row (-inf outside the vocabulary)
   int2* succ;                // fused tail, greedy path: [B][L-1][16] each predecessor's best

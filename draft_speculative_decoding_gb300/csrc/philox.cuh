@@ -35,27 +35,29 @@ __device__ __forceinline__ float u01_from_word(uint64_t w) {
   return static_cast<float>(2u * static_cast<uint32_t>(w >> 41) + 1u) * 0x1p-24f;
 }
 
-// Accept-test uniform of draft position t of request b: counter (0, t, b, 0), word 0.
-__device__ __forceinline__ float uniform_accept(uint64_t seed, int b, int t) {
-  uint64_t c[4] = {0ull, static_cast<uint64_t>(t), static_cast<uint64_t>(b), 0ull};
+// Uniform of Philox stream s at draft position t of request b: counter (0, t, b, s), word 0.
+// Streams: 0 the acceptance tests, 1 the redraws, 3 the path draws.
+__device__ __forceinline__ float uniform_stream(uint64_t seed, int b, int t, uint64_t s) {
+  uint64_t c[4] = {0ull, static_cast<uint64_t>(t), static_cast<uint64_t>(b), s};
   philox4x64_10(c, seed, 0ull);
   return u01_from_word(c[0]);
+}
+
+// Accept-test uniform of draft position t of request b: counter (0, t, b, 0), word 0.
+__device__ __forceinline__ float uniform_accept(uint64_t seed, int b, int t) {
+  return uniform_stream(seed, b, t, 0ull);
 }
 
 // The redraw's one uniform for draft position t of request b (the draw from row t - 1, or
 // from the bonus row when t = L): counter (0, t, b, 1), word 0.
 __device__ __forceinline__ float uniform_redraw(uint64_t seed, int b, int t) {
-  uint64_t c[4] = {0ull, static_cast<uint64_t>(t), static_cast<uint64_t>(b), 1ull};
-  philox4x64_10(c, seed, 0ull);
-  return u01_from_word(c[0]);
+  return uniform_stream(seed, b, t, 1ull);
 }
 
 // Path-draw uniform of the sampled traversal at draft position t of request b: counter
 // (0, t, b, 3), word 0.
 __device__ __forceinline__ float uniform_path(uint64_t seed, int b, int t) {
-  uint64_t c[4] = {0ull, static_cast<uint64_t>(t), static_cast<uint64_t>(b), 3ull};
-  philox4x64_10(c, seed, 0ull);
-  return u01_from_word(c[0]);
+  return uniform_stream(seed, b, t, 3ull);
 }
 
 }  // namespace dfs

@@ -697,20 +697,21 @@ __device__ float pair_dot_block(int r, const float* P, const float* Q, const flo
 // ------------------------------------------------------------------ path
 // Sampled traversal (mode 2) by the whole block: from the last verified token, x_t is drawn
 // from q_t(c) = softmax_c(S_t(x_{t-1}, c) / T) over the 16 candidates by one uniform (Philox
-// stream 3) against the cumulative q in candidate order; if rounding leaves no candidate
-// above it, the last one with mass. With backward messages logb (the joint path draw, mode
-// 3) the weights are S_t(x_{t-1}, c) / T + logb[t][c]. Every (position p, predecessor a)
-// row's q and draw are computed first, one row per thread, the row's q kept in place of its
-// scores; then thread 0 walks from predecessor 0 and the drawn rows' q are copied out.
-// Writes path_tok[P], pidx[P] and q[P][16]; returns the path score in thread 0. Contains
-// block barriers.
-__device__ float path_sample_block(float* S, const int* ids, int P, float inv_T, uint64_t seed,
-                                   int b, int* path_tok, int* pidx, float* q, float* sdraw,
-                                   float* upath, unsigned char* draw,
-                                   const float* logb = nullptr) {
-  if (threadIdx.x < P) upath[threadIdx.x] = uniform_path(seed, b, threadIdx.x + 1);
-  __syncthreads();
-  for (int x = threadIdx.x; x < P * kK; x += blockDim.x) {
+// stream 3, published by the position blocks in the row statistics: upub[p * 8 + 5] for
+// position p + 1) against the cumulative q in candidate order; if rounding leaves no
+// candidate above it, the last one with mass. With backward messages logb (the joint path
+// draw, mode 3) the weights are S_t(x_{t-1}, c) / T + logb[t][c]. Every (position p,
+// predecessor a) row's q and draw are computed first, one row per thread (the rows spread
+// over all eight warps), the row's q kept in place of its scores; then thread 0 walks from
+// predecessor 0 and the drawn rows' q are copied out. Writes path_tok[P], pidx[P] and
+// q[P][16]; returns the path score in thread 0. Contains block barriers.
+__device__ float path_sample_block(float* S, const int* ids, int P, float inv_T, const float* upub,
+                                   int* path_tok, int* pidx, float* q, float* sdraw,
+                                   unsigned char* draw, const float* logb = nullptr) {
+  const int nrow = P * kK;  // at most 240: one pass of the 256 threads
+  const int per_warp = (nrow + kTailThreads / 32 - 1) / (kTailThreads / 32);
+  const int lane = threadIdx.x & 31, x = (threadIdx.x >> 5) * per_warp + lane;
+  if (lane < per_warp && x < nrow) {
     float* row = S + x * kK;
     const float* lb = logb != nullptr ? logb + (x >> 4) * kK : nullptr;
     float v[kK], w[kK];
@@ -728,12 +729,13 @@ __device__ float path_sample_block(float* S, const int* ids, int P, float inv_T,
       e[c] = expf(w[c] - m);
       z += e[c];
     }
-    const float u = upath[x >> 4];
+    const float rz = 1.0f / z;
+    const float u = upub[(x >> 4) * 8 + 5];
     float cum = 0.f, v_pick = v[0], v_last = v[0];
     int pick = -1, last = 0;
 #pragma unroll
     for (int c = 0; c < kK; ++c) {
-      const float qc = e[c] / z;
+      const float qc = e[c] * rz;
       cum += qc;
       if (qc > 0.f) {
         last = c;
@@ -892,22 +894,30 @@ struct VerifySmem {
 // from the residual max(0, p - q): a chunk's mass loses min(p, q) of each candidate in it,
 // and a candidate's weight is scaled by max(0, 1 - q/p). Without one the proposal is the
 // path itself (q = 1 on x_t).
-// Statistics of target row `row` (max, argmax, log of the sum of exp), by one warp.
-// The statistics of target row `row` (b = row / L, n = row % L) for the request's last block:
-// dst[0..2] = max, argmax bits, log-sum-exp; at T > 0 also dst[3] = the acceptance uniform of
-// the draft the row verifies (n < L - 1) and dst[4] = the row's redraw uniform (both at
-// counter position n + 1), so that the last block draws no Philox numbers itself.
+// The statistics of target row `row` (b = row / L, n = row % L) for the request's last block,
+// by one warp: dst[0..2] = max, argmax bits, log-sum-exp; at T > 0 also dst[3] = the
+// acceptance uniform of the draft the row verifies (n < L - 1), dst[4] = the row's redraw
+// uniform and, for the drawn paths (modes 2 and 3), dst[5] = the path uniform of position
+// n + 1 (n < L - 1), all at counter position n + 1, so that the last block draws no Philox
+// numbers itself.
 __device__ void row_stat_publish(const TailLaunch& a, int row, float* dst) {
   const RowStat st = row_stat_warp(a, row);
-  if ((threadIdx.x & 31) == 0) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
     dst[0] = st.m;
     dst[1] = __int_as_float(st.i);
     dst[2] = a.T > 0.f ? logf(st.s) : 0.f;
-    if (a.T > 0.f) {
-      const int b = row / a.L, n = row - b * a.L;
-      dst[3] = n < a.L - 1 ? uniform_accept(a.seed, b, n + 1) : 0.f;
-      dst[4] = uniform_redraw(a.seed, b, n + 1);
-    }
+  }
+  if (a.T > 0.f && lane < 3) {
+    // lanes 0, 1, 2 side by side: the acceptance uniform (stream 0), the redraw uniform
+    // (stream 1) and, for the drawn paths, the path uniform (stream 3) of position n + 1
+    const int b = row / a.L, n = row - b * a.L;
+    const bool drafted = n < a.L - 1;  // the bonus row verifies no draft and draws no path
+    const bool drawn = a.path_mode == 2 || a.path_mode == 3;
+    const float u = uniform_stream(a.seed, b, n + 1, lane == 2 ? 3ull : static_cast<uint64_t>(lane));
+    if (lane == 0) dst[3] = drafted ? u : 0.f;
+    if (lane == 1) dst[4] = u;
+    if (lane == 2) dst[5] = drafted && drawn ? u : 0.f;
   }
 }
 
@@ -1155,7 +1165,6 @@ struct TailSmem {
   VerifySmem* vs;
   float* qprop;                  // sampled traversal: [P][16] proposal distributions
   float* sdraw;                  // [P][16] score of the drawn successor of each (p, a)
-  float* upath;                  // [P] path-draw uniforms
   float* logb;                   // joint path draw: [P][16] backward messages (log beta)
   int* pidx;                     // [16] drawn candidate indices
   float* rstat;                  // [L][8] the request's published row statistics and uniforms
@@ -1176,7 +1185,7 @@ __host__ __device__ inline size_t tail_smem_bytes(int G, int r) {
   n += kMaxL * kK + 16 + 144 + 80 + 16;
   n += sizeof(VerifySmem) + 16;
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
-  n += static_cast<size_t>(kMaxL) * kK * 4 + 16 + kMaxL * 4 + 16;
+  n += static_cast<size_t>(kMaxL) * kK * 4 + 16;
   n += static_cast<size_t>(kMaxL) * kK * 4 + 16;
   n += kMaxL * 32 + 16 + kMaxL * kK * 4 + 16;
   n += sizeof(MergeSmem) + 16;
@@ -1214,7 +1223,6 @@ __device__ TailSmem carve(uint8_t* base, int G, int r) {
   s.qprop = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
   s.pidx = reinterpret_cast<int*>(take(kMaxL * 4));
   s.sdraw = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
-  s.upath = reinterpret_cast<float*>(take(kMaxL * 4));
   s.logb = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxL) * kK * 4));
   s.rstat = reinterpret_cast<float*>(take(kMaxL * 32));
   s.zc_all = reinterpret_cast<float*>(take(kMaxL * kK * 4));
@@ -1310,8 +1318,8 @@ __device__ void finish_request(const TailLaunch& a, const TailSmem& sm, int b) {
   } else if (sampled) {
     const float inv_T = 1.0f / a.T;
     if (a.path_mode == 3) backward_messages_block(sm.S_all, P, inv_T, sm.logb);
-    const float score = path_sample_block(sm.S_all, sm.ids_all, P, inv_T, a.seed, b,
-                                          sm.path_tok, sm.pidx, sm.qprop, sm.sdraw, sm.upath, sm.bp,
+    const float score = path_sample_block(sm.S_all, sm.ids_all, P, inv_T, sm.rstat, sm.path_tok,
+                                          sm.pidx, sm.qprop, sm.sdraw, sm.bp,
                                           a.path_mode == 3 ? sm.logb : nullptr);
     if (threadIdx.x < P) a.path[static_cast<size_t>(b) * P + threadIdx.x] = sm.path_tok[threadIdx.x];
     if (threadIdx.x == 0 && a.path_score) a.path_score[b] = score;
