@@ -186,3 +186,51 @@ def test_fused_candidates_logits_increasing_with_id(lib, B, variant, monkeypatch
     want = _ramp_expected(V)
     for i in range(ids.shape[0]):
         assert ids[i].tolist() == want, f"row {i}"
+
+
+@pytest.mark.parametrize("mode", [binding.DFS_PATH_GREEDY, binding.DFS_PATH_VITERBI])
+@pytest.mark.parametrize("B,L,V,variant", [(4, 8, 5000, "0"), (32, 8, 151936, "5")])
+def test_fused_path_ties_go_to_the_lower_id(lib, orc, B, L, V, variant, mode, monkeypatch):
+    """Exact ties in the path choice of the fused call: with A = 0 every pair score is the
+    successor's logit, S_t(a, c) = U_t(c) (exactly, on the GPU and in the oracle), and the
+    planted logits tie the two best candidates of every position (e = 4). The greedy
+    traversal's successor ties, and Viterbi's predecessor ties and final choice, must all go
+    to the lower token id: the path is that token at every position. Compared with the
+    oracle's path (its tie rule is pinned on the CPU) and its verification, request by
+    request, with no near-tie exclusion."""
+    monkeypatch.setenv("DFS_LMHEAD_VARIANT", variant)
+    d, r = 256, 16
+    h, W, hot = _tie_inputs(B, L, V, d, seed=23 + B)
+    low4 = min(int(v) for v, e in zip(hot.tolist(), EXPONENTS) if e == 4)
+    g = torch.Generator().manual_seed(19)
+    Wg = (torch.randn(r, d, generator=g) / math.sqrt(d)).to(torch.bfloat16)
+    A = torch.zeros(V, r, dtype=torch.bfloat16)
+    Bt = (torch.randn(V, r, generator=g) / math.sqrt(r)).to(torch.bfloat16)
+    x0 = torch.randint(0, V, (B,), generator=g, dtype=torch.int32)
+    Z = torch.randn(B, L, V, generator=g).to(torch.bfloat16)
+    dims = binding.make_dims(B, L, V, d, r, binding.DFS_BF16, binding.DFS_BF16)
+    ws = binding.alloc_workspace(dims)
+    res = binding.dfs_select_verify(dims, h.cuda(), W.cuda(), Wg.cuda(), A.cuda(), Bt.cuda(),
+                                    x0.cuda(), Z.cuda(), mode, 0.0, 1, ws, want_intermediates=True)
+    torch.cuda.synchronize()
+    assert binding.dfs_get_device_error(ws) == binding.DFS_OK
+    path, out, acc = to_cpu(res["path"]), to_cpu(res["out_tokens"]), to_cpu(res["accept_len"])
+    cand_U = to_cpu(res["cand_U"]).reshape(B, L - 1, 16)
+    assert np.all(cand_U[:, :, 0] == cand_U[:, :, 1])  # the planted tie reached the tail
+    npd = {k: wl.to_numpy_bits(v) for k, v in (("h", h), ("W", W), ("Wg", Wg), ("A", A),
+                                                 ("Bt", Bt), ("Z", Z))}
+    rows = np.array([b * L + t for b in range(B) for t in range(1, L)])
+    o_ids, o_U, _ = orc.topk(orc.logits(npd["h"], npd["W"], rows), 16)
+    o_g = orc.gate(npd["h"], npd["Wg"], rows)
+    fn = orc.path_viterbi if mode == binding.DFS_PATH_VITERBI else orc.path_greedy
+    for b in range(B):
+        sl = slice(b * (L - 1), (b + 1) * (L - 1))
+        ids = o_ids[sl].reshape(L - 1, 16)
+        S = orc.pair_scores(npd["A"], npd["Bt"], ids, o_U[sl].reshape(L - 1, 16),
+                            o_g[sl].reshape(L - 1, -1), int(x0[b]))
+        assert np.array_equal(S, np.broadcast_to(o_U[sl].reshape(L - 1, 1, 16), S.shape))
+        o_path, _, o_score, _ = fn(S, ids)
+        assert o_path.tolist() == [low4] * (L - 1), f"request {b}: oracle path"
+        assert path[b].tolist() == [low4] * (L - 1), f"request {b}: path {path[b].tolist()}"
+        o_out, o_acc = orc.verify_greedy(npd["Z"][b], o_path)
+        assert acc[b] == o_acc and out[b].tolist() == o_out.tolist(), f"request {b}: verify"
