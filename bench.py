@@ -468,7 +468,10 @@ def run_ours(args):
     copied = [[torch.cuda.Event() for _ in copy_streams] for _ in range(nbuf)]
     freed = [torch.cuda.Event() for _ in range(nbuf)]  # the step using a set has read it
     B2 = spec.B // 2
-    K_e2e = max(10, args.steps // 2)
+    # at least 50 steps: the first step's copies cannot overlap a previous step (no copy of
+    # the timed steps starts before the timed region), and over a handful of steps that one
+    # exposed copy would stand for the leg's steady state
+    K_e2e = max(50, args.steps // 2)
 
     def issue_copies(i):
         k = i % nbuf
