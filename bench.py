@@ -229,8 +229,35 @@ def run_ours(args):
         binding.dfs_set_trace_events(None, None)
         replicas.barrier()
         ms = e0.elapsed_time(e1) / K
-        lm = statistics.mean(a.elapsed_time(b) for a, b in tr) if trace else None
+        lm = [a.elapsed_time(b) for a, b in tr] if trace else None
         return ms, lm, n1 - n0
+
+    def per_call(T, K, W, path_mode=None):
+        """Per-call durations: events around each call. The event between two calls stops
+        the second launching early (no programmatic overlap), so each call pays its own
+        launch; used for the spread, not the headline."""
+        for i in range(W):
+            step(i, T, path_mode=path_mode)
+        torch.cuda.synchronize()
+        replicas.barrier()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        for i in range(K):
+            evs[i][0].record(stream)
+            step(W + i, T, path_mode=path_mode)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        replicas.barrier()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def spread(xs):
+        q = sorted(xs)
+
+        def pct(f):  # nearest rank
+            return q[min(len(q) - 1, max(0, math.ceil(f * len(q)) - 1))]
+        return {"median_ms": round(statistics.median(q), 4), "p10_ms": round(pct(0.1), 4),
+                "p90_ms": round(pct(0.9), 4), "n": len(q)}
 
     uuid = None
     try:
@@ -264,7 +291,8 @@ def run_ours(args):
             clk["sm_kcycles_per_step"] = round(ms_greedy * clk["sm_mhz"], 1)
     # the dominant kernel's own duration, from events recorded around it on its stream (a
     # separate pass: an event between two kernels stops the second launching early)
-    _, lm_ms, _ = timed(0.0, args.steps, 1, trace=True)
+    _, lm_list, _ = timed(0.0, args.steps, 1, trace=True)
+    lm_ms = statistics.mean(lm_list)
     assert binding.dfs_get_device_error(ws) == binding.DFS_OK
     accept = outs[2].float().mean().item()
     ms_samp, _, _ = timed(args.sampling_temperature, max(10, args.steps // 2), args.warmup)
@@ -279,6 +307,13 @@ def run_ours(args):
     ms_joint, _, _ = timed(args.sampling_temperature, max(10, args.steps // 2), args.warmup,
                            path_mode=binding.DFS_PATH_SAMPLE_JOINT)
     accept_joint = outs[2].float().mean().item()
+    # the other path mode at both temperatures (the headline's is the greedy traversal)
+    other = binding.DFS_PATH_GREEDY if mode == binding.DFS_PATH_VITERBI else binding.DFS_PATH_VITERBI
+    ms_other0, _, _ = timed(0.0, max(10, args.steps // 2), args.warmup, path_mode=other)
+    ms_other_s, _, _ = timed(args.sampling_temperature, max(10, args.steps // 2), args.warmup,
+                             path_mode=other)
+    # the spread of single calls (greedy headline mode, T = 0)
+    call_ms = per_call(0.0, max(20, args.steps // 4), args.warmup)
 
     # the same step with the LM head given quantised to E4M3 (one power-of-two scale per
     # vocabulary entry; rows quantised per call): half the LM-head bytes
@@ -524,6 +559,8 @@ def run_ours(args):
     value_samp = replicas.job_throughput(spec.B, ms_samp / 1e3)
     value_prop = replicas.job_throughput(spec.B, ms_prop / 1e3)
     value_joint = replicas.job_throughput(spec.B, ms_joint / 1e3)
+    value_other0 = replicas.job_throughput(spec.B, ms_other0 / 1e3)
+    value_other_s = replicas.job_throughput(spec.B, ms_other_s / 1e3)
     value_graph = replicas.job_throughput(spec.B, ms_graph / 1e3)
     value_q = replicas.job_throughput(spec.B, ms_q / 1e3)
     q_bytes = spec.d * spec.V + spec.B * spec.L * spec.V * 2  # E4M3 head + target logits
@@ -600,6 +637,18 @@ def run_ours(args):
                          "joint_path": {"value": round(value_joint, 1), "unit": UNIT,
                                         "ms_per_step": round(ms_joint, 4),
                                         "mean_accept_len": round(accept_joint, 3)}},
+            "other_path_mode": {
+                "path": "greedy" if other == binding.DFS_PATH_GREEDY else "viterbi",
+                "T0": {"value": round(value_other0, 1), "unit": UNIT,
+                       "ms_per_step": round(ms_other0, 4)},
+                f"T{args.sampling_temperature:g}": {"value": round(value_other_s, 1),
+                                                    "unit": UNIT,
+                                                    "ms_per_step": round(ms_other_s, 4)}},
+            "spread": {
+                "per_call": {**spread(call_ms),
+                             "note": "events around each greedy T=0 call: no programmatic "
+                                     "overlap with the previous call, so each pays its launch"},
+                "lmhead_per_launch": spread(lm_list)},
             "e4m3_head": {"value": round(value_q, 1), "unit": UNIT,
                           "ms_per_step": round(ms_q, 4),
                           "hbm_roofline_frac_step": round(q_bytes / (ms_q * 1e-3) / 1e9 /
