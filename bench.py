@@ -180,7 +180,7 @@ def run_ours(args):
 
     spec = wl.WORKLOADS[args.workload]
     data = wl.generate(spec.with_(seed=spec.seed + 1000 * rank), dev)
-    nrot = 4  # rotate target-logit / hidden buffers so no step rereads an L2-resident copy
+    nrot = 3  # rotate target-logit / hidden buffers so no step rereads an L2-resident copy
     Zs = [data["Z"]] + [wl.fresh_targets(data, 100 + i) for i in range(1, nrot)]
     hs = [data["h"]] + [data["h"].clone() for _ in range(1, nrot)]
     dims = binding.make_dims(spec.B, spec.L, spec.V, spec.d, spec.r, binding.DFS_BF16,
